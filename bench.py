@@ -1,0 +1,329 @@
+#!/usr/bin/env python3
+"""Benchmark of the forward 2-D convolution on one or more GB300 GPUs.
+
+One step = one conv2d_fwd call over a full batch of the workload: argument
+checks, filter repack, input transform (window tensor or channels-last copy,
+per the chosen algorithm), the contraction kernel and its epilogue.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--dtype DT]
+                  [--algo A] [--impl reference]
+
+Prints ONE JSON line (rank 0).  Default workload: the ResNet stage-1 layer
+(N=32, Cin=64, 56x56, Cout=64, 3x3, stride 1, pad 1) in fp16 with fp32
+accumulation.  Timing: CUDA events on the launching stream, one event pair
+per step, L2 flushed (a 512 MiB write) before every timed step and outside
+its events; W untimed warm-up steps; barrier + synchronize around the timed
+region; max over ranks.  Multi-GPU runs are independent batches per rank
+(weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "conv fwd TFLOP/s (2*N*Cout*Ho*Wo*Cin*Kh*Kw/t), % of roofline, workspace MB"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "sm_max_mhz": 2070.0}, "fallback"
+
+
+def fp32_alu_peak_tflops(sm_count: int, mhz: float) -> float:
+    """FFMA peak: SMs x 128 fp32 lanes x 2 FLOP x clock."""
+    return sm_count * 128 * 2 * mhz * 1e6 / 1e12
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, fl in rows for i, v in enumerate(fl) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_oracle_baseline(wl, dtype, budget_s=12.0, threads=None):
+    """Time the fp64 oracle (as it stands) on host threads over a bounded
+    sample of the workload: whole (n, co) output planes, enough of them for
+    about ``budget_s`` seconds.  Returns a cpu_baseline dict in TFLOP/s."""
+    import concurrent.futures as cf
+    from oracle import ref
+    threads = threads or (os.cpu_count() or 1)
+    d = synth.make_inputs(wl, dtype, N=1)
+    X64, W64 = d["X64"], d["W64"]
+    Ho, Wo = wl.out_hw()
+    Y = np.empty((1, wl.Co, Ho, Wo))
+    S = np.empty_like(Y)
+    plane_flops = 2 * Ho * Wo * wl.Ci * wl.Kh * wl.Kw
+    t0 = time.perf_counter()
+    ref.conv2d_slice(X64, W64, Y, S, wl.stride, wl.pad, 0, 1, 0, 1)
+    t_plane = max(time.perf_counter() - t0, 1e-6)
+    planes = int(min(wl.Co, max(1, budget_s * threads / t_plane)))   # image 0's channels
+    jobs = list(range(planes))
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(threads) as ex:
+        list(ex.map(lambda co: ref.conv2d_slice(X64, W64, Y, S, wl.stride, wl.pad, 0, 1, co, co + 1), jobs))
+    dt = time.perf_counter() - t0
+    flops = planes * plane_flops
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{planes} output planes (image 0, channels 0..{planes - 1}) of {wl.name}, "
+                      f"{flops / 1e9:.2f} GFLOP in {dt:.2f} s, fp64 7-loop"}
+
+
+def _workload(args):
+    wl = synth.WORKLOADS[args.workload]
+    dtype = args.dtype or wl.dtypes[0]
+    return wl, dtype
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the oracle on the host cores, a bounded sample per step."""
+    wl, dtype = _workload(args)
+    if rank != 0:
+        return
+    # Each step times a bounded sample; the whole run stays within ~2 minutes.
+    per_step = min(3.0, 120.0 / (args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_oracle_baseline(wl, dtype, budget_s=per_step / 4)
+    samples = [cpu_oracle_baseline(wl, dtype, budget_s=per_step) for _ in range(args.steps)]
+    vals = [s["value"] for s in samples]
+    v = statistics.median(vals)
+    step_ms = wl.flops() / (v * 1e12) * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "N": wl.N, "Cin": wl.Ci, "H": wl.H, "W": wl.W, "Cout": wl.Co,
+                       "Kh": wl.Kh, "Kw": wl.Kw, "stride": wl.stride, "pad": wl.pad, "input_dtype": dtype},
+            "cpu_baseline": {**samples[0], "value": v},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args, rank, world):
+    import torch
+    import torch.distributed as dist
+    from dense_convolution_gb300 import build, capi
+    from dense_convolution_gb300.conv import Conv2d
+
+    build.build()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    wl, dtype = _workload(args)
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+
+    d = synth.make_inputs(wl, dtype)
+    xh = (torch.from_numpy(d["X"]) if dtype != "bf16" else d["X"]).contiguous().pin_memory()
+    wh = (torch.from_numpy(d["W"]) if dtype != "bf16" else d["W"]).contiguous().pin_memory()
+    op = Conv2d(wl.N, wl.Ci, wl.H, wl.W, wl.Co, wl.Kh, wl.Kw, wl.stride, wl.pad, dtype, args.algo)
+    x = xh.to(dev)
+    w = wh.to(dev)
+    y = op.alloc_output(dev)
+    ws = op.alloc_workspace(dev)
+    yh = torch.empty(y.shape, dtype=tdt, pin_memory=True)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    launches = capi.conv2d_launches_per_call(op.desc)
+
+    def step(ev0=None, ev1=None):
+        if ev0 is None:
+            capi.conv2d_fwd(op.desc, x.data_ptr(), w.data_ptr(), y.data_ptr(), ws.data_ptr(), ws.numel(), sp)
+        else:
+            capi.conv2d_fwd_profiled(op.desc, x.data_ptr(), w.data_ptr(), y.data_ptr(), ws.data_ptr(),
+                                     ws.numel(), sp, ev0.cuda_event, ev1.cuda_event)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    assert capi.conv2d_device_status(sp) == 0
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in kev:          # materialise the raw events before handing them to the library
+        a.record(stream)
+        b.record(stream)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(K):
+            flush.fill_(1)
+            ev[i][0].record(stream)
+            step(*kev[i])
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        # Keep the GPU busy long enough for the clock sampler to see the load.
+        t_end = time.perf_counter() + 0.4
+        while time.perf_counter() < t_end:
+            for _ in range(20):
+                step()
+            torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    assert capi.conv2d_device_status(sp) == 0
+    ms = sum(step_ms) / K
+    kms = sum(kern_ms) / K
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # End to end through the public API: pinned host X and W in, Y out, every step.
+    e2e_ms = []
+    for i in range(max(3, min(K, 50))):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.fill_(1)
+        e0.record(stream)
+        x.copy_(xh, non_blocking=True)
+        w.copy_(wh, non_blocking=True)
+        step()
+        yh.copy_(y, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e = sum(e2e_ms[1:]) / max(1, len(e2e_ms) - 1)
+    if world > 1:
+        t = torch.tensor([e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e = float(t.item())
+
+    flops = wl.flops()
+    value = flops * world / (ms * 1e-3) / 1e12
+    peaks, src = _peaks()
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    if dtype == "f32":
+        peak = fp32_alu_peak_tflops(sm_count, peaks.get("sm_max_mhz", 2070.0))
+        bound, psrc = "alu", "derived: SMs x 128 FFMA lanes x 2 x max SM clock"
+    else:
+        peak = peaks["bf16_tflops"]
+        bound, psrc = "tensor", f"{src} bf16 dense burst (fp16 rate equal)"
+    achieved = flops / (kms * 1e-3) / 1e12
+    clocks = clk.summary()
+    elem = 4 if dtype == "f32" else 2
+    Ho, Wo = wl.out_hw()
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "N": wl.N, "Cin": wl.Ci, "H": wl.H, "W": wl.W, "Cout": wl.Co,
+                   "Kh": wl.Kh, "Kw": wl.Kw, "stride": wl.stride, "pad": wl.pad, "algo": op.algo,
+                   "accumulate": "f32", "l2": "flushed before every timed step (512 MiB write)",
+                   "workspace_mb": op.workspace_bytes / 2 ** 20,
+                   "im2win_tensor_mb": wl.N * wl.Ci * Ho * (wl.W + 2 * wl.pad) * wl.Kh * elem / 2 ** 20,
+                   "parallelism": f"independent batch per GPU x{world}"},
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": "contraction kernel",
+                     "kernel_ms": kms, "peak_source": psrc,
+                     "step_frac": (flops / (ms * 1e-3) / 1e12) / peak},
+        "gpu_launches": launches * K,
+        "e2e": {"value": flops * world / (e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": xh.numel() * xh.element_size() + wh.numel() * wh.element_size(),
+                "d2h_bytes_per_step": yh.numel() * yh.element_size(), "ms_per_step": e2e},
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_baseline(wl, dtype)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="resnet_stage1", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--dtype", default=None, choices=list(synth.DTYPES))
+    ap.add_argument("--algo", default="auto")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl != "reference":
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    if world > 1 and args.impl != "reference":
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world)
+    if world > 1 and args.impl != "reference":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,278 @@
+// C ABI: descriptor creation and validation, per-shape algorithm choice,
+// workspace layout and the launch sequence of conv2d_fwd.  Host code only;
+// the kernels live in transforms.cu, conv_fp32.cu and conv_tc.cu.
+#include <new>
+#include <stdint.h>
+#include <string.h>
+
+#include "internal.h"
+
+#define CONV2D_API extern "C" __attribute__((visibility("default")))
+
+using namespace conv2d_gb300;
+
+namespace {
+
+constexpr long long kMaxElems = 0x7fffffffLL;   // kernels index tensors with 32-bit element counts
+
+bool is_tc(conv2d_algo a) { return a == CONV2D_ALGO_IM2WIN_TC || a == CONV2D_ALGO_IMPLICIT_TC; }
+
+// Fraction of the tensor-core K extent that holds real filter taps, for the
+// two operand sources (the rest is zero fill up to the 64-element chunk).
+double tc_k_efficiency(const conv2d_desc& d, bool im2win) {
+    const long long ci8 = (d.Ci + 7) / 8 * 8;
+    const long long chunk = im2win ? (long long)d.Kh * ci8 : ci8;
+    const long long padded = (chunk + kTcBlockK - 1) / kTcBlockK * kTcBlockK;
+    return (double)(im2win ? (long long)d.Kh * d.Ci : d.Ci) / (double)padded;
+}
+
+// Shape limits of the tensor-core kernels (im2col-mode TMA corners are 8-bit
+// signed for a 4-D map; channel pitch must be a 16-byte multiple).
+bool tc_shape_ok(const conv2d_desc& d, bool im2win) {
+    if (im2win) {
+        if (d.Kw - 1 > 128) return false;
+    } else {
+        if (d.p > 128 || d.p - (d.Kw - 1) < -128 || d.p - (d.Kh - 1) < -128) return false;
+        if (d.p - (d.Kw - 1) > 127 || d.p - (d.Kh - 1) > 127) return false;
+        if (d.layout == CONV2D_LAYOUT_NHWC && d.Ci % 8 != 0) return false;
+    }
+    if (d.Kh > 0xffff || d.Kw > 0xffff) return false;
+    return true;
+}
+
+// Recorded per-shape choice.  fp32: the im2win strips (the method of the
+// im2win paper) unless the row width keeps the direct staging off 16-byte
+// boundaries.  16-bit: the operand source that wastes less of the 64-wide K
+// chunk; ties go to the implicit path, which needs less workspace.
+conv2d_algo resolve_auto(const conv2d_desc& d) {
+    if (d.dtype == CONV2D_F32) return CONV2D_ALGO_IM2WIN_FP32_CC;
+    if (d.layout == CONV2D_LAYOUT_NHWC) return CONV2D_ALGO_IMPLICIT_TC;
+    const bool imp_ok = tc_shape_ok(d, false), win_ok = tc_shape_ok(d, true);
+    if (imp_ok && (!win_ok || tc_k_efficiency(d, false) >= tc_k_efficiency(d, true)))
+        return CONV2D_ALGO_IMPLICIT_TC;
+    return CONV2D_ALGO_IM2WIN_TC;
+}
+
+conv2d_status finalize(conv2d_desc& d) {
+    d.algo = d.requested == CONV2D_ALGO_AUTO ? resolve_auto(d) : d.requested;
+    const bool tc = is_tc(d.algo);
+    if (tc != (d.dtype != CONV2D_F32)) return CONV2D_ERR_BAD_PARAM;
+    if (d.layout == CONV2D_LAYOUT_NHWC && d.algo != CONV2D_ALGO_IMPLICIT_TC) return CONV2D_ERR_UNSUPPORTED;
+    d.ws_weights = d.ws_input = d.ws_input_off = d.ws_total = 0;
+    if (!tc) {
+        d.Lp = (d.Wp * d.Kh + 3) & ~3;
+        d.cc_wpt = d.Wo <= 32 ? 1 : (d.Wo <= 64 ? 2 : 4);
+        int warps = (d.Co + 15) / 16;
+        if (warps > 8) warps = 8;
+        while (warps > 1 && (long long)d.Kh * d.Kw * 16 * warps * 4 > 64 * 1024) --warps;
+        d.cc_warps = warps;
+        if ((long long)d.Kh * d.Kw * 16 * 4 > 96 * 1024) return CONV2D_ERR_UNSUPPORTED;
+        const long long bco = 16LL * warps, ncb = (d.Co + bco - 1) / bco;
+        d.ws_weights = (size_t)(ncb * bco * d.Ci * d.Kh * d.Kw * 4);
+        if (d.algo == CONV2D_ALGO_IM2WIN_FP32_CC) {
+            const long long strips = (long long)d.N * d.Ci * d.Ho * d.Lp;
+            if (strips > kMaxElems * 4) return CONV2D_ERR_UNSUPPORTED;
+            d.ws_input = (size_t)strips * 4;
+        } else {
+            if (d.W % 4 != 0) return CONV2D_ERR_UNSUPPORTED;    // 16-byte row pitch for the row copies
+            if (d.Kh > 256) return CONV2D_ERR_UNSUPPORTED;
+            if ((256 - 3 - d.Kw) / d.s + 1 < 1 || d.Kw > 250) return CONV2D_ERR_UNSUPPORTED;
+        }
+    } else {
+        const bool im2win = d.algo == CONV2D_ALGO_IM2WIN_TC;
+        if (!tc_shape_ok(d, im2win)) return CONV2D_ERR_UNSUPPORTED;
+        d.Ci8 = (d.Ci + 7) / 8 * 8;
+        d.taps = im2win ? d.Kw : d.Kh * d.Kw;
+        const long long chunk = im2win ? (long long)d.Kh * d.Ci8 : d.Ci8;
+        d.CP = (int)((chunk + kTcBlockK - 1) / kTcBlockK * kTcBlockK);
+        d.BN = d.Co <= 64 ? 64 : (d.Co <= 128 ? 128 : 256);
+        const long long wq = (long long)d.Co * d.taps * d.CP;
+        if (wq > kMaxElems) return CONV2D_ERR_UNSUPPORTED;
+        d.ws_weights = (size_t)wq * 2;
+        if (im2win) {
+            const long long win = (long long)d.N * d.Ho * d.Wp * d.Kh * d.Ci8;
+            if (win > kMaxElems * 4) return CONV2D_ERR_UNSUPPORTED;
+            d.ws_input = (size_t)win * 2;
+        } else if (d.layout == CONV2D_LAYOUT_NCHW) {
+            d.ws_input = (size_t)((long long)d.N * d.H * d.W * d.Ci8) * 2;
+        }
+    }
+    d.ws_input_off = d.ws_input ? align_up(d.ws_weights, 1024) : 0;
+    d.ws_total = d.ws_input ? d.ws_input_off + d.ws_input : d.ws_weights;
+    return CONV2D_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+CONV2D_API conv2d_status conv2d_desc_create(conv2d_desc_t* out, int N, int Cin, int H, int W, int Cout, int Kh,
+                                            int Kw, int stride, int pad, conv2d_dtype dtype, conv2d_algo algo) {
+    if (!out) return CONV2D_ERR_NULL_PTR;
+    *out = nullptr;
+    if (N < 1 || Cin < 1 || H < 1 || W < 1 || Cout < 1 || Kh < 1 || Kw < 1 || stride < 1 || pad < 0)
+        return CONV2D_ERR_BAD_PARAM;
+    if (dtype != CONV2D_F32 && dtype != CONV2D_F16 && dtype != CONV2D_BF16) return CONV2D_ERR_BAD_PARAM;
+    if (algo < CONV2D_ALGO_AUTO || algo > CONV2D_ALGO_IMPLICIT_FP32_CC) return CONV2D_ERR_BAD_PARAM;
+    const long long Hp = (long long)H + 2LL * pad, Wp = (long long)W + 2LL * pad;
+    if (Hp < Kh || Wp < Kw || Wp > 0x7fffffffLL) return CONV2D_ERR_BAD_PARAM;
+    const long long Ho = (Hp - Kh) / stride + 1, Wo = (Wp - Kw) / stride + 1;
+    if ((long long)N * Cin * H * W > kMaxElems || (long long)N * Cout * Ho * Wo > kMaxElems ||
+        (long long)Cout * Cin * Kh * Kw > kMaxElems)
+        return CONV2D_ERR_BAD_PARAM;
+    conv2d_desc d{};
+    d.N = N; d.Ci = Cin; d.H = H; d.W = W; d.Co = Cout; d.Kh = Kh; d.Kw = Kw; d.s = stride; d.p = pad;
+    d.dtype = dtype;
+    d.requested = algo;
+    d.layout = CONV2D_LAYOUT_NCHW;
+    d.Ho = (int)Ho; d.Wo = (int)Wo; d.Wp = (int)Wp;
+    conv2d_status st = finalize(d);
+    if (st != CONV2D_OK) return st;
+    conv2d_desc* h = new (std::nothrow) conv2d_desc(d);
+    if (!h) return CONV2D_ERR_BAD_PARAM;
+    *out = h;
+    return CONV2D_OK;
+}
+
+CONV2D_API conv2d_status conv2d_desc_set_input_layout(conv2d_desc_t d, conv2d_layout layout) {
+    if (!d) return CONV2D_ERR_NULL_PTR;
+    if (layout != CONV2D_LAYOUT_NCHW && layout != CONV2D_LAYOUT_NHWC) return CONV2D_ERR_BAD_PARAM;
+    conv2d_desc t = *d;
+    t.layout = layout;
+    conv2d_status st = finalize(t);
+    if (st != CONV2D_OK) return st;
+    *d = t;
+    return CONV2D_OK;
+}
+
+CONV2D_API conv2d_status conv2d_desc_destroy(conv2d_desc_t d) {
+    delete d;
+    return CONV2D_OK;
+}
+
+CONV2D_API conv2d_status conv2d_out_dims(conv2d_desc_t d, int* Ho, int* Wo) {
+    if (!d || !Ho || !Wo) return CONV2D_ERR_NULL_PTR;
+    *Ho = d->Ho;
+    *Wo = d->Wo;
+    return CONV2D_OK;
+}
+
+CONV2D_API conv2d_status conv2d_workspace_size(conv2d_desc_t d, size_t* bytes) {
+    if (!d || !bytes) return CONV2D_ERR_NULL_PTR;
+    *bytes = d->ws_total;
+    return CONV2D_OK;
+}
+
+CONV2D_API conv2d_status conv2d_get_algo(conv2d_desc_t d, conv2d_algo* chosen) {
+    if (!d || !chosen) return CONV2D_ERR_NULL_PTR;
+    *chosen = d->algo;
+    return CONV2D_OK;
+}
+
+namespace {
+
+// Records an optional event on the stream; false when the record fails.
+bool record(void* ev, cudaStream_t st) {
+    return !ev || cudaEventRecord(static_cast<cudaEvent_t>(ev), st) == cudaSuccess;
+}
+
+conv2d_status fwd_impl(conv2d_desc_t dp, const void* x, const void* w, void* y, void* workspace,
+                       size_t workspace_bytes, void* stream, void* ev0, void* ev1) {
+    if (!dp || !x || !w || !y) return CONV2D_ERR_NULL_PTR;
+    const conv2d_desc& d = *dp;
+    if (d.ws_total > 0 && !workspace) return CONV2D_ERR_NULL_PTR;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (workspace && !aligned16(workspace)))
+        return CONV2D_ERR_MISALIGNED;
+    if (workspace_bytes < d.ws_total) return CONV2D_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    void* wq = ws;
+    void* win = ws ? ws + d.ws_input_off : nullptr;
+    cudaError_t e = cudaSuccess;
+    conv2d_status s = CONV2D_OK;
+    switch (d.algo) {
+        case CONV2D_ALGO_IM2WIN_FP32_CC:
+            e = launch_pack_filter_f32(static_cast<const float*>(w), static_cast<float*>(wq), d, st);
+            if (e == cudaSuccess) e = launch_im2win_strips_f32(static_cast<const float*>(x), static_cast<float*>(win), d, st);
+            if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
+            if (e == cudaSuccess)
+                s = launch_conv_fp32(d, static_cast<const float*>(win), static_cast<const float*>(wq),
+                                     static_cast<float*>(y), true, st);
+            break;
+        case CONV2D_ALGO_IMPLICIT_FP32_CC:
+            e = launch_pack_filter_f32(static_cast<const float*>(w), static_cast<float*>(wq), d, st);
+            if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
+            if (e == cudaSuccess)
+                s = launch_conv_fp32(d, static_cast<const float*>(x), static_cast<const float*>(wq),
+                                     static_cast<float*>(y), false, st);
+            break;
+        case CONV2D_ALGO_IM2WIN_TC:
+            e = launch_pack_filter_tc(w, wq, d, true, st);
+            if (e == cudaSuccess) e = launch_window_cl16(x, win, d.N, d.Ci, d.H, d.W, d.Ci8, d.Ho, d.Wp, d.Kh, d.s, d.p, st);
+            if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
+            if (e == cudaSuccess) s = launch_conv_tc(d, win, wq, y, true, st);
+            break;
+        case CONV2D_ALGO_IMPLICIT_TC: {
+            e = launch_pack_filter_tc(w, wq, d, false, st);
+            const void* src = x;
+            if (e == cudaSuccess && d.layout == CONV2D_LAYOUT_NCHW) {
+                e = launch_window_cl16(x, win, d.N, d.Ci, d.H, d.W, d.Ci8, d.H, d.W, 1, 1, 0, st);
+                src = win;
+            }
+            if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
+            if (e == cudaSuccess) s = launch_conv_tc(d, src, wq, y, false, st);
+            break;
+        }
+        default:
+            return CONV2D_ERR_BAD_PARAM;
+    }
+    if (e != cudaSuccess) return CONV2D_ERR_CUDA;
+    if (s == CONV2D_OK && !record(ev1, st)) return CONV2D_ERR_CUDA;
+    return s;
+}
+
+}  // namespace
+
+CONV2D_API conv2d_status conv2d_fwd(conv2d_desc_t d, const void* x, const void* w, void* y, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+    return fwd_impl(d, x, w, y, workspace, workspace_bytes, stream, nullptr, nullptr);
+}
+
+CONV2D_API conv2d_status conv2d_fwd_profiled(conv2d_desc_t d, const void* x, const void* w, void* y,
+                                             void* workspace, size_t workspace_bytes, void* stream, void* ev_start,
+                                             void* ev_end) {
+    return fwd_impl(d, x, w, y, workspace, workspace_bytes, stream, ev_start, ev_end);
+}
+
+CONV2D_API conv2d_status conv2d_launches_per_call(conv2d_desc_t d, int* launches) {
+    if (!d || !launches) return CONV2D_ERR_NULL_PTR;
+    int n = 2;   // filter repack + contraction
+    if (d->algo == CONV2D_ALGO_IM2WIN_FP32_CC || d->algo == CONV2D_ALGO_IM2WIN_TC ||
+        (d->algo == CONV2D_ALGO_IMPLICIT_TC && d->layout == CONV2D_LAYOUT_NCHW))
+        ++n;
+    *launches = n;
+    return CONV2D_OK;
+}
+
+CONV2D_API conv2d_status conv2d_device_status(void* stream, uint32_t* code_out) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t a = 0, b = 0;
+    if (status_read_clear_tc(st, &a) != cudaSuccess || status_read_clear_fp32(st, &b) != cudaSuccess)
+        return CONV2D_ERR_CUDA;
+    if (code_out) *code_out = a | b;
+    return (a | b) ? CONV2D_ERR_DEVICE_TIMEOUT : CONV2D_OK;
+}
+
+CONV2D_API const char* conv2d_status_string(conv2d_status s) {
+    switch (s) {
+        case CONV2D_OK: return "ok";
+        case CONV2D_ERR_BAD_PARAM: return "bad parameter";
+        case CONV2D_ERR_UNSUPPORTED: return "unsupported shape or option";
+        case CONV2D_ERR_NULL_PTR: return "null pointer";
+        case CONV2D_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case CONV2D_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case CONV2D_ERR_CUDA: return "CUDA error";
+        case CONV2D_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}

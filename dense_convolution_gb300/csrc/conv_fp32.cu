@@ -1,0 +1,316 @@
+// fp32 convolution on CUDA cores (FFMA only; no TF32 anywhere).
+//
+// Work split: a block computes one output row (n, ho), a run of up to 32*WPT
+// output columns, and 16*warps output channels.  Lane l of every warp owns
+// the WPT consecutive columns wo0 + l*WPT + t, and 16 channels (one warp's
+// slice); accumulators are WPT x 16 registers.
+//
+// K loop: input channels in chunks staged in shared memory, double-buffered,
+// by the asynchronous copy engine (completion on an mbarrier):
+//   im2win mode  one 1-D bulk copy per channel of the Eq. (2) strip range the
+//                block's windows touch ("Enabling Memory-efficient Im2win
+//                Convolution ...", Sec. III-B/C: a window is a contiguous run
+//                of the strip, Kh elements per input column);
+//   direct mode  one 3-D tensor-map copy of the Kh input rows of the chunk,
+//                zero-filled outside the image (padding), x origin aligned
+//                down to 16 bytes.
+// plus one bulk copy of the chunk's repacked filter ([ci][kh][kw][16*warps]).
+//
+// Reuse across output columns: for each (channel, filter row) a lane loads
+// only its own WPT*s window columns and takes the Kw - s overlapping columns
+// its windows share with the next lanes by warp shuffle.
+#include <cuda.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace conv2d_gb300 {
+
+struct Fp32Params {
+    const float* src;   // im2win strips [N][Ci][Ho][Lp] or X [N][Ci][H][W]
+    const float* wq;    // packed filter
+    float* y;
+    int N, Ci, H, W, Co, Kh, Kw, s, p, Ho, Wo, Lp;
+    int BCO, n_cb, WB, n_wb, chunk, n_chunks;
+    int pitch;          // floats per channel of staged input (im2win), or Kh*boxw (direct)
+    int boxw;           // direct mode: staged row width (multiple of 4)
+    int xs_floats;      // staged-input floats per stage (including read slack)
+    int ws_floats;      // filter floats per stage
+};
+
+template <int KW, int S, int WPT, bool IM2WIN>
+__global__ void __launch_bounds__(256) conv_fp32_kernel(const Fp32Params prm,
+                                                        const __grid_constant__ CUtensorMap xmap) {
+    extern __shared__ uint8_t smem_raw[];
+    // Tensor-map copies need 128-byte aligned destinations.
+    float* smem = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    __shared__ __align__(8) uint64_t bars[2];
+    __shared__ int abort_flag;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    long long b = blockIdx.x;
+    const int cb = (int)(b % prm.n_cb); b /= prm.n_cb;
+    const int wb = (int)(b % prm.n_wb); b /= prm.n_wb;
+    const int ho = (int)(b % prm.Ho);
+    const int n = (int)(b / prm.Ho);
+    const int Kh = prm.Kh;
+    const int kw_n = KW > 0 ? KW : prm.Kw;
+    const int sd = S > 0 ? S : prm.s;
+    const int wo0 = wb * prm.WB;
+    const int KK = Kh * kw_n;
+    const int stage_floats = prm.xs_floats + prm.ws_floats;
+
+    // First staged strip element (im2win) / first staged column (direct).
+    const int e0 = IM2WIN ? ((wo0 * sd * Kh) & ~3) : 0;
+    int e1 = 0;
+    if (IM2WIN) {
+        e1 = ((wo0 + prm.WB - 1) * sd + kw_n) * Kh;
+        e1 = (e1 + 3) & ~3;
+        if (e1 > prm.Lp) e1 = prm.Lp;
+    }
+    const int xbase = IM2WIN ? 0 : ((wo0 * sd - prm.p) >= 0 ? ((wo0 * sd - prm.p) & ~3)
+                                                             : -(((prm.p - wo0 * sd) + 3) & ~3));
+
+    if (tid == 0) {
+        abort_flag = 0;
+        mbar_init(smem_addr(&bars[0]), 1);
+        mbar_init(smem_addr(&bars[1]), 1);
+        mbar_fence_init();
+        if (!IM2WIN) tma_prefetch_desc(&xmap);
+    }
+    __syncthreads();
+
+    auto issue = [&](int k) {
+        const int st = k & 1;
+        float* xs = smem + st * stage_floats;
+        float* ws = xs + prm.xs_floats;
+        const uint32_t bar = smem_addr(&bars[st]);
+        const int ci0 = k * prm.chunk;
+        const int nci = min(prm.chunk, prm.Ci - ci0);
+        const uint32_t wbytes = (uint32_t)(nci * KK * prm.BCO * 4);
+        if (IM2WIN) {
+            const uint32_t xbytes = (uint32_t)((e1 - e0) * 4);
+            mbar_arrive_expect_tx(bar, wbytes + xbytes * nci);
+            for (int c = 0; c < nci; ++c) {
+                const float* src = prm.src + (((long long)n * prm.Ci + ci0 + c) * prm.Ho + ho) * prm.Lp + e0;
+                bulk_load(smem_addr(xs + c * prm.pitch), src, xbytes, bar);
+            }
+        } else {
+            const uint32_t xbytes = (uint32_t)(prm.boxw * Kh * prm.chunk * 4);
+            mbar_arrive_expect_tx(bar, wbytes + xbytes);
+            tma_load_3d(smem_addr(xs), &xmap, bar, xbase, ho * sd - prm.p, n * prm.Ci + ci0);
+        }
+        bulk_load(smem_addr(ws), prm.wq + ((long long)cb * prm.Ci + ci0) * KK * prm.BCO, wbytes, bar);
+    };
+
+    float acc[WPT][16];
+#pragma unroll
+    for (int t = 0; t < WPT; ++t)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[t][j] = 0.f;
+
+    // Padded column of this lane's first window.
+    const int cl = (wo0 + lane * WPT) * sd;
+    constexpr int C = WPT * (S > 0 ? S : 1);
+    constexpr int WIN = KW > 0 ? (WPT - 1) * S + KW : 1;
+
+    if (tid == 0) issue(0);
+    bool ok = true;
+    for (int k = 0; k < prm.n_chunks; ++k) {
+        if (tid == 0 && k + 1 < prm.n_chunks) issue(k + 1);
+        if (!mbar_wait(smem_addr(&bars[k & 1]), (k >> 1) & 1, &abort_flag)) {
+            // Let a copy issued for the next chunk land before the CTA exits.
+            if (tid == 0 && k + 1 < prm.n_chunks) {
+                int dummy = 0;
+                mbar_wait(smem_addr(&bars[(k + 1) & 1]), ((k + 1) >> 1) & 1, &dummy);
+            }
+            ok = false;
+            break;
+        }
+        const float* xs = smem + (k & 1) * stage_floats;
+        const float* ws = xs + prm.xs_floats;
+        const int nci = min(prm.chunk, prm.Ci - k * prm.chunk);
+        for (int c = 0; c < nci; ++c) {
+            for (int kh = 0; kh < Kh; ++kh) {
+                // row[col * XSTR] = padded input value at column col of this filter row.
+                const float* row;
+                int xstr;
+                if (IM2WIN) { row = xs + c * prm.pitch + kh - e0; xstr = Kh; }
+                else        { row = xs + (c * Kh + kh) * prm.boxw - prm.p - xbase; xstr = 1; }
+                const float* wr = ws + ((c * Kh + kh) * kw_n) * prm.BCO + warp * 16;
+                if constexpr (KW > 0) {
+                    float v[WIN];
+#pragma unroll
+                    for (int j = 0; j < C; ++j) v[j] = row[(cl + j) * xstr];
+#pragma unroll
+                    for (int j = C; j < WIN; ++j) {
+                        float t = __shfl_down_sync(0xffffffffu, v[j % C], j / C);
+                        if (lane + j / C >= 32) t = row[(cl + j) * xstr];
+                        v[j] = t;
+                    }
+#pragma unroll
+                    for (int kw = 0; kw < KW; ++kw) {
+                        const float4* w4 = reinterpret_cast<const float4*>(wr + kw * prm.BCO);
+                        float wv[16];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            float4 f = w4[q];
+                            wv[4 * q] = f.x; wv[4 * q + 1] = f.y; wv[4 * q + 2] = f.z; wv[4 * q + 3] = f.w;
+                        }
+#pragma unroll
+                        for (int t = 0; t < WPT; ++t) {
+                            const float xv = v[t * S + kw];
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) acc[t][j] = fmaf(xv, wv[j], acc[t][j]);
+                        }
+                    }
+                } else {
+                    for (int kw = 0; kw < kw_n; ++kw) {
+                        const float4* w4 = reinterpret_cast<const float4*>(wr + kw * prm.BCO);
+                        float wv[16];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            float4 f = w4[q];
+                            wv[4 * q] = f.x; wv[4 * q + 1] = f.y; wv[4 * q + 2] = f.z; wv[4 * q + 3] = f.w;
+                        }
+#pragma unroll
+                        for (int t = 0; t < WPT; ++t) {
+                            const float xv = row[(cl + t * sd + kw) * xstr];
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) acc[t][j] = fmaf(xv, wv[j], acc[t][j]);
+                        }
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (!ok) return;
+
+    const int co_base = cb * prm.BCO + warp * 16;
+#pragma unroll
+    for (int t = 0; t < WPT; ++t) {
+        const int wo = wo0 + lane * WPT + t;
+        if (wo >= prm.Wo || wo >= wo0 + prm.WB) continue;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int co = co_base + j;
+            if (co < prm.Co) prm.y[(((long long)n * prm.Co + co) * prm.Ho + ho) * prm.Wo + wo] = acc[t][j];
+        }
+    }
+}
+
+// ---------------------------------------------------------------- host side
+cudaError_t status_read_clear_fp32(cudaStream_t st, uint32_t* out) { return status_read_clear(st, out); }
+
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+void* driver_entry(const char* name);   // conv_tc.cu
+
+template <int KW, int S, int WPT, bool IM2WIN>
+static cudaError_t launch_fp32_inst(const Fp32Params& prm, const CUtensorMap& map, int threads, size_t smem,
+                                    long long blocks, cudaStream_t st) {
+    auto kern = conv_fp32_kernel<KW, S, WPT, IM2WIN>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)blocks, threads, smem, st>>>(prm, map);
+    return cudaGetLastError();
+}
+
+template <int KW, int S, bool IM2WIN>
+static cudaError_t launch_fp32_wpt(int wpt, const Fp32Params& prm, const CUtensorMap& map, int threads,
+                                   size_t smem, long long blocks, cudaStream_t st) {
+    switch (wpt) {
+        case 1: return launch_fp32_inst<KW, S, 1, IM2WIN>(prm, map, threads, smem, blocks, st);
+        case 2: return launch_fp32_inst<KW, S, 2, IM2WIN>(prm, map, threads, smem, blocks, st);
+        default: return launch_fp32_inst<KW, S, 4, IM2WIN>(prm, map, threads, smem, blocks, st);
+    }
+}
+
+template <bool IM2WIN>
+static cudaError_t launch_fp32_shape(const conv2d_desc& d, const Fp32Params& prm, const CUtensorMap& map,
+                                     int threads, size_t smem, long long blocks, cudaStream_t st) {
+    const int w = d.cc_wpt;
+#define CONV2D_FP32_CASE(KW_, S_)                                                               \
+    if (d.Kw == KW_ && d.s == S_) return launch_fp32_wpt<KW_, S_, IM2WIN>(w, prm, map, threads, smem, blocks, st);
+    CONV2D_FP32_CASE(1, 1)
+    CONV2D_FP32_CASE(3, 1)
+    CONV2D_FP32_CASE(5, 1)
+    CONV2D_FP32_CASE(7, 1)
+    CONV2D_FP32_CASE(9, 1)
+    CONV2D_FP32_CASE(11, 1)
+    CONV2D_FP32_CASE(3, 2)
+    CONV2D_FP32_CASE(7, 2)
+#undef CONV2D_FP32_CASE
+    return launch_fp32_wpt<0, 0, IM2WIN>(w, prm, map, threads, smem, blocks, st);
+}
+
+conv2d_status launch_conv_fp32(const conv2d_desc& d, const float* src, const float* wq, float* y, bool im2win,
+                               cudaStream_t st) {
+    Fp32Params prm{};
+    prm.src = src; prm.wq = wq; prm.y = y;
+    prm.N = d.N; prm.Ci = d.Ci; prm.H = d.H; prm.W = d.W; prm.Co = d.Co; prm.Kh = d.Kh; prm.Kw = d.Kw;
+    prm.s = d.s; prm.p = d.p; prm.Ho = d.Ho; prm.Wo = d.Wo; prm.Lp = d.Lp;
+    prm.BCO = 16 * d.cc_warps;
+    prm.n_cb = (d.Co + prm.BCO - 1) / prm.BCO;
+    const int lanes_w = 32 * d.cc_wpt;
+    int WB = d.Wo < lanes_w ? d.Wo : lanes_w;
+    if (!im2win) {
+        const int maxwb = (256 - 3 - d.Kw) / d.s + 1;   // staged row width <= 256 (box limit)
+        if (WB > maxwb) WB = maxwb;
+    }
+    prm.WB = WB;
+    prm.n_wb = (d.Wo + WB - 1) / WB;
+    // Staged input per channel, with slack so that idle lanes read inside the buffer.
+    const int slack = lanes_w * d.s + d.Kw + 8;
+    int per_ci_x;
+    if (im2win) {
+        // Staged range [e0, e1) is rounded out to 16 bytes on both ends (+6 at most).
+        prm.pitch = ((((lanes_w - 1) * d.s + d.Kw) * d.Kh + 8) + 3) & ~3;
+        per_ci_x = prm.pitch;
+        prm.boxw = 0;
+    } else {
+        prm.boxw = (((WB - 1) * d.s + d.Kw + 3) + 3) & ~3;
+        prm.pitch = d.Kh * prm.boxw;
+        per_ci_x = prm.pitch;
+    }
+    const int per_ci_w = d.Kh * d.Kw * prm.BCO;
+    const int budget = 100 * 1024 / 4;   // floats per stage (two stages resident)
+    int chunk = budget / (per_ci_x + per_ci_w);
+    if (chunk < 1) chunk = 1;
+    if (chunk > d.Ci) chunk = d.Ci;
+    if (chunk > 32) chunk = 32;
+    if (!im2win && chunk * d.Kh > 256) chunk = 256 / d.Kh;
+    if (chunk < 1) return CONV2D_ERR_UNSUPPORTED;
+    prm.chunk = chunk;
+    prm.n_chunks = (d.Ci + chunk - 1) / chunk;
+    prm.xs_floats = ((chunk * per_ci_x + slack) + 31) & ~31;
+    prm.ws_floats = (chunk * per_ci_w + 31) & ~31;
+    const size_t smem = (size_t)2 * (prm.xs_floats + prm.ws_floats) * 4 + 128;
+    if (smem > 220 * 1024) return CONV2D_ERR_UNSUPPORTED;
+
+    CUtensorMap map;
+    memset(&map, 0, sizeof(map));
+    if (!im2win) {
+        auto enc = reinterpret_cast<PFN_encodeTiled>(driver_entry("cuTensorMapEncodeTiled"));
+        if (!enc) return CONV2D_ERR_CUDA;
+        cuuint64_t dims[3] = {(cuuint64_t)d.W, (cuuint64_t)d.H, (cuuint64_t)d.N * d.Ci};
+        cuuint64_t strides[2] = {(cuuint64_t)d.W * 4, (cuuint64_t)d.W * d.H * 4};
+        cuuint32_t box[3] = {(cuuint32_t)prm.boxw, (cuuint32_t)d.Kh, (cuuint32_t)chunk};
+        cuuint32_t estr[3] = {1, 1, 1};
+        if ((d.W * 4) % 16 != 0) return CONV2D_ERR_UNSUPPORTED;   // row pitch must be 16-byte aligned
+        CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(src), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
+    }
+    const long long blocks = (long long)d.N * d.Ho * prm.n_wb * prm.n_cb;
+    if (blocks > 0x7fffffffLL) return CONV2D_ERR_UNSUPPORTED;
+    const int threads = 32 * d.cc_warps;
+    cudaError_t e = im2win ? launch_fp32_shape<true>(d, prm, map, threads, smem, blocks, st)
+                           : launch_fp32_shape<false>(d, prm, map, threads, smem, blocks, st);
+    return e == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
+}
+
+}  // namespace conv2d_gb300

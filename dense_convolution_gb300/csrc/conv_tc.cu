@@ -1,0 +1,337 @@
+// fp16/bf16-in, fp32-accumulate convolution on the 5th-generation tensor
+// cores (tcgen05 MMA, accumulators in tensor memory), operands fed by TMA.
+//
+// GEMM view ("Enabling Memory-efficient Im2win Convolution ...", Sec. III-D,
+// Algorithm 1 line 1, with the roles of M and N swapped so that the MMA's
+// 128-row side runs over output pixels):
+//   M = N*Ho*Wo output pixels (row-major over n, ho, wo = NCHW plane order),
+//   N = Co output channels,
+//   K = taps x channel chunks, 64 16-bit elements per pipeline stage.
+//
+// A tile (128 pixels x 64 K) comes from one im2col-mode TMA load of a
+// channels-innermost tensor: the copy engine walks 128 consecutive output
+// pixels (across row and image boundaries) and, for each, reads 64 channels
+// at the pixel's window origin plus a filter-tap offset.
+//   im2win    source = the window tensor [N][Ho][W+2p][Kh*Ci8]; a window is
+//             Kw consecutive "pixels" of Kh*Ci8 channels (Eq. (2)/(3) of the
+//             im2win paper, NHWC variant); tap t = kw, offset (kw, 0).
+//   implicit  source = X in NHWC [N][H][W][Ci8]; tap t = (kh, kw), offset
+//             (kw, kh); the map's bounding box shifts by -p and the walk
+//             strides by s, so padding is the copy engine's zero fill.
+// B tile (BN channels x 64 K) is a tiled TMA load of the repacked filter.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over tiles):
+//   warp 0     TMA producer (one elected lane), STAGES-deep shared-memory ring
+//   warp 1     TMEM allocation + MMA issue (one lane): 4 x (128xBNx16) per stage
+//   warps 2-5  epilogue: tcgen05.ld of their 32-lane TMEM quarter, round to the
+//              output type, store NCHW (32 consecutive pixels per store)
+// Two TMEM accumulators let the epilogue of tile i overlap the MMAs of i+1.
+// Every wait is bounded (ptx.cuh); on a timeout the CTA drains what it issued,
+// frees its TMEM and exits with the device status word set.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace conv2d_gb300 {
+
+struct TcParams {
+    int M, HoWo, Ho, Wo, Co;
+    int n_n_tiles, n_tiles;
+    int n_cchunks, n_kchunks, CP, Kw, s, p;
+    int im2win;
+    void* y;
+};
+
+template <int BN>
+struct TcConfig {
+    static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int kABytes = kTcBlockM * kTcBlockK * 2;   // 16 KB
+    static constexpr int kBBytes = BN * kTcBlockK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kTmemCols = 2 * BN;                    // two accumulators
+    static constexpr int kBarOffset = kStages * kStageBytes;
+    static constexpr int kSmemBytes = kBarOffset + 256 + 1024;  // barriers + alignment slack
+};
+
+template <int BN, bool BF16>
+__global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__ CUtensorMap amap,
+                                                         const __grid_constant__ CUtensorMap bmap,
+                                                         const TcParams prm) {
+    using Cfg = TcConfig<BN>;
+    constexpr int S = Cfg::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    // 128-byte swizzled operand tiles need 1024-byte alignment.
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOffset);
+    // bars[0..S) full, [S..2S) empty, [2S..2S+2) accumulator full, [2S+2..2S+4) accumulator empty, [2S+4] drain
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto full_bar = [&](int i) { return smem_addr(&bars[i]); };
+    auto empty_bar = [&](int i) { return smem_addr(&bars[S + i]); };
+    auto accf_bar = [&](int i) { return smem_addr(&bars[2 * S + i]); };
+    auto acce_bar = [&](int i) { return smem_addr(&bars[2 * S + 2 + i]); };
+    const uint32_t drain_bar = smem_addr(&bars[2 * S + 4]);
+
+    if (warp == 0 && lane == 0) {
+        for (int i = 0; i < S; ++i) { mbar_init(full_bar(i), 1); mbar_init(empty_bar(i), 1); }
+        for (int i = 0; i < 2; ++i) { mbar_init(accf_bar(i), 1); mbar_init(acce_bar(i), 4); }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+        tma_prefetch_desc(&amap);
+        tma_prefetch_desc(&bmap);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < prm.n_tiles && ok; tile += gridDim.x) {
+                const int m0 = (tile / prm.n_n_tiles) * kTcBlockM;
+                const int n0 = (tile % prm.n_n_tiles) * BN;
+                const int img = m0 / prm.HoWo, r = m0 - img * prm.HoWo;
+                const int ho = r / prm.Wo, wo = r - ho * prm.Wo;
+                for (int kc = 0; kc < prm.n_kchunks; ++kc) {
+                    const int t = kc / prm.n_cchunks;
+                    const int c0 = (kc - t * prm.n_cchunks) * kTcBlockK;
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
+                    const uint32_t a_dst = smem_addr(smem + stage * Cfg::kStageBytes);
+                    const uint32_t b_dst = a_dst + Cfg::kABytes;
+                    if (prm.im2win) {
+                        tma_load_im2col_4d(a_dst, &amap, full_bar(stage), c0, wo * prm.s, ho, img, (uint16_t)t, 0);
+                    } else {
+                        const int kh = t / prm.Kw, kw = t - kh * prm.Kw;
+                        tma_load_im2col_4d(a_dst, &amap, full_bar(stage), c0, wo * prm.s - prm.p,
+                                           ho * prm.s - prm.p, img, (uint16_t)kw, (uint16_t)kh);
+                    }
+                    tma_load_2d(b_dst, &bmap, full_bar(stage), t * prm.CP + c0, n0);
+                    ++issued;
+                    if (++stage == S) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok) {
+                // Let every copy already issued land before the CTA can exit.
+                int dummy = 0;
+                int st = stage;
+                uint32_t ph = phase;
+                for (int i = 0; i < S && i < issued; ++i) {
+                    if (--st < 0) { st = S - 1; ph ^= 1; }
+                    mbar_wait(full_bar(st), ph, &dummy);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = umma_idesc_f16(BF16, kTcBlockM, BN);
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true, issued_any = false;
+            for (int tile = blockIdx.x; tile < prm.n_tiles && ok; tile += gridDim.x) {
+                if (!mbar_wait(acce_bar(acc), acc_phase ^ 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kc = 0; kc < prm.n_kchunks; ++kc) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_addr(smem + stage * Cfg::kStageBytes);
+                    const uint32_t b_base = a_base + Cfg::kABytes;
+#pragma unroll
+                    for (int k = 0; k < kTcBlockK / 16; ++k) {
+                        umma_f16(d_tmem, sw128_kmajor_desc(a_base + 32 * k), sw128_kmajor_desc(b_base + 32 * k),
+                                 idesc, (kc > 0 || k > 0) ? 1u : 0u);
+                    }
+                    issued_any = true;
+                    umma_commit(empty_bar(stage));
+                    if (++stage == S) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                umma_commit(accf_bar(acc));
+                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            }
+            if (!ok && issued_any) {
+                int dummy = 0;
+                umma_commit(drain_bar);
+                mbar_wait(drain_bar, 0, &dummy);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quarter = warp & 3;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < prm.n_tiles; tile += gridDim.x) {
+            const bool got = mbar_wait(accf_bar(acc), acc_phase, abort_flag);
+            __syncwarp();
+            if (!__all_sync(0xffffffffu, got)) break;
+            tc_fence_after();
+            const int m0 = (tile / prm.n_n_tiles) * kTcBlockM;
+            const int n0 = (tile % prm.n_n_tiles) * BN;
+            const int m = m0 + quarter * 32 + lane;
+            const bool m_ok = m < prm.M;
+            const int img = m_ok ? m / prm.HoWo : 0;
+            const int r = m_ok ? m - img * prm.HoWo : 0;
+            uint16_t* out = static_cast<uint16_t*>(prm.y) + ((long long)img * prm.Co) * prm.HoWo + r;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(t_row + cc * 32, v);
+                tmem_ld_wait();
+                const int cob = n0 + cc * 32;
+                if (m_ok) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int co = cob + j;
+                        if (co < prm.Co) {
+                            const float f = __uint_as_float(v[j]);
+                            uint16_t h;
+                            if (BF16) h = __bfloat16_as_ushort(__float2bfloat16_rn(f));
+                            else      h = __half_as_ushort(__float2half_rn(f));
+                            out[(long long)co * prm.HoWo] = h;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce_bar(acc));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+void* driver_entry(const char* name) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return fn;
+}
+
+cudaError_t status_read_clear_tc(cudaStream_t st, uint32_t* out) { return status_read_clear(st, out); }
+
+int device_sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+    int v = 148;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    if (dev >= 0 && dev < 64) cached[dev] = v;
+    return v;
+}
+
+typedef CUresult (*PFN_encodeTiled_t)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                      const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                      CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                      CUtensorMapFloatOOBfill);
+typedef CUresult (*PFN_encodeIm2col_t)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                       const cuuint64_t*, const int*, const int*, cuuint32_t, cuuint32_t,
+                                       const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                       CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+template <int BN, bool BF16>
+static cudaError_t launch_tc_inst(const CUtensorMap& a, const CUtensorMap& b, const TcParams& prm, int grid,
+                                  cudaStream_t st) {
+    auto kern = conv_tc_kernel<BN, BF16>;
+    const int smem = TcConfig<BN>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, 192, smem, st>>>(a, b, prm);
+    return cudaGetLastError();
+}
+
+conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* wq, void* y, bool im2win,
+                             cudaStream_t st) {
+    auto enc_tiled = reinterpret_cast<PFN_encodeTiled_t>(driver_entry("cuTensorMapEncodeTiled"));
+    auto enc_im2col = reinterpret_cast<PFN_encodeIm2col_t>(driver_entry("cuTensorMapEncodeIm2col"));
+    if (!enc_tiled || !enc_im2col) return CONV2D_ERR_CUDA;
+    const CUtensorMapDataType dt =
+        d.dtype == CONV2D_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+
+    CUtensorMap amap, bmap;
+    // A: im2col view of a channels-innermost tensor (C, W, H, N).
+    cuuint64_t C, Wd, Hd;
+    int lower[2], upper[2];
+    cuuint32_t estr[4];
+    if (im2win) {
+        C = (cuuint64_t)d.Kh * d.Ci8; Wd = d.Wp; Hd = d.Ho;
+        lower[0] = 0; lower[1] = 0;
+        upper[0] = -(d.Kw - 1); upper[1] = 0;
+        estr[0] = 1; estr[1] = d.s; estr[2] = 1; estr[3] = 1;
+    } else {
+        C = d.Ci8; Wd = d.W; Hd = d.H;
+        lower[0] = -d.p; lower[1] = -d.p;
+        upper[0] = d.p - (d.Kw - 1); upper[1] = d.p - (d.Kh - 1);
+        estr[0] = 1; estr[1] = d.s; estr[2] = d.s; estr[3] = 1;
+    }
+    cuuint64_t adims[4] = {C, Wd, Hd, (cuuint64_t)d.N};
+    cuuint64_t astr[3] = {C * 2, C * 2 * Wd, C * 2 * Wd * Hd};
+    CUresult r = enc_im2col(&amap, dt, 4, const_cast<void*>(src), adims, astr, lower, upper, kTcBlockK,
+                            kTcBlockM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
+
+    // B: repacked filter [Co][taps*CP], K-major, box 64 x BN.
+    cuuint64_t bdims[2] = {(cuuint64_t)d.taps * d.CP, (cuuint64_t)d.Co};
+    cuuint64_t bstr[1] = {(cuuint64_t)d.taps * d.CP * 2};
+    cuuint32_t bbox[2] = {(cuuint32_t)kTcBlockK, (cuuint32_t)d.BN};
+    cuuint32_t bestr[2] = {1, 1};
+    r = enc_tiled(&bmap, dt, 2, const_cast<void*>(wq), bdims, bstr, bbox, bestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
+
+    TcParams prm{};
+    prm.M = d.N * d.Ho * d.Wo;
+    prm.HoWo = d.Ho * d.Wo; prm.Ho = d.Ho; prm.Wo = d.Wo; prm.Co = d.Co;
+    prm.n_n_tiles = (d.Co + d.BN - 1) / d.BN;
+    const int n_m_tiles = (prm.M + kTcBlockM - 1) / kTcBlockM;
+    prm.n_tiles = n_m_tiles * prm.n_n_tiles;
+    prm.n_cchunks = d.CP / kTcBlockK;
+    prm.n_kchunks = d.taps * prm.n_cchunks;
+    prm.CP = d.CP; prm.Kw = d.Kw; prm.s = d.s; prm.p = d.p;
+    prm.im2win = im2win ? 1 : 0;
+    prm.y = y;
+    int grid = device_sm_count();
+    if (grid > prm.n_tiles) grid = prm.n_tiles;
+
+    const bool bf = d.dtype == CONV2D_BF16;
+    cudaError_t e;
+    switch (d.BN) {
+        case 64:  e = bf ? launch_tc_inst<64, true>(amap, bmap, prm, grid, st) : launch_tc_inst<64, false>(amap, bmap, prm, grid, st); break;
+        case 128: e = bf ? launch_tc_inst<128, true>(amap, bmap, prm, grid, st) : launch_tc_inst<128, false>(amap, bmap, prm, grid, st); break;
+        default:  e = bf ? launch_tc_inst<256, true>(amap, bmap, prm, grid, st) : launch_tc_inst<256, false>(amap, bmap, prm, grid, st); break;
+    }
+    return e == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
+}
+
+}  // namespace conv2d_gb300

@@ -1,0 +1,58 @@
+// Host-side plan shared by the translation units of the library (not public).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/conv2d.h"
+
+struct conv2d_desc {
+    // Problem, as given to conv2d_desc_create.
+    int N, Ci, H, W, Co, Kh, Kw, s, p;
+    conv2d_dtype dtype;
+    conv2d_algo requested;
+    conv2d_layout layout;
+    // Derived geometry.
+    int Ho, Wo, Wp;       // output size; padded input width W + 2p
+    conv2d_algo algo;     // resolved (never AUTO)
+    // fp32 CUDA-core paths.
+    int Lp;               // im2win strip pitch in floats: Wp*Kh rounded up to 4
+    int cc_warps;         // warps per block (16 output channels each)
+    int cc_wpt;           // output columns per lane (1, 2 or 4)
+    // Tensor-core paths.
+    int Ci8;              // Ci rounded up to 8 (16-byte channel vectors)
+    int taps;             // filter taps per K-chunk group: Kw (im2win) or Kh*Kw (implicit)
+    int CP;               // channel extent per tap, padded to the 64-element K chunk
+    int BN;               // output channels per MMA tile (64, 128 or 256)
+    // Workspace layout (bytes): packed filter at 0, input-side tensor after it.
+    size_t ws_weights, ws_input_off, ws_input, ws_total;
+};
+
+namespace conv2d_gb300 {
+
+constexpr int kTcBlockM = 128;   // output pixels per MMA tile
+constexpr int kTcBlockK = 64;    // K elements per pipeline stage (128 bytes of 16-bit)
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// transforms.cu
+cudaError_t launch_im2win_strips_f32(const float* x, float* xw, const conv2d_desc& d, cudaStream_t st);
+cudaError_t launch_window_cl16(const void* x, void* out, int N, int Ci, int H, int W, int Ci8, int R, int Wq,
+                               int Kh, int s, int p, cudaStream_t st);
+cudaError_t launch_pack_filter_tc(const void* w, void* wq, const conv2d_desc& d, bool im2win, cudaStream_t st);
+cudaError_t launch_pack_filter_f32(const float* w, float* wq, const conv2d_desc& d, cudaStream_t st);
+
+// conv_fp32.cu
+conv2d_status launch_conv_fp32(const conv2d_desc& d, const float* src, const float* wq, float* y,
+                               bool im2win, cudaStream_t st);
+
+// conv_tc.cu
+conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* wq, void* y, bool im2win,
+                             cudaStream_t st);
+int device_sm_count();
+void* driver_entry(const char* name);
+cudaError_t status_read_clear_tc(cudaStream_t st, uint32_t* out);
+cudaError_t status_read_clear_fp32(cudaStream_t st, uint32_t* out);
+
+}  // namespace conv2d_gb300

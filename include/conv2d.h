@@ -1,0 +1,167 @@
+/*
+ * conv2d.h — C ABI of the GB300 (sm_103a) forward 2-D convolution library.
+ *
+ * Operation (every entry point below computes or serves this):
+ *
+ *   Y[n,co,ho,wo] = sum_{ci,kh,kw} X[n,ci, ho*s+kh-p, wo*s+kw-p] * W[co,ci,kh,kw]
+ *
+ * a cross-correlation (no kernel flip) with symmetric zero padding p and one
+ * stride s, as defined in "Enabling Memory-efficient Im2win Convolution with
+ * Multi-precision Support on GPU CUDA and Tensor Cores", Sec. III-A, Eq. (1),
+ * and in the 7-loop of "Unifying Convolutions and GEMM", Sec. 1.  Output size
+ * (floor rule, "Unifying Convolutions and GEMM", Sec. 5):
+ *
+ *   Ho = (H + 2p - Kh) / s + 1,   Wo = (W + 2p - Kw) / s + 1.
+ *
+ * Conventions for every call:
+ *   - All functions return a conv2d_status; no C++ exception crosses the ABI.
+ *   - Device pointers are plain CUDA device addresses owned by the caller.
+ *     The library never allocates, frees or retains device memory, and keeps
+ *     no pointer after a call returns.
+ *   - `stream` is a cudaStream_t (or CUstream) cast to void*; NULL is the
+ *     legacy default stream.  Kernels are launched asynchronously on it;
+ *     conv2d_fwd returns once the launches are queued.
+ *   - A descriptor is immutable after creation except through the
+ *     conv2d_desc_set_* calls; concurrent conv2d_fwd calls on one descriptor
+ *     from several host threads are safe (each call uses only its arguments).
+ */
+#ifndef CONV2D_GB300_H
+#define CONV2D_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CONV2D_OK = 0,
+    CONV2D_ERR_BAD_PARAM = 1,            /* invalid geometry or enum value              */
+    CONV2D_ERR_UNSUPPORTED = 2,          /* valid request this build does not implement */
+    CONV2D_ERR_NULL_PTR = 3,             /* a required pointer was NULL                 */
+    CONV2D_ERR_MISALIGNED = 4,           /* a device pointer was not 16-byte aligned    */
+    CONV2D_ERR_WORKSPACE_TOO_SMALL = 5,  /* workspace_bytes < conv2d_workspace_size     */
+    CONV2D_ERR_CUDA = 6,                 /* a CUDA runtime/driver call failed           */
+    CONV2D_ERR_DEVICE_TIMEOUT = 7        /* a kernel's bounded wait expired (see below) */
+} conv2d_status;
+
+/* Element type of X and W.  Accumulation is always fp32 (fp32 FFMA on the
+ * CUDA-core path, fp32 TMEM accumulators on the tensor-core path).  Y is fp32
+ * for CONV2D_F32 and has the input type for CONV2D_F16 / CONV2D_BF16, rounded
+ * to nearest even once at the store. */
+typedef enum { CONV2D_F32 = 0, CONV2D_F16 = 1, CONV2D_BF16 = 2 } conv2d_dtype;
+
+/* Algorithms.
+ *  IM2WIN_FP32_CC   fp32 on CUDA cores.  Workspace holds the im2win tensor of
+ *                   "Enabling Memory-efficient Im2win Convolution ...",
+ *                   Sec. III-B, Eq. (2) (one strip of Kh rows per output row
+ *                   and input channel, padding included); the convolution of
+ *                   Sec. III-C, Eq. (3) reads it.
+ *  IM2WIN_TC        fp16/bf16 on tcgen05 tensor cores.  Workspace holds the
+ *                   channels-innermost window tensor (the NHWC variant the
+ *                   same paper uses on tensor cores, Sec. III-D) and the
+ *                   repacked filter.
+ *  IMPLICIT_TC      fp16/bf16 on tcgen05 tensor cores; operand tiles are
+ *                   gathered straight from channels-last X in the load path
+ *                   (the implicit expansion of "im2col Expansion, FFT
+ *                   Convolution, and Winograd Transforms", im2col section).
+ *                   Workspace: the repacked filter, plus a channels-last copy
+ *                   of X when the input layout is NCHW.
+ *  IMPLICIT_FP32_CC fp32 on CUDA cores, staging X's rows directly (no input
+ *                   expansion); workspace: the repacked filter only.
+ *  AUTO             resolved per shape when the descriptor is created
+ *                   (conv2d_get_algo reports the choice). */
+typedef enum {
+    CONV2D_ALGO_AUTO = 0,
+    CONV2D_ALGO_IM2WIN_FP32_CC = 1,
+    CONV2D_ALGO_IM2WIN_TC = 2,
+    CONV2D_ALGO_IMPLICIT_TC = 3,
+    CONV2D_ALGO_IMPLICIT_FP32_CC = 4
+} conv2d_algo;
+
+/* Memory layout of X.  Y is always NCHW.  W is always [Cout][Cin][Kh][Kw]. */
+typedef enum { CONV2D_LAYOUT_NCHW = 0, CONV2D_LAYOUT_NHWC = 1 } conv2d_layout;
+
+typedef struct conv2d_desc *conv2d_desc_t;   /* opaque, host memory, owned by the caller */
+
+/* Create a descriptor for one problem shape.  Host-only: makes no CUDA call,
+ * so it works without a GPU.  Arguments follow the problem statement of
+ * "Enabling Memory-efficient Im2win Convolution ...", Sec. III-A (N, Ci, Hi,
+ * Wi, Co, Hf, Wf, s) with the padding of "Unifying Convolutions and GEMM",
+ * Sec. 5.
+ *   out       receives the new descriptor (set to NULL on failure)
+ *   N, Cin, H, W   input batch, channels, height, width   (all >= 1)
+ *   Cout           output channels                         (>= 1)
+ *   Kh, Kw         filter height and width                 (>= 1)
+ *   stride >= 1, pad >= 0 (symmetric, zero fill); Ho and Wo must be >= 1
+ *   dtype, algo    see above; an algo that does not serve dtype -> BAD_PARAM
+ * Errors: NULL_PTR (out NULL), BAD_PARAM (any check above, or a tensor with
+ * more than 2^31-1 elements), UNSUPPORTED (shape outside the algo's limits,
+ * e.g. pad > 127 on a tensor-core algo). */
+conv2d_status conv2d_desc_create(conv2d_desc_t *out, int N, int Cin, int H, int W, int Cout,
+                                 int Kh, int Kw, int stride, int pad,
+                                 conv2d_dtype dtype, conv2d_algo algo);
+
+/* Select the layout of X (default NCHW).  Re-resolves AUTO and changes the
+ * workspace size; call before conv2d_workspace_size.  BAD_PARAM for an
+ * unknown layout; UNSUPPORTED for NHWC with an fp32 algorithm. */
+conv2d_status conv2d_desc_set_input_layout(conv2d_desc_t d, conv2d_layout layout);
+
+/* Release a descriptor (NULL is accepted and ignored). */
+conv2d_status conv2d_desc_destroy(conv2d_desc_t d);
+
+/* Output spatial size (floor rule above). */
+conv2d_status conv2d_out_dims(conv2d_desc_t d, int *Ho, int *Wo);
+
+/* Workspace bytes conv2d_fwd needs for the resolved algorithm (may be 0).
+ * The buffer must be device memory, 16-byte aligned (256 recommended). */
+conv2d_status conv2d_workspace_size(conv2d_desc_t d, size_t *bytes);
+
+/* Algorithm the descriptor resolved to (never AUTO). */
+conv2d_status conv2d_get_algo(conv2d_desc_t d, conv2d_algo *chosen);
+
+/* Forward convolution on `stream`.
+ *   x  device, layout per conv2d_desc_set_input_layout, dtype of the desc
+ *   w  device, [Cout][Cin][Kh][Kw] contiguous, dtype of the desc
+ *   y  device, [N][Cout][Ho][Wo] contiguous; fp32 for CONV2D_F32, else dtype
+ *   workspace, workspace_bytes: device scratch of at least
+ *      conv2d_workspace_size bytes (NULL/0 allowed when that size is 0);
+ *      its contents on entry do not matter and are garbage on exit.
+ * x, w, y and workspace must be 16-byte aligned and must not overlap y.
+ * Errors: NULL_PTR, MISALIGNED, WORKSPACE_TOO_SMALL (checked before any
+ * launch), CUDA (a launch or driver call failed; the CUDA error is left
+ * pending for the caller to inspect).  Device-side timeouts are reported by
+ * conv2d_device_status, not here, because launches are asynchronous. */
+conv2d_status conv2d_fwd(conv2d_desc_t d, const void *x, const void *w, void *y,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/* conv2d_fwd that also records two CUDA events on `stream`: `ev_start`
+ * immediately before and `ev_end` immediately after the launch of the main
+ * contraction kernel (the im2win / implicit-GEMM / CUDA-core convolution
+ * kernel, not the transforms).  Events are cudaEvent_t cast to void*; either
+ * may be NULL.  Lets a caller time that kernel alone inside a full call.
+ * Same arguments, layouts and errors as conv2d_fwd, plus CONV2D_ERR_CUDA when
+ * an event record fails. */
+conv2d_status conv2d_fwd_profiled(conv2d_desc_t d, const void *x, const void *w, void *y,
+                                  void *workspace, size_t workspace_bytes, void *stream,
+                                  void *ev_start, void *ev_end);
+
+/* Number of kernel launches one conv2d_fwd call makes for this descriptor
+ * (filter repack, input transform if any, contraction). */
+conv2d_status conv2d_launches_per_call(conv2d_desc_t d, int *launches);
+
+/* Read and clear the library's device status word on the current device
+ * (synchronises `stream`).  Returns CONV2D_OK when every kernel since the
+ * last call finished normally, CONV2D_ERR_DEVICE_TIMEOUT when a kernel gave
+ * up on a bounded wait (its output is then invalid), CONV2D_ERR_CUDA when the
+ * readback failed.  `*code_out` (may be NULL) receives the raw status bits. */
+conv2d_status conv2d_device_status(void *stream, uint32_t *code_out);
+
+/* Static string for a status code (never NULL). */
+const char *conv2d_status_string(conv2d_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CONV2D_GB300_H */

@@ -1,0 +1,141 @@
+"""Host-side checks of the C ABI: the library loads without a GPU, exports
+every function ``include/conv2d.h`` declares, and its descriptor, workspace
+and argument checks behave as documented.  No kernel is launched here."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def capi():
+    from dense_convolution_gb300 import build, capi
+    build.build()
+    capi.load()
+    return capi
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "conv2d.h")).read()
+    return sorted(set(re.findall(r"\b(conv2d_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(capi):
+    import ctypes
+    names = _declared()
+    assert len(names) == len(capi.EXPORTED)
+    assert set(names) == set(capi.EXPORTED)
+    L = ctypes.CDLL(capi.LIB_PATH)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(capi):
+    for s in range(8):
+        assert capi.conv2d_status_string(s)
+    assert capi.conv2d_status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("args", [
+    (0, 3, 8, 8, 4, 3, 3, 1, 1), (1, 0, 8, 8, 4, 3, 3, 1, 1), (1, 3, 8, 8, 4, 3, 3, 0, 1),
+    (1, 3, 8, 8, 4, 3, 3, 1, -1), (1, 3, 2, 2, 4, 5, 5, 1, 0), (1, 3, 8, 8, 4, 0, 3, 1, 0),
+])
+def test_bad_geometry(capi, args):
+    with pytest.raises(capi.Conv2dError) as e:
+        capi.conv2d_desc_create(*args, "f32", "auto")
+    assert e.value.status == capi.ERR_BAD_PARAM
+
+
+def test_dtype_algo_mismatch(capi):
+    with pytest.raises(capi.Conv2dError) as e:
+        capi.conv2d_desc_create(1, 8, 8, 8, 8, 3, 3, 1, 1, "f16", "im2win_fp32_cc")
+    assert e.value.status == capi.ERR_BAD_PARAM
+    with pytest.raises(capi.Conv2dError) as e:
+        capi.conv2d_desc_create(1, 8, 8, 8, 8, 3, 3, 1, 1, "f32", "implicit_tc")
+    assert e.value.status == capi.ERR_BAD_PARAM
+    with pytest.raises(capi.Conv2dError) as e:
+        capi.conv2d_desc_create(1, 8, 8, 8, 8, 3, 3, 1, 1, 7, "auto")
+    assert e.value.status == capi.ERR_BAD_PARAM
+
+
+def test_out_dims_floor_rule(capi):
+    d = capi.conv2d_desc_create(2, 64, 224, 224, 64, 7, 7, 2, 0, "f32", "auto")
+    try:
+        assert capi.conv2d_out_dims(d) == (109, 109)     # Table I, cv4
+    finally:
+        capi.conv2d_desc_destroy(d)
+
+
+def test_auto_choices_and_workspace(capi):
+    cases = {
+        # name: (shape, dtype, expected algo)
+        "resnet_f16": ((32, 64, 56, 56, 64, 3, 3, 1, 1), "f16", "implicit_tc"),
+        "stem_f16": ((32, 3, 224, 224, 64, 7, 7, 2, 3), "f16", "im2win_tc"),
+        "vgg_bf16": ((64, 512, 28, 28, 512, 3, 3, 1, 1), "bf16", "implicit_tc"),
+        "resnet_f32": ((32, 64, 56, 56, 64, 3, 3, 1, 1), "f32", "im2win_fp32_cc"),
+    }
+    for name, (shape, dt, algo) in cases.items():
+        d = capi.conv2d_desc_create(*shape, dt, "auto")
+        try:
+            assert capi.conv2d_get_algo(d) == algo, name
+            N, Ci, H, W, Co, Kh, Kw, s, p = shape
+            Ho = (H + 2 * p - Kh) // s + 1
+            ws = capi.conv2d_workspace_size(d)
+            elem = 4 if dt == "f32" else 2
+            im2win_tensor = N * Ci * Ho * (W + 2 * p) * Kh * elem
+            assert ws > 0
+            if algo == "implicit_tc":
+                ci8 = (Ci + 7) // 8 * 8
+                assert ws >= N * H * W * ci8 * 2          # channels-last copy of X
+                assert ws < im2win_tensor
+        finally:
+            capi.conv2d_desc_destroy(d)
+
+
+def test_nhwc_layout_drops_input_copy(capi):
+    d = capi.conv2d_desc_create(8, 64, 28, 28, 64, 3, 3, 1, 1, "f16", "implicit_tc")
+    try:
+        nchw = capi.conv2d_workspace_size(d)
+        capi.conv2d_desc_set_input_layout(d, "nhwc")
+        nhwc = capi.conv2d_workspace_size(d)
+        assert nhwc == 64 * 9 * 64 * 2                   # packed filter only
+        assert nchw > nhwc
+        with pytest.raises(capi.Conv2dError):
+            capi.conv2d_desc_set_input_layout(d, 5)
+    finally:
+        capi.conv2d_desc_destroy(d)
+    d = capi.conv2d_desc_create(8, 64, 28, 28, 64, 3, 3, 1, 1, "f32", "auto")
+    try:
+        with pytest.raises(capi.Conv2dError) as e:
+            capi.conv2d_desc_set_input_layout(d, "nhwc")
+        assert e.value.status == capi.ERR_UNSUPPORTED
+    finally:
+        capi.conv2d_desc_destroy(d)
+
+
+def test_fwd_argument_checks_before_launch(capi):
+    # These return before any CUDA call, so fake addresses are safe here.
+    d = capi.conv2d_desc_create(1, 8, 16, 16, 8, 3, 3, 1, 1, "f32", "im2win_fp32_cc")
+    try:
+        ws = capi.conv2d_workspace_size(d)
+        A = 1 << 20
+        with pytest.raises(capi.Conv2dError) as e:
+            capi.conv2d_fwd(d, 0, A, A, A, ws)
+        assert e.value.status == capi.ERR_NULL_PTR
+        with pytest.raises(capi.Conv2dError) as e:
+            capi.conv2d_fwd(d, A + 4, A, A, A, ws)
+        assert e.value.status == capi.ERR_MISALIGNED
+        with pytest.raises(capi.Conv2dError) as e:
+            capi.conv2d_fwd(d, A, A, A, A, ws - 1)
+        assert e.value.status == capi.ERR_WORKSPACE_TOO_SMALL
+        with pytest.raises(capi.Conv2dError) as e:
+            capi.conv2d_fwd(d, A, A, A, 0, ws)
+        assert e.value.status == capi.ERR_NULL_PTR
+    finally:
+        capi.conv2d_desc_destroy(d)
+
+
+def test_destroy_null_is_ok(capi):
+    capi.conv2d_desc_destroy(0)
