@@ -107,32 +107,35 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def cpu_oracle_baseline(wl, dtype, budget_s=12.0, threads=None):
+def cpu_oracle_baseline(wl, dtype, budget_s=12.0, threads=None, inputs=None):
     """Time the fp64 oracle (as it stands) on host threads over a bounded
-    sample of the workload: whole (n, co) output planes, enough of them for
-    about ``budget_s`` seconds.  Returns a cpu_baseline dict in TFLOP/s."""
+    sample of the workload: whole (n, co) output planes taken in order,
+    enough of them for about ``budget_s`` seconds (the whole batch at most).
+    Returns a cpu_baseline dict in TFLOP/s."""
     import concurrent.futures as cf
     from oracle import ref
     threads = threads or (os.cpu_count() or 1)
-    d = synth.make_inputs(wl, dtype, N=1)
+    d = inputs if inputs is not None else synth.make_inputs(wl, dtype)
     X64, W64 = d["X64"], d["W64"]
+    N = X64.shape[0]
     Ho, Wo = wl.out_hw()
-    Y = np.empty((1, wl.Co, Ho, Wo))
+    Y = np.empty((N, wl.Co, Ho, Wo))
     S = np.empty_like(Y)
     plane_flops = 2 * Ho * Wo * wl.Ci * wl.Kh * wl.Kw
     t0 = time.perf_counter()
     ref.conv2d_slice(X64, W64, Y, S, wl.stride, wl.pad, 0, 1, 0, 1)
     t_plane = max(time.perf_counter() - t0, 1e-6)
-    planes = int(min(wl.Co, max(1, budget_s * threads / t_plane)))   # image 0's channels
-    jobs = list(range(planes))
+    planes = int(min(N * wl.Co, max(1, budget_s * threads / t_plane)))
+    jobs = [(i // wl.Co, i % wl.Co) for i in range(planes)]
     t0 = time.perf_counter()
     with cf.ThreadPoolExecutor(threads) as ex:
-        list(ex.map(lambda co: ref.conv2d_slice(X64, W64, Y, S, wl.stride, wl.pad, 0, 1, co, co + 1), jobs))
+        list(ex.map(lambda j: ref.conv2d_slice(X64, W64, Y, S, wl.stride, wl.pad, j[0], j[0] + 1, j[1], j[1] + 1),
+                    jobs))
     dt = time.perf_counter() - t0
     flops = planes * plane_flops
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"{planes} output planes (image 0, channels 0..{planes - 1}) of {wl.name}, "
-                      f"{flops / 1e9:.2f} GFLOP in {dt:.2f} s, fp64 7-loop"}
+            "sample": f"{planes} of {N * wl.Co} output planes (n, co in order) of {wl.name}, "
+                      f"{flops / 1e9:.2f} GFLOP in {dt:.2f} s, fp64 7-loop on {threads} threads"}
 
 
 def _workload(args):
@@ -148,9 +151,10 @@ def run_reference(args, rank, world):
         return
     # Each step times a bounded sample; the whole run stays within ~2 minutes.
     per_step = min(3.0, 120.0 / (args.steps + args.warmup))
+    inputs = synth.make_inputs(wl, dtype)
     for _ in range(args.warmup):
-        cpu_oracle_baseline(wl, dtype, budget_s=per_step / 4)
-    samples = [cpu_oracle_baseline(wl, dtype, budget_s=per_step) for _ in range(args.steps)]
+        cpu_oracle_baseline(wl, dtype, budget_s=per_step / 4, inputs=inputs)
+    samples = [cpu_oracle_baseline(wl, dtype, budget_s=per_step, inputs=inputs) for _ in range(args.steps)]
     vals = [s["value"] for s in samples]
     v = statistics.median(vals)
     step_ms = wl.flops() / (v * 1e12) * 1e3
@@ -291,7 +295,7 @@ def run_gpu(args, rank, world):
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_baseline(wl, dtype)
+        line["cpu_baseline"] = cpu_oracle_baseline(wl, dtype, inputs=d)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
