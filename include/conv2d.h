@@ -151,6 +151,30 @@ conv2d_status conv2d_fwd_profiled(conv2d_desc_t d, const void *x, const void *w,
  * (filter repack, input transform if any, contraction). */
 conv2d_status conv2d_launches_per_call(conv2d_desc_t d, int *launches);
 
+/* Size of the library's built-in workspace used by
+ * conv2d_fwd_static_workspace (64 MiB). */
+#define CONV2D_STATIC_WORKSPACE_BYTES (64u << 20)
+
+/* conv2d_fwd for callers that cannot allocate device memory (a host
+ * application that owns all device memory and passes in only the tensors, a
+ * loop that cannot afford the synchronisation of cudaMalloc/cudaFree, a
+ * process under a memory cap set by someone else).  The paper has no
+ * counterpart to this call; it is a deployment convenience.
+ *   Same x, w, y, stream and layouts as conv2d_fwd; no workspace argument:
+ *   scratch comes from one array of CONV2D_STATIC_WORKSPACE_BYTES that is
+ *   part of the library's device image on every GPU that loads the library,
+ *   held until the process exits.  The call allocates nothing.
+ *   The first call on each device (with that device current) looks up the
+ *   array's device address; make that first call before any stream capture.
+ *   Every call uses the same array and it keeps the previous call's contents
+ *   (nothing in it needs to start at zero).  Calls whose kernels overlap on
+ *   the GPU (other streams, other host threads) race on it: serialise them.
+ * Errors: as conv2d_fwd; WORKSPACE_TOO_SMALL when conv2d_workspace_size(d)
+ * exceeds CONV2D_STATIC_WORKSPACE_BYTES (checked before any launch); CUDA
+ * when the address lookup fails. */
+conv2d_status conv2d_fwd_static_workspace(conv2d_desc_t d, const void *x, const void *w, void *y,
+                                          void *stream);
+
 /* Read and clear the library's device status word on the current device
  * (synchronises `stream`).  Returns CONV2D_OK when every kernel since the
  * last call finished normally, CONV2D_ERR_DEVICE_TIMEOUT when a kernel gave
