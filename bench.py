@@ -224,7 +224,7 @@ def run_gpu(args, rank, world):
             ev[i][1].record(stream)
         torch.cuda.synchronize()
         # Keep the GPU busy long enough for the clock sampler to see the load.
-        t_end = time.perf_counter() + 0.4
+        t_end = time.perf_counter() + (0.0 if args.quick else 0.4)
         while time.perf_counter() < t_end:
             for _ in range(20):
                 step()
@@ -243,7 +243,7 @@ def run_gpu(args, rank, world):
 
     # End to end through the public API: pinned host X and W in, Y out, every step.
     e2e_ms = []
-    for i in range(max(3, min(K, 50))):
+    for i in range(3 if args.quick else max(3, min(K, 50))):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         flush.fill_(1)
         e0.record(stream)
@@ -294,7 +294,7 @@ def run_gpu(args, rank, world):
                 "d2h_bytes_per_step": yh.numel() * yh.element_size(), "ms_per_step": e2e},
         "clocks": clocks,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not (args.no_cpu_baseline or args.quick):
         line["cpu_baseline"] = cpu_oracle_baseline(wl, dtype, inputs=d)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -310,6 +310,8 @@ def main():
     ap.add_argument("--algo", default="auto")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="profiling runs: no CPU baseline, 3 end-to-end steps, no clock-sustain loop")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -86,6 +86,8 @@ conv2d_status finalize(conv2d_desc& d) {
         const long long chunk = im2win ? (long long)d.Kh * d.Ci8 : d.Ci8;
         d.CP = (int)((chunk + kTcBlockK - 1) / kTcBlockK * kTcBlockK);
         d.BN = d.Co <= 64 ? 64 : (d.Co <= 128 ? 128 : 256);
+        if ((long long)d.Ci * d.Kh * d.Kw > 16384) return CONV2D_ERR_UNSUPPORTED;   // per-channel filter staging
+        if (d.N > 65535) return CONV2D_ERR_UNSUPPORTED;
         const long long wq = (long long)d.Co * d.taps * d.CP;
         if (wq > kMaxElems) return CONV2D_ERR_UNSUPPORTED;
         d.ws_weights = (size_t)wq * 2;
@@ -216,7 +218,7 @@ conv2d_status fwd_impl(conv2d_desc_t dp, const void* x, const void* w, void* y, 
             e = launch_pack_filter_tc(w, wq, d, false, st);
             const void* src = x;
             if (e == cudaSuccess && d.layout == CONV2D_LAYOUT_NCHW) {
-                e = launch_window_cl16(x, win, d.N, d.Ci, d.H, d.W, d.Ci8, d.H, d.W, 1, 1, 0, st);
+                e = launch_nchw_to_nhwc16(x, win, d.N, d.Ci, d.H, d.W, d.Ci8, st);
                 src = win;
             }
             if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;

@@ -276,7 +276,7 @@ conv2d_status launch_conv_fp32(const conv2d_desc& d, const float* src, const flo
         per_ci_x = prm.pitch;
     }
     const int per_ci_w = d.Kh * d.Kw * prm.BCO;
-    const int budget = 100 * 1024 / 4;   // floats per stage (two stages resident)
+    const int budget = 12 * 1024 / 4;    // floats per stage: two stages ~24 KB, several blocks per SM
     int chunk = budget / (per_ci_x + per_ci_w);
     if (chunk < 1) chunk = 1;
     if (chunk > d.Ci) chunk = d.Ci;

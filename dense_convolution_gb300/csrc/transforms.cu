@@ -17,43 +17,101 @@
 namespace conv2d_gb300 {
 
 // ---------------------------------------------------------------- fp32 strips
-// One thread writes one 16-byte vector (4 consecutive strip elements); a warp
-// writes 512 contiguous bytes.  Reads walk Kh neighbouring rows and are served
-// by L1/L2.
-__global__ void __launch_bounds__(256) im2win_strips_f32_kernel(const float* __restrict__ x,
+// One block per strip (n, ci, ho); one thread writes one 16-byte vector (4
+// consecutive strip elements), so a warp writes 512 contiguous bytes.  Reads
+// walk Kh neighbouring rows and are served by L1/L2.
+__global__ void __launch_bounds__(128) im2win_strips_f32_kernel(const float* __restrict__ x,
                                                                 float4* __restrict__ xw, int Ci, int H, int W,
-                                                                int Ho, int Kh, int s, int p, int Wp, int Lp,
-                                                                long long total_vec) {
-    const int Lv = Lp >> 2;
-    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total_vec;
-         q += (long long)gridDim.x * blockDim.x) {
-        long long strip = q / Lv;
-        int e = (int)(q - strip * Lv) * 4;
-        int ho = (int)(strip % Ho);
-        long long nc = strip / Ho;                      // n*Ci + ci
-        const float* plane = x + nc * (long long)H * W;
+                                                                int Ho, int Kh, int s, int p, int Wp, int Lp) {
+    const long long strip = blockIdx.x;                 // (n*Ci + ci)*Ho + ho
+    const int ho = (int)(strip % Ho);
+    const long long nc = strip / Ho;
+    const float* plane = x + nc * (long long)H * W;
+    float4* out = xw + strip * (Lp >> 2);
+    for (int q = threadIdx.x; q < (Lp >> 2); q += blockDim.x) {
+        const int e = q * 4;
         int kx = e / Kh, u = e - kx * Kh;
         float v[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            int y = ho * s + u - p, xx = kx - p;
+            const int y = ho * s + u - p, xx = kx - p;
             float val = 0.f;
-            if (kx < Wp && y >= 0 && y < H && xx >= 0 && xx < W) val = __ldg(plane + (long long)y * W + xx);
+            if (kx < Wp && y >= 0 && y < H && xx >= 0 && xx < W) val = __ldg(plane + y * W + xx);
             v[j] = val;
             if (++u == Kh) { u = 0; ++kx; }
         }
-        xw[q] = make_float4(v[0], v[1], v[2], v[3]);
+        out[q] = make_float4(v[0], v[1], v[2], v[3]);
     }
 }
 
 cudaError_t launch_im2win_strips_f32(const float* x, float* xw, const conv2d_desc& d, cudaStream_t st) {
-    long long total_vec = (long long)d.N * d.Ci * d.Ho * (d.Lp / 4);
-    long long blocks = (total_vec + 255) / 256;
-    long long cap = (long long)device_sm_count() * 16;
-    int grid = (int)(blocks < cap ? blocks : cap);
-    if (grid < 1) grid = 1;
-    im2win_strips_f32_kernel<<<grid, 256, 0, st>>>(x, reinterpret_cast<float4*>(xw), d.Ci, d.H, d.W, d.Ho, d.Kh,
-                                                     d.s, d.p, d.Wp, d.Lp, total_vec);
+    const long long strips = (long long)d.N * d.Ci * d.Ho;
+    if (strips > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    im2win_strips_f32_kernel<<<(unsigned)strips, 128, 0, st>>>(x, reinterpret_cast<float4*>(xw), d.Ci, d.H, d.W,
+                                                                d.Ho, d.Kh, d.s, d.p, d.Wp, d.Lp);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- 16-bit NCHW -> NHWC (channels padded to 8)
+// Batched transpose of [C][P] planes (P = H*W) into [P][C8]: a block moves a
+// 64-channel x 64-pixel tile, reading 16-byte vectors along pixels and
+// writing 16-byte vectors along channels (a warp writes 4 x 128 contiguous
+// bytes).  The shared tile pitch of 66 halves keeps the column reads at two
+// ways of bank conflict.
+constexpr int kNhwcTile = 64;
+constexpr int kNhwcPitch = 66;
+
+__global__ void __launch_bounds__(256) nchw_to_nhwc16_kernel(const uint16_t* __restrict__ x,
+                                                             uint4* __restrict__ out, int C, int C8, int P,
+                                                             int vec_ok) {
+    __shared__ uint32_t tile[kNhwcTile * kNhwcPitch / 2];
+    uint16_t* t16 = reinterpret_cast<uint16_t*>(tile);
+    const int p0 = blockIdx.x * kNhwcTile, c0 = blockIdx.y * kNhwcTile;
+    const long long n = blockIdx.z;
+    const uint16_t* xn = x + n * (long long)C * P;
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int c = tid / 8 + 32 * i, pv = (tid % 8) * 8;
+        const int cc = c0 + c, pp = p0 + pv;
+        uint32_t w[4] = {0, 0, 0, 0};
+        if (cc < C) {
+            const uint16_t* src = xn + (long long)cc * P + pp;
+            if (vec_ok && pp + 8 <= P) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
+                w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (pp + j < P) w[j >> 1] |= (uint32_t)src[j] << (16 * (j & 1));
+            }
+        }
+        uint32_t* dst = tile + (c * kNhwcPitch + pv) / 2;
+        dst[0] = w[0]; dst[1] = w[1]; dst[2] = w[2]; dst[3] = w[3];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int pl = tid / 8 + 32 * i, cg = tid % 8;
+        const int pp = p0 + pl, cc = c0 + cg * 8;
+        if (pp < P && cc < C8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                w[j] = (uint32_t)t16[(cg * 8 + 2 * j) * kNhwcPitch + pl] |
+                       ((uint32_t)t16[(cg * 8 + 2 * j + 1) * kNhwcPitch + pl] << 16);
+            out[((n * P + pp) * C8 + cc) >> 3] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+cudaError_t launch_nchw_to_nhwc16(const void* x, void* out, int N, int C, int H, int W, int C8, cudaStream_t st) {
+    const int P = H * W;
+    const int vec_ok = (P % 8 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) ? 1 : 0;
+    dim3 grid((P + kNhwcTile - 1) / kNhwcTile, (C8 + kNhwcTile - 1) / kNhwcTile, N);
+    if (grid.z > 65535 || grid.y > 65535) return cudaErrorInvalidConfiguration;
+    nchw_to_nhwc16_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(x), static_cast<uint4*>(out), C, C8,
+                                                P, vec_ok);
     return cudaGetLastError();
 }
 
@@ -154,57 +212,59 @@ cudaError_t launch_window_cl16(const void* x, void* out, int N, int Ci, int H, i
 // Tensor-core filter: wq[co][t][c], c in [0, CP).
 //   im2win   t = kw, c = u*Ci8 + ci  (the window tensor's (u, ci) column order)
 //   implicit t = kh*Kw + kw, c = ci
-// Entries outside the real filter are zero.
-__global__ void pack_filter_tc_kernel(const uint16_t* __restrict__ w, uint16_t* __restrict__ wq, int Co, int Ci,
-                                      int Kh, int Kw, int Ci8, int taps, int CP, int im2win, long long total) {
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const int c = (int)(i % CP);
-        const int t = (int)((i / CP) % taps);
-        const int co = (int)(i / ((long long)CP * taps));
+// Entries outside the real filter are zero.  One block per output channel:
+// the channel's Ci*Kh*Kw filter (contiguous) is staged in shared memory, then
+// the repacked row is written contiguously.
+constexpr int kPackSmemElems = 16384;   // 32 KB of 16-bit filter per output channel
+
+__global__ void __launch_bounds__(256) pack_filter_tc_kernel(const uint16_t* __restrict__ w,
+                                                             uint16_t* __restrict__ wq, int Ci, int Kh, int Kw,
+                                                             int Ci8, int taps, int CP, int im2win) {
+    __shared__ uint16_t fw[kPackSmemElems];
+    const int co = blockIdx.x;
+    const int KK = Kh * Kw, n = Ci * KK;
+    const uint16_t* src = w + (long long)co * n;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) fw[i] = src[i];
+    __syncthreads();
+    uint16_t* dst = wq + (long long)co * taps * CP;
+    const int total = taps * CP;
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+        const int t = i / CP, c = i - t * CP;
         int ci, kh, kw;
         if (im2win) { kw = t; kh = c / Ci8; ci = c - kh * Ci8; }
         else        { kh = t / Kw; kw = t - kh * Kw; ci = c; }
-        uint16_t v = 0;
-        if (ci < Ci && kh < Kh) v = w[(((long long)co * Ci + ci) * Kh + kh) * Kw + kw];
-        wq[i] = v;
+        dst[i] = (ci < Ci && kh < Kh) ? fw[ci * KK + kh * Kw + kw] : (uint16_t)0;
     }
 }
 
 cudaError_t launch_pack_filter_tc(const void* w, void* wq, const conv2d_desc& d, bool im2win, cudaStream_t st) {
-    long long total = (long long)d.Co * d.taps * d.CP;
-    long long blocks = (total + 255) / 256, cap = (long long)device_sm_count() * 8;
-    int grid = (int)(blocks < cap ? blocks : cap);
-    pack_filter_tc_kernel<<<grid < 1 ? 1 : grid, 256, 0, st>>>(static_cast<const uint16_t*>(w),
-                                                                static_cast<uint16_t*>(wq), d.Co, d.Ci, d.Kh,
-                                                                d.Kw, d.Ci8, d.taps, d.CP, im2win ? 1 : 0, total);
+    if ((long long)d.Ci * d.Kh * d.Kw > kPackSmemElems) return cudaErrorInvalidValue;
+    pack_filter_tc_kernel<<<d.Co, 256, 0, st>>>(static_cast<const uint16_t*>(w), static_cast<uint16_t*>(wq), d.Ci,
+                                                d.Kh, d.Kw, d.Ci8, d.taps, d.CP, im2win ? 1 : 0);
     return cudaGetLastError();
 }
 
-// CUDA-core filter: wq[cb][ci][kh][kw][j] = w[cb*BCO + j][ci][kh][kw], BCO = 16 * warps
-// output channels per block, zero past Co.  A block's slice for a run of
-// input channels is then one contiguous range.
-__global__ void pack_filter_f32_kernel(const float* __restrict__ w, float* __restrict__ wq, int Co, int Ci,
-                                       int KK, int BCO, long long total) {
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const int j = (int)(i % BCO);
-        long long r = i / BCO;
-        const int k = (int)(r % KK); r /= KK;
-        const int ci = (int)(r % Ci);
-        const int cb = (int)(r / Ci);
+// CUDA-core filter: wq[cb][ci][k][j] = w[cb*BCO + j][ci][k] (k = kh*Kw + kw),
+// BCO = 16 * warps output channels per block, zero past Co, so that a block's
+// slice for a run of input channels is one contiguous range.  One block per
+// (cb, ci): reads BCO runs of Kh*Kw floats, writes Kh*Kw*BCO floats in order.
+__global__ void __launch_bounds__(256) pack_filter_f32_kernel(const float* __restrict__ w, float* __restrict__ wq,
+                                                              int Co, int Ci, int KK, int BCO) {
+    const int ci = blockIdx.x, cb = blockIdx.y;
+    float* dst = wq + ((long long)cb * Ci + ci) * KK * BCO;
+    const int total = KK * BCO;
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+        const int k = i / BCO, j = i - k * BCO;
         const int co = cb * BCO + j;
-        wq[i] = co < Co ? w[((long long)co * Ci + ci) * KK + k] : 0.f;
+        dst[i] = co < Co ? __ldg(w + ((long long)co * Ci + ci) * KK + k) : 0.f;
     }
 }
 
 cudaError_t launch_pack_filter_f32(const float* w, float* wq, const conv2d_desc& d, cudaStream_t st) {
     const int BCO = 16 * d.cc_warps;
     const int ncb = (d.Co + BCO - 1) / BCO;
-    long long total = (long long)ncb * d.Ci * d.Kh * d.Kw * BCO;
-    long long blocks = (total + 255) / 256, cap = (long long)device_sm_count() * 8;
-    int grid = (int)(blocks < cap ? blocks : cap);
-    pack_filter_f32_kernel<<<grid < 1 ? 1 : grid, 256, 0, st>>>(w, wq, d.Co, d.Ci, d.Kh * d.Kw, BCO, total);
+    if (ncb > 65535) return cudaErrorInvalidConfiguration;
+    pack_filter_f32_kernel<<<dim3(d.Ci, ncb), 256, 0, st>>>(w, wq, d.Co, d.Ci, d.Kh * d.Kw, BCO);
     return cudaGetLastError();
 }
 
