@@ -42,6 +42,7 @@ struct TcParams {
     int n_n_tiles, n_tiles;
     int n_cchunks, n_kchunks, CP, Kw, s, p;
     int im2win;
+    int vec_store;      // Ho*Wo % 8 == 0: 8-pixel groups never straddle an image, 16-byte stores
     void* y;
 };
 
@@ -52,7 +53,9 @@ struct TcConfig {
     static constexpr int kBBytes = BN * kTcBlockK * 2;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kTmemCols = 2 * BN;                    // two accumulators
-    static constexpr int kBarOffset = kStages * kStageBytes;
+    static constexpr int kEpiOffset = kStages * kStageBytes;    // epilogue staging: 32 channels x 128 pixels
+    static constexpr int kEpiBytes = 32 * kTcBlockM * 2;
+    static constexpr int kBarOffset = kEpiOffset + kEpiBytes;
     static constexpr int kSmemBytes = kBarOffset + 256 + 1024;  // barriers + alignment slack
 };
 
@@ -174,38 +177,78 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        // Each 32-column chunk of the accumulator (32 output channels x 128
+        // pixels) is rounded, staged in shared memory as [channel][pixel] and
+        // written as whole 256-byte channel rows with 16-byte stores.  The
+        // four epilogue warps synchronise on named barrier 1; the per-tile
+        // barrier also ANDs the wait results so all four leave together.
         const int quarter = warp & 3;
+        const int et = threadIdx.x - 64;                 // 0..127
+        uint16_t* stage_out = reinterpret_cast<uint16_t*>(smem + Cfg::kEpiOffset);
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < prm.n_tiles; tile += gridDim.x) {
             const bool got = mbar_wait(accf_bar(acc), acc_phase, abort_flag);
-            __syncwarp();
-            if (!__all_sync(0xffffffffu, got)) break;
+            if (!named_bar_and(1, 128, got)) break;
             tc_fence_after();
             const int m0 = (tile / prm.n_n_tiles) * kTcBlockM;
             const int n0 = (tile % prm.n_n_tiles) * BN;
-            const int m = m0 + quarter * 32 + lane;
-            const bool m_ok = m < prm.M;
-            const int img = m_ok ? m / prm.HoWo : 0;
-            const int r = m_ok ? m - img * prm.HoWo : 0;
-            uint16_t* out = static_cast<uint16_t*>(prm.y) + ((long long)img * prm.Co) * prm.HoWo + r;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+            if (prm.vec_store) {
+                const int grp = et & 15;                    // this thread's 8-pixel group
+                const int mg = m0 + 8 * grp;
+                const bool g_ok = mg < prm.M;
+                const int img = g_ok ? mg / prm.HoWo : 0;
+                const int r = g_ok ? mg - img * prm.HoWo : 0;
+                uint16_t* gbase = static_cast<uint16_t*>(prm.y) + ((long long)img * prm.Co) * prm.HoWo + r;
 #pragma unroll 1
-            for (int cc = 0; cc < BN / 32; ++cc) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(t_row + cc * 32, v);
-                tmem_ld_wait();
-                const int cob = n0 + cc * 32;
-                if (m_ok) {
+                for (int cc = 0; cc < BN / 32; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(t_row + cc * 32, v);
+                    tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const int co = cob + j;
-                        if (co < prm.Co) {
-                            const float f = __uint_as_float(v[j]);
-                            uint16_t h;
-                            if (BF16) h = __bfloat16_as_ushort(__float2bfloat16_rn(f));
-                            else      h = __half_as_ushort(__float2half_rn(f));
-                            out[(long long)co * prm.HoWo] = h;
+                        const float f = __uint_as_float(v[j]);
+                        uint16_t h;
+                        if (BF16) h = __bfloat16_as_ushort(__float2bfloat16_rn(f));
+                        else      h = __half_as_ushort(__float2half_rn(f));
+                        stage_out[j * kTcBlockM + quarter * 32 + lane] = h;
+                    }
+                    named_bar_sync(1, 128);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int row = (et >> 4) + 8 * i;
+                        const int co = n0 + cc * 32 + row;
+                        if (g_ok && co < prm.Co) {
+                            const uint4 val = *reinterpret_cast<const uint4*>(stage_out + row * kTcBlockM + 8 * grp);
+                            *reinterpret_cast<uint4*>(gbase + (long long)co * prm.HoWo) = val;
+                        }
+                    }
+                    named_bar_sync(1, 128);
+                }
+            } else {
+                const int m = m0 + quarter * 32 + lane;
+                const bool m_ok = m < prm.M;
+                const int img = m_ok ? m / prm.HoWo : 0;
+                const int r = m_ok ? m - img * prm.HoWo : 0;
+                uint16_t* out = static_cast<uint16_t*>(prm.y) + ((long long)img * prm.Co) * prm.HoWo + r;
+#pragma unroll 1
+                for (int cc = 0; cc < BN / 32; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(t_row + cc * 32, v);
+                    tmem_ld_wait();
+                    const int cob = n0 + cc * 32;
+                    if (m_ok) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int co = cob + j;
+                            if (co < prm.Co) {
+                                const float f = __uint_as_float(v[j]);
+                                uint16_t h;
+                                if (BF16) h = __bfloat16_as_ushort(__float2bfloat16_rn(f));
+                                else      h = __half_as_ushort(__float2half_rn(f));
+                                out[(long long)co * prm.HoWo] = h;
+                            }
                         }
                     }
                 }
@@ -321,6 +364,7 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     prm.CP = d.CP; prm.Kw = d.Kw; prm.s = d.s; prm.p = d.p;
     prm.im2win = im2win ? 1 : 0;
     prm.y = y;
+    prm.vec_store = ((prm.HoWo % 8) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) ? 1 : 0;
     int grid = device_sm_count();
     if (grid > prm.n_tiles) grid = prm.n_tiles;
 
