@@ -71,7 +71,7 @@ conv2d_status finalize(conv2d_desc& d) {
         d.ws_weights = (size_t)(ncb * bco * d.Ci * d.Kh * d.Kw * 4);
         if (d.algo == CONV2D_ALGO_IM2WIN_FP32_CC) {
             const long long strips = (long long)d.N * d.Ci * d.Ho * d.Lp;
-            if (strips > kMaxElems * 4) return CONV2D_ERR_UNSUPPORTED;
+            if (strips / 4 > kMaxElems) return CONV2D_ERR_UNSUPPORTED;   // 32-bit vector index
             d.ws_input = (size_t)strips * 4;
         } else {
             if (d.W % 4 != 0) return CONV2D_ERR_UNSUPPORTED;    // 16-byte row pitch for the row copies

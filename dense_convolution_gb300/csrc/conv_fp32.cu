@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(256) conv_fp32_kernel(const Fp32Params prm,
         if (!IM2WIN) tma_prefetch_desc(&xmap);
     }
     __syncthreads();
+    pdl_wait();   // the repacked filter / strips come from the kernels launched just before
 
     auto issue = [&](int k) {
         const int st = k & 1;
@@ -214,8 +215,7 @@ static cudaError_t launch_fp32_inst(const Fp32Params& prm, const CUtensorMap& ma
     auto kern = conv_fp32_kernel<KW, S, WPT, IM2WIN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)blocks, threads, smem, st>>>(prm, map);
-    return cudaGetLastError();
+    return launch_after(kern, dim3((unsigned)blocks), dim3(threads), smem, st, prm, map);
 }
 
 template <int KW, int S, bool IM2WIN>

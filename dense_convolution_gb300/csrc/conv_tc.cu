@@ -97,6 +97,9 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Operands (window / NHWC tensor, repacked filter) come from the kernels
+    // launched just before this one; the set-up above overlapped their tail.
+    pdl_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -308,8 +311,7 @@ static cudaError_t launch_tc_inst(const CUtensorMap& a, const CUtensorMap& b, co
     const int smem = TcConfig<BN>::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, 192, smem, st>>>(a, b, prm);
-    return cudaGetLastError();
+    return launch_after(kern, dim3(grid), dim3(192), smem, st, a, b, prm);
 }
 
 conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* wq, void* y, bool im2win,

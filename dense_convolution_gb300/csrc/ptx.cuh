@@ -43,6 +43,17 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Allow the next kernel in the stream to start launching (no-op without PDL).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the preceding kernel has completed and its writes are visible
+// (no-op when this kernel was not launched as a dependent).
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -13,23 +13,28 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace conv2d_gb300 {
 
 // ---------------------------------------------------------------- fp32 strips
-// One block per strip (n, ci, ho); one thread writes one 16-byte vector (4
-// consecutive strip elements), so a warp writes 512 contiguous bytes.  Reads
-// walk Kh neighbouring rows and are served by L1/L2.
-__global__ void __launch_bounds__(128) im2win_strips_f32_kernel(const float* __restrict__ x,
+// One thread writes one 16-byte vector (4 consecutive strip elements) and the
+// grid strides over all vectors, so consecutive threads write consecutive
+// bytes across strip boundaries.  Reads walk Kh neighbouring input rows and
+// are served by L1/L2.  32-bit index arithmetic (the launcher checks the
+// vector count fits).
+__global__ void __launch_bounds__(256) im2win_strips_f32_kernel(const float* __restrict__ x,
                                                                 float4* __restrict__ xw, int Ci, int H, int W,
-                                                                int Ho, int Kh, int s, int p, int Wp, int Lp) {
-    const long long strip = blockIdx.x;                 // (n*Ci + ci)*Ho + ho
-    const int ho = (int)(strip % Ho);
-    const long long nc = strip / Ho;
-    const float* plane = x + nc * (long long)H * W;
-    float4* out = xw + strip * (Lp >> 2);
-    for (int q = threadIdx.x; q < (Lp >> 2); q += blockDim.x) {
-        const int e = q * 4;
+                                                                int Ho, int Kh, int s, int p, int Wp, int Lp,
+                                                                int total_vec) {
+    pdl_launch_dependents();
+    const int Lv = Lp >> 2;
+    for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < total_vec; q += gridDim.x * blockDim.x) {
+        const int strip = q / Lv;                       // (n*Ci + ci)*Ho + ho
+        const int e = (q - strip * Lv) * 4;
+        const int nc = strip / Ho;
+        const int ho = strip - nc * Ho;
+        const float* plane = x + (long long)nc * H * W;
         int kx = e / Kh, u = e - kx * Kh;
         float v[4];
 #pragma unroll
@@ -40,16 +45,19 @@ __global__ void __launch_bounds__(128) im2win_strips_f32_kernel(const float* __r
             v[j] = val;
             if (++u == Kh) { u = 0; ++kx; }
         }
-        out[q] = make_float4(v[0], v[1], v[2], v[3]);
+        xw[q] = make_float4(v[0], v[1], v[2], v[3]);
     }
+    pdl_wait();   // complete only after the filter repack launched before us
 }
 
 cudaError_t launch_im2win_strips_f32(const float* x, float* xw, const conv2d_desc& d, cudaStream_t st) {
-    const long long strips = (long long)d.N * d.Ci * d.Ho;
-    if (strips > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    im2win_strips_f32_kernel<<<(unsigned)strips, 128, 0, st>>>(x, reinterpret_cast<float4*>(xw), d.Ci, d.H, d.W,
-                                                                d.Ho, d.Kh, d.s, d.p, d.Wp, d.Lp);
-    return cudaGetLastError();
+    const long long total_vec = (long long)d.N * d.Ci * d.Ho * (d.Lp / 4);
+    if (total_vec > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const long long blocks = (total_vec + 255) / 256, cap = (long long)device_sm_count() * 16;
+    const int grid = (int)(blocks < cap ? blocks : cap);
+    return launch_after(im2win_strips_f32_kernel, dim3(grid < 1 ? 1 : grid), dim3(256), 0, st, x,
+                        reinterpret_cast<float4*>(xw), d.Ci, d.H, d.W, d.Ho, d.Kh, d.s, d.p, d.Wp, d.Lp,
+                        (int)total_vec);
 }
 
 // ---------------------------------------------------------------- 16-bit NCHW -> NHWC (channels padded to 8)
@@ -66,6 +74,7 @@ __global__ void __launch_bounds__(256) nchw_to_nhwc16_kernel(const uint16_t* __r
                                                              int vec_ok) {
     __shared__ uint32_t tile[kNhwcTile * kNhwcPitch / 2];
     uint16_t* t16 = reinterpret_cast<uint16_t*>(tile);
+    pdl_launch_dependents();
     const int p0 = blockIdx.x * kNhwcTile, c0 = blockIdx.y * kNhwcTile;
     const long long n = blockIdx.z;
     const uint16_t* xn = x + n * (long long)C * P;
@@ -103,6 +112,7 @@ __global__ void __launch_bounds__(256) nchw_to_nhwc16_kernel(const uint16_t* __r
             out[((n * P + pp) * C8 + cc) >> 3] = make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
+    pdl_wait();   // complete only after the filter repack launched before us
 }
 
 cudaError_t launch_nchw_to_nhwc16(const void* x, void* out, int N, int C, int H, int W, int C8, cudaStream_t st) {
@@ -110,9 +120,8 @@ cudaError_t launch_nchw_to_nhwc16(const void* x, void* out, int N, int C, int H,
     const int vec_ok = (P % 8 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) ? 1 : 0;
     dim3 grid((P + kNhwcTile - 1) / kNhwcTile, (C8 + kNhwcTile - 1) / kNhwcTile, N);
     if (grid.z > 65535 || grid.y > 65535) return cudaErrorInvalidConfiguration;
-    nchw_to_nhwc16_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(x), static_cast<uint4*>(out), C, C8,
-                                                P, vec_ok);
-    return cudaGetLastError();
+    return launch_after(nchw_to_nhwc16_kernel, grid, dim3(256), 0, st, static_cast<const uint16_t*>(x),
+                        static_cast<uint4*>(out), C, C8, P, vec_ok);
 }
 
 // ---------------------------------------------------------------- 16-bit channels-innermost window
@@ -127,6 +136,7 @@ __global__ void __launch_bounds__(256) window_cl16_tiled_kernel(const uint16_t* 
                                                                 int Ci8, int R, int Wq, int Kh, int s, int p,
                                                                 int n_xt, int n_ct) {
     __shared__ uint16_t tile[kWinTileC][kWinTileX + 2];
+    pdl_launch_dependents();
     long long b = blockIdx.x;
     const int xt = (int)(b % n_xt); b /= n_xt;
     const int ct = (int)(b % n_ct); b /= n_ct;
@@ -157,6 +167,7 @@ __global__ void __launch_bounds__(256) window_cl16_tiled_kernel(const uint16_t* 
         long long o = ((nr * Wq + kx) * Kh + u) * (long long)Ci8 + cc;
         out[o >> 3] = make_uint4(w[0], w[1], w[2], w[3]);
     }
+    pdl_wait();   // complete only after the filter repack launched before us
 }
 
 // Small-channel version (Ci8 <= 16): one thread builds one 8-channel vector;
@@ -165,6 +176,7 @@ __global__ void __launch_bounds__(256) window_cl16_small_kernel(const uint16_t* 
                                                                 uint4* __restrict__ out, int Ci, int H, int W,
                                                                 int Ci8, int R, int Wq, int Kh, int s, int p,
                                                                 long long total_vec) {
+    pdl_launch_dependents();
     const int cgs = Ci8 / 8;
     for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total_vec;
          q += (long long)gridDim.x * blockDim.x) {
@@ -186,6 +198,7 @@ __global__ void __launch_bounds__(256) window_cl16_small_kernel(const uint16_t* 
         }
         out[q] = make_uint4(w[0], w[1], w[2], w[3]);
     }
+    pdl_wait();   // complete only after the filter repack launched before us
 }
 
 cudaError_t launch_window_cl16(const void* x, void* out, int N, int Ci, int H, int W, int Ci8, int R, int Wq,
@@ -196,16 +209,15 @@ cudaError_t launch_window_cl16(const void* x, void* out, int N, int Ci, int H, i
         long long total_vec = (long long)N * R * Wq * Kh * (Ci8 / 8);
         long long blocks = (total_vec + 255) / 256, cap = (long long)device_sm_count() * 16;
         int grid = (int)(blocks < cap ? blocks : cap);
-        window_cl16_small_kernel<<<grid < 1 ? 1 : grid, 256, 0, st>>>(xi, o, Ci, H, W, Ci8, R, Wq, Kh, s, p,
-                                                                       total_vec);
+        return launch_after(window_cl16_small_kernel, dim3(grid < 1 ? 1 : grid), dim3(256), 0, st, xi, o, Ci, H, W,
+                            Ci8, R, Wq, Kh, s, p, total_vec);
     } else {
         int n_xt = (Wq + kWinTileX - 1) / kWinTileX, n_ct = (Ci8 + kWinTileC - 1) / kWinTileC;
         long long blocks = (long long)n_xt * n_ct * Kh * N * R;
         if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-        window_cl16_tiled_kernel<<<(unsigned)blocks, 256, 0, st>>>(xi, o, Ci, H, W, Ci8, R, Wq, Kh, s, p, n_xt,
-                                                                    n_ct);
+        return launch_after(window_cl16_tiled_kernel, dim3((unsigned)blocks), dim3(256), 0, st, xi, o, Ci, H, W, Ci8,
+                            R, Wq, Kh, s, p, n_xt, n_ct);
     }
-    return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- filter repacks
@@ -221,6 +233,7 @@ __global__ void __launch_bounds__(256) pack_filter_tc_kernel(const uint16_t* __r
                                                              uint16_t* __restrict__ wq, int Ci, int Kh, int Kw,
                                                              int Ci8, int taps, int CP, int im2win) {
     __shared__ uint16_t fw[kPackSmemElems];
+    pdl_launch_dependents();
     const int co = blockIdx.x;
     const int KK = Kh * Kw, n = Ci * KK;
     const uint16_t* src = w + (long long)co * n;
@@ -250,6 +263,7 @@ cudaError_t launch_pack_filter_tc(const void* w, void* wq, const conv2d_desc& d,
 // (cb, ci): reads BCO runs of Kh*Kw floats, writes Kh*Kw*BCO floats in order.
 __global__ void __launch_bounds__(256) pack_filter_f32_kernel(const float* __restrict__ w, float* __restrict__ wq,
                                                               int Co, int Ci, int KK, int BCO) {
+    pdl_launch_dependents();
     const int ci = blockIdx.x, cb = blockIdx.y;
     float* dst = wq + ((long long)cb * Ci + ci) * KK * BCO;
     const int total = KK * BCO;
