@@ -15,7 +15,19 @@ namespace {
 
 constexpr long long kMaxElems = 0x7fffffffLL;   // kernels index tensors with 32-bit element counts
 
-bool is_tc(conv2d_algo a) { return a == CONV2D_ALGO_IM2WIN_TC || a == CONV2D_ALGO_IMPLICIT_TC; }
+bool is_tc(conv2d_algo a) {
+    return a == CONV2D_ALGO_IM2WIN_TC || a == CONV2D_ALGO_IMPLICIT_TC || a == CONV2D_ALGO_PADDED_TC;
+}
+
+// Padded algorithm geometry: row pitch W+2p, rounded up to 4 when Wo % 4 == 0
+// so that 4-pixel output groups never straddle a row (8-byte stores).
+int padded_pitch(const conv2d_desc& d) { return d.Wo % 4 == 0 ? (d.Wp + 3) / 4 * 4 : d.Wp; }
+
+// Fraction of the padded grid's virtual pixels that are junk (not outputs).
+double padded_waste(const conv2d_desc& d) {
+    const double grid = (double)(d.H + 2 * d.p) * padded_pitch(d);
+    return 1.0 - (double)d.Ho * d.Wo / grid;
+}
 
 // Fraction of the tensor-core K extent that holds real filter taps, for the
 // two operand sources (the rest is zero fill up to the 64-element chunk).
@@ -47,6 +59,9 @@ bool tc_shape_ok(const conv2d_desc& d, bool im2win) {
 conv2d_algo resolve_auto(const conv2d_desc& d) {
     if (d.dtype == CONV2D_F32) return CONV2D_ALGO_IM2WIN_FP32_CC;
     if (d.layout == CONV2D_LAYOUT_NHWC) return CONV2D_ALGO_IMPLICIT_TC;
+    // Stride 1: tiled operand loads over a padded copy beat im2col-mode loads
+    // unless the padded grid adds too many junk rows (measured on GB300).
+    if (d.s == 1 && padded_waste(d) <= 0.15 && (d.Ci + 7) / 8 * 8 >= 64) return CONV2D_ALGO_PADDED_TC;
     const bool imp_ok = tc_shape_ok(d, false), win_ok = tc_shape_ok(d, true);
     if (imp_ok && (!win_ok || tc_k_efficiency(d, false) >= tc_k_efficiency(d, true)))
         return CONV2D_ALGO_IMPLICIT_TC;
@@ -80,7 +95,12 @@ conv2d_status finalize(conv2d_desc& d) {
         }
     } else {
         const bool im2win = d.algo == CONV2D_ALGO_IM2WIN_TC;
-        if (!tc_shape_ok(d, im2win)) return CONV2D_ERR_UNSUPPORTED;
+        const bool padded = d.algo == CONV2D_ALGO_PADDED_TC;
+        if (padded) {
+            if (d.s != 1 || d.layout != CONV2D_LAYOUT_NCHW) return CONV2D_ERR_UNSUPPORTED;
+        } else if (!tc_shape_ok(d, im2win)) {
+            return CONV2D_ERR_UNSUPPORTED;
+        }
         d.Ci8 = (d.Ci + 7) / 8 * 8;
         d.taps = im2win ? d.Kw : d.Kh * d.Kw;
         const long long chunk = im2win ? (long long)d.Kh * d.Ci8 : d.Ci8;
@@ -91,7 +111,14 @@ conv2d_status finalize(conv2d_desc& d) {
         const long long wq = (long long)d.Co * d.taps * d.CP;
         if (wq > kMaxElems) return CONV2D_ERR_UNSUPPORTED;
         d.ws_weights = (size_t)wq * 2;
-        if (im2win) {
+        if (padded) {
+            d.Hp = d.H + 2 * d.p;
+            d.Wq = padded_pitch(d);
+            const long long rows = (long long)d.N * d.Hp * d.Wq;
+            if (rows + (long long)d.Kh * d.Wq + d.Kw + kTcBlockM > kMaxElems) return CONV2D_ERR_UNSUPPORTED;
+            if (rows * d.Ci8 > kMaxElems * 4) return CONV2D_ERR_UNSUPPORTED;
+            d.ws_input = (size_t)(rows * d.Ci8) * 2;
+        } else if (im2win) {
             const long long win = (long long)d.N * d.Ho * d.Wp * d.Kh * d.Ci8;
             if (win > kMaxElems * 4) return CONV2D_ERR_UNSUPPORTED;
             d.ws_input = (size_t)win * 2;
@@ -115,7 +142,7 @@ CONV2D_API conv2d_status conv2d_desc_create(conv2d_desc_t* out, int N, int Cin, 
     if (N < 1 || Cin < 1 || H < 1 || W < 1 || Cout < 1 || Kh < 1 || Kw < 1 || stride < 1 || pad < 0)
         return CONV2D_ERR_BAD_PARAM;
     if (dtype != CONV2D_F32 && dtype != CONV2D_F16 && dtype != CONV2D_BF16) return CONV2D_ERR_BAD_PARAM;
-    if (algo < CONV2D_ALGO_AUTO || algo > CONV2D_ALGO_IMPLICIT_FP32_CC) return CONV2D_ERR_BAD_PARAM;
+    if (algo < CONV2D_ALGO_AUTO || algo > CONV2D_ALGO_PADDED_TC) return CONV2D_ERR_BAD_PARAM;
     const long long Hp = (long long)H + 2LL * pad, Wp = (long long)W + 2LL * pad;
     if (Hp < Kh || Wp < Kw || Wp > 0x7fffffffLL) return CONV2D_ERR_BAD_PARAM;
     const long long Ho = (Hp - Kh) / stride + 1, Wo = (Wp - Kw) / stride + 1;
@@ -212,7 +239,7 @@ conv2d_status fwd_impl(conv2d_desc_t dp, const void* x, const void* w, void* y, 
             e = launch_pack_filter_tc(w, wq, d, true, st);
             if (e == cudaSuccess) e = launch_window_cl16(x, win, d.N, d.Ci, d.H, d.W, d.Ci8, d.Ho, d.Wp, d.Kh, d.s, d.p, st);
             if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
-            if (e == cudaSuccess) s = launch_conv_tc(d, win, wq, y, true, st);
+            if (e == cudaSuccess) s = launch_conv_tc(d, win, wq, y, 1, st);
             break;
         case CONV2D_ALGO_IMPLICIT_TC: {
             e = launch_pack_filter_tc(w, wq, d, false, st);
@@ -222,9 +249,15 @@ conv2d_status fwd_impl(conv2d_desc_t dp, const void* x, const void* w, void* y, 
                 src = win;
             }
             if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
-            if (e == cudaSuccess) s = launch_conv_tc(d, src, wq, y, false, st);
+            if (e == cudaSuccess) s = launch_conv_tc(d, src, wq, y, 0, st);
             break;
         }
+        case CONV2D_ALGO_PADDED_TC:
+            e = launch_pack_filter_tc(w, wq, d, false, st);
+            if (e == cudaSuccess) e = launch_nchw_to_padded_nhwc16(x, win, d, st);
+            if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
+            if (e == cudaSuccess) s = launch_conv_tc(d, win, wq, y, 2, st);
+            break;
         default:
             return CONV2D_ERR_BAD_PARAM;
     }
@@ -249,7 +282,7 @@ CONV2D_API conv2d_status conv2d_fwd_profiled(conv2d_desc_t d, const void* x, con
 CONV2D_API conv2d_status conv2d_launches_per_call(conv2d_desc_t d, int* launches) {
     if (!d || !launches) return CONV2D_ERR_NULL_PTR;
     int n = 2;   // filter repack + contraction
-    if (d->algo == CONV2D_ALGO_IM2WIN_FP32_CC || d->algo == CONV2D_ALGO_IM2WIN_TC ||
+    if (d->algo == CONV2D_ALGO_IM2WIN_FP32_CC || d->algo == CONV2D_ALGO_IM2WIN_TC || d->algo == CONV2D_ALGO_PADDED_TC ||
         (d->algo == CONV2D_ALGO_IMPLICIT_TC && d->layout == CONV2D_LAYOUT_NCHW))
         ++n;
     *launches = n;

@@ -41,8 +41,10 @@ struct TcParams {
     int M, HoWo, Ho, Wo, Co;
     int n_n_tiles, n_tiles;
     int n_cchunks, n_kchunks, CP, Kw, s, p;
-    int im2win;
-    int vec_store;      // Ho*Wo % 8 == 0: 8-pixel groups never straddle an image, 16-byte stores
+    int amode;          // A source: 0 implicit (im2col over NHWC X), 1 im2win (im2col over the window
+                        // tensor), 2 padded (tiled boxes over the zero-padded NHWC copy)
+    int N, Wq, HpWq;    // padded mode: batch, row pitch and image pitch of the padded grid
+    int vec_store;      // modes 0/1: Ho*Wo % 8 == 0 (16-byte stores); mode 2: Wo % 4 == 0 (8-byte stores)
     void* y;
 };
 
@@ -111,8 +113,13 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
             for (int tile = blockIdx.x; tile < prm.n_tiles && ok; tile += gridDim.x) {
                 const int m0 = (tile / prm.n_n_tiles) * kTcBlockM;
                 const int n0 = (tile % prm.n_n_tiles) * BN;
-                const int img = m0 / prm.HoWo, r = m0 - img * prm.HoWo;
-                const int ho = r / prm.Wo, wo = r - ho * prm.Wo;
+                int img = 0, ho = 0, wo = 0;
+                if (prm.amode != 2) {
+                    img = m0 / prm.HoWo;
+                    const int r = m0 - img * prm.HoWo;
+                    ho = r / prm.Wo;
+                    wo = r - ho * prm.Wo;
+                }
                 for (int kc = 0; kc < prm.n_kchunks; ++kc) {
                     const int t = kc / prm.n_cchunks;
                     const int c0 = (kc - t * prm.n_cchunks) * kTcBlockK;
@@ -120,7 +127,11 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
                     mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
                     const uint32_t a_dst = smem_addr(smem + stage * Cfg::kStageBytes);
                     const uint32_t b_dst = a_dst + Cfg::kABytes;
-                    if (prm.im2win) {
+                    if (prm.amode == 2) {
+                        // Virtual pixel q reads padded pixel q + kh*Wq + kw: one tiled box per tap.
+                        const int kh = t / prm.Kw, kw = t - kh * prm.Kw;
+                        tma_load_2d(a_dst, &amap, full_bar(stage), c0, m0 + kh * prm.Wq + kw);
+                    } else if (prm.amode == 1) {
                         tma_load_im2col_4d(a_dst, &amap, full_bar(stage), c0, wo * prm.s, ho, img, (uint16_t)t, 0);
                     } else {
                         const int kh = t / prm.Kw, kw = t - kh * prm.Kw;
@@ -197,7 +208,54 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
             const int m0 = (tile / prm.n_n_tiles) * kTcBlockM;
             const int n0 = (tile % prm.n_n_tiles) * BN;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
-            if (prm.vec_store) {
+            if (prm.amode == 2) {
+                // Rows are virtual pixels of the padded grid [N][Hp][Wq]; only
+                // those with y < Ho and x < Wo are outputs.  With Wo % 4 == 0 a
+                // 4-pixel group is all-valid or all-junk: 8-byte stores.
+                const int g = et & 31;
+                const int qg = m0 + 4 * g;
+                const int ng = qg / prm.HpWq, rg = qg - ng * prm.HpWq;
+                const int yg = rg / prm.Wq, xg = rg - yg * prm.Wq;
+                const bool g_ok = ng < prm.N && yg < prm.Ho && xg < prm.Wo;
+                uint16_t* gbase = static_cast<uint16_t*>(prm.y) + (long long)ng * prm.Co * prm.HoWo + yg * prm.Wo + xg;
+                const int qp = m0 + et;                      // scalar fallback: one pixel per thread
+                const int np = qp / prm.HpWq, rp = qp - np * prm.HpWq;
+                const int yp = rp / prm.Wq, xp = rp - yp * prm.Wq;
+                const bool p_ok = np < prm.N && yp < prm.Ho && xp < prm.Wo;
+                uint16_t* pbase = static_cast<uint16_t*>(prm.y) + (long long)np * prm.Co * prm.HoWo + yp * prm.Wo + xp;
+#pragma unroll 1
+                for (int cc = 0; cc < BN / 32; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(t_row + cc * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float f = __uint_as_float(v[j]);
+                        uint16_t h;
+                        if (BF16) h = __bfloat16_as_ushort(__float2bfloat16_rn(f));
+                        else      h = __half_as_ushort(__float2half_rn(f));
+                        stage_out[j * kTcBlockM + quarter * 32 + lane] = h;
+                    }
+                    named_bar_sync(1, 128);
+                    if (prm.vec_store) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int row = (et >> 5) + 4 * i;
+                            const int co = n0 + cc * 32 + row;
+                            if (g_ok && co < prm.Co)
+                                *reinterpret_cast<uint2*>(gbase + (long long)co * prm.HoWo) =
+                                    *reinterpret_cast<const uint2*>(stage_out + row * kTcBlockM + 4 * g);
+                        }
+                    } else if (p_ok) {
+#pragma unroll 4
+                        for (int row = 0; row < 32; ++row) {
+                            const int co = n0 + cc * 32 + row;
+                            if (co < prm.Co) pbase[(long long)co * prm.HoWo] = stage_out[row * kTcBlockM + et];
+                        }
+                    }
+                    named_bar_sync(1, 128);
+                }
+            } else if (prm.vec_store) {
                 const int grp = et & 15;                    // this thread's 8-pixel group
                 const int mg = m0 + 8 * grp;
                 const bool g_ok = mg < prm.M;
@@ -314,8 +372,9 @@ static cudaError_t launch_tc_inst(const CUtensorMap& a, const CUtensorMap& b, co
     return launch_after(kern, dim3(grid), dim3(192), smem, st, a, b, prm);
 }
 
-conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* wq, void* y, bool im2win,
+conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* wq, void* y, int amode,
                              cudaStream_t st) {
+    const bool im2win = amode == 1;
     auto enc_tiled = reinterpret_cast<PFN_encodeTiled_t>(driver_entry("cuTensorMapEncodeTiled"));
     auto enc_im2col = reinterpret_cast<PFN_encodeIm2col_t>(driver_entry("cuTensorMapEncodeIm2col"));
     if (!enc_tiled || !enc_im2col) return CONV2D_ERR_CUDA;
@@ -340,9 +399,21 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     }
     cuuint64_t adims[4] = {C, Wd, Hd, (cuuint64_t)d.N};
     cuuint64_t astr[3] = {C * 2, C * 2 * Wd, C * 2 * Wd * Hd};
-    CUresult r = enc_im2col(&amap, dt, 4, const_cast<void*>(src), adims, astr, lower, upper, kTcBlockK,
-                            kTcBlockM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r;
+    if (amode == 2) {
+        // Padded channels-last copy viewed as [N*Hp*Wq pixel rows][Ci8 channels].
+        cuuint64_t pdims[2] = {(cuuint64_t)d.Ci8, (cuuint64_t)d.N * d.Hp * d.Wq};
+        cuuint64_t pstr[1] = {(cuuint64_t)d.Ci8 * 2};
+        cuuint32_t pbox[2] = {(cuuint32_t)kTcBlockK, (cuuint32_t)kTcBlockM};
+        cuuint32_t pestr[2] = {1, 1};
+        r = enc_tiled(&amap, dt, 2, const_cast<void*>(src), pdims, pstr, pbox, pestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        r = enc_im2col(&amap, dt, 4, const_cast<void*>(src), adims, astr, lower, upper, kTcBlockK, kTcBlockM, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (r != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
 
     // B: repacked filter [Co][taps*CP], K-major, box 64 x BN.
@@ -356,7 +427,11 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     if (r != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
 
     TcParams prm{};
-    prm.M = d.N * d.Ho * d.Wo;
+    // M runs over output pixels, or over the padded grid up to the last output (padded mode).
+    prm.M = amode == 2 ? (d.N - 1) * d.Hp * d.Wq + (d.Ho - 1) * d.Wq + d.Wo : d.N * d.Ho * d.Wo;
+    prm.N = d.N;
+    prm.Wq = d.Wq;
+    prm.HpWq = d.Hp * d.Wq;
     prm.HoWo = d.Ho * d.Wo; prm.Ho = d.Ho; prm.Wo = d.Wo; prm.Co = d.Co;
     prm.n_n_tiles = (d.Co + d.BN - 1) / d.BN;
     const int n_m_tiles = (prm.M + kTcBlockM - 1) / kTcBlockM;
@@ -364,9 +439,12 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     prm.n_cchunks = d.CP / kTcBlockK;
     prm.n_kchunks = d.taps * prm.n_cchunks;
     prm.CP = d.CP; prm.Kw = d.Kw; prm.s = d.s; prm.p = d.p;
-    prm.im2win = im2win ? 1 : 0;
+    prm.amode = amode;
     prm.y = y;
-    prm.vec_store = ((prm.HoWo % 8) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) ? 1 : 0;
+    if (amode == 2)
+        prm.vec_store = ((d.Wo % 4) == 0 && (d.Wq % 4) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) ? 1 : 0;
+    else
+        prm.vec_store = ((prm.HoWo % 8) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) ? 1 : 0;
     int grid = device_sm_count();
     if (grid > prm.n_tiles) grid = prm.n_tiles;
 

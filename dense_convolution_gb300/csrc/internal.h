@@ -25,6 +25,7 @@ struct conv2d_desc {
     int taps;             // filter taps per K-chunk group: Kw (im2win) or Kh*Kw (implicit)
     int CP;               // channel extent per tap, padded to the 64-element K chunk
     int BN;               // output channels per MMA tile (64, 128 or 256)
+    int Hp, Wq;           // padded algorithm: padded height H+2p, row pitch (W+2p rounded up to 4 when Wo % 4 == 0)
     // Workspace layout (bytes): packed filter at 0, input-side tensor after it.
     size_t ws_weights, ws_input_off, ws_input, ws_total;
 };
@@ -62,6 +63,7 @@ cudaError_t launch_im2win_strips_f32(const float* x, float* xw, const conv2d_des
 cudaError_t launch_window_cl16(const void* x, void* out, int N, int Ci, int H, int W, int Ci8, int R, int Wq,
                                int Kh, int s, int p, cudaStream_t st);
 cudaError_t launch_nchw_to_nhwc16(const void* x, void* out, int N, int C, int H, int W, int C8, cudaStream_t st);
+cudaError_t launch_nchw_to_padded_nhwc16(const void* x, void* out, const conv2d_desc& d, cudaStream_t st);
 cudaError_t launch_pack_filter_tc(const void* w, void* wq, const conv2d_desc& d, bool im2win, cudaStream_t st);
 cudaError_t launch_pack_filter_f32(const float* w, float* wq, const conv2d_desc& d, cudaStream_t st);
 
@@ -70,7 +72,7 @@ conv2d_status launch_conv_fp32(const conv2d_desc& d, const float* src, const flo
                                bool im2win, cudaStream_t st);
 
 // conv_tc.cu
-conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* wq, void* y, bool im2win,
+conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* wq, void* y, int amode,
                              cudaStream_t st);
 int device_sm_count();
 void* driver_entry(const char* name);

@@ -124,6 +124,57 @@ cudaError_t launch_nchw_to_nhwc16(const void* x, void* out, int N, int C, int H,
                         static_cast<uint4*>(out), C, C8, P, vec_ok);
 }
 
+// ---------------------------------------------------------------- 16-bit NCHW -> zero-padded NHWC
+// out[n][yy][xx][c] = X[n][c][yy-p][xx-p] (zero outside the image and for
+// c >= C), yy in [0, Hp), xx in [0, Wq): every output pixel of the padded
+// grid is written, borders included.  A block covers 64 padded pixels x 64
+// channels: reads run along image rows, writes are 16-byte channel vectors.
+__global__ void __launch_bounds__(256) nchw_to_padded_nhwc16_kernel(const uint16_t* __restrict__ x,
+                                                                    uint4* __restrict__ out, int C, int C8, int H,
+                                                                    int W, int Hp, int Wq, int p) {
+    __shared__ uint32_t tile[kNhwcTile * kNhwcPitch / 2];
+    uint16_t* t16 = reinterpret_cast<uint16_t*>(tile);
+    pdl_launch_dependents();
+    const int P = Hp * Wq;
+    const int p0 = blockIdx.x * kNhwcTile, c0 = blockIdx.y * kNhwcTile;
+    const long long n = blockIdx.z;
+    const int pl = threadIdx.x & 63;
+    const int q = p0 + pl;
+    const int yy = q / Wq, xx = q - yy * Wq;
+    const int y = yy - p, xw = xx - p;
+    const bool in = q < P && y >= 0 && y < H && xw >= 0 && xw < W;
+    const uint16_t* src = x + n * (long long)C * H * W + (in ? y * W + xw : 0);
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+        const int c = (threadIdx.x >> 6) + 4 * i;
+        const int cc = c0 + c;
+        t16[c * kNhwcPitch + pl] = (in && cc < C) ? src[(long long)cc * H * W] : (uint16_t)0;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int pl2 = threadIdx.x / 8 + 32 * i, cg = threadIdx.x % 8;
+        const int pp = p0 + pl2, cc = c0 + cg * 8;
+        if (pp < P && cc < C8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                w[j] = (uint32_t)t16[(cg * 8 + 2 * j) * kNhwcPitch + pl2] |
+                       ((uint32_t)t16[(cg * 8 + 2 * j + 1) * kNhwcPitch + pl2] << 16);
+            out[((n * P + pp) * C8 + cc) >> 3] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    pdl_wait();   // complete only after the filter repack launched before us
+}
+
+cudaError_t launch_nchw_to_padded_nhwc16(const void* x, void* out, const conv2d_desc& d, cudaStream_t st) {
+    const int P = d.Hp * d.Wq;
+    dim3 grid((P + kNhwcTile - 1) / kNhwcTile, (d.Ci8 + kNhwcTile - 1) / kNhwcTile, d.N);
+    if (grid.z > 65535 || grid.y > 65535) return cudaErrorInvalidConfiguration;
+    return launch_after(nchw_to_padded_nhwc16_kernel, grid, dim3(256), 0, st, static_cast<const uint16_t*>(x),
+                        static_cast<uint4*>(out), d.Ci, d.Ci8, d.H, d.W, d.Hp, d.Wq, d.p);
+}
+
 // ---------------------------------------------------------------- 16-bit channels-innermost window
 // Tiled version: a block transposes a 64-channel x 32-column tile of one input
 // row (reads coalesced along x) and writes it channel-innermost, one 16-byte
@@ -232,21 +283,34 @@ constexpr int kPackSmemElems = 16384;   // 32 KB of 16-bit filter per output cha
 __global__ void __launch_bounds__(256) pack_filter_tc_kernel(const uint16_t* __restrict__ w,
                                                              uint16_t* __restrict__ wq, int Ci, int Kh, int Kw,
                                                              int Ci8, int taps, int CP, int im2win) {
-    __shared__ uint16_t fw[kPackSmemElems];
+    __shared__ __align__(16) uint16_t fw[kPackSmemElems];
     pdl_launch_dependents();
     const int co = blockIdx.x;
     const int KK = Kh * Kw, n = Ci * KK;
     const uint16_t* src = w + (long long)co * n;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) fw[i] = src[i];
+    if ((n & 7) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(src);
+        for (int i = threadIdx.x; i < (n >> 3); i += blockDim.x) reinterpret_cast<uint4*>(fw)[i] = __ldg(s4 + i);
+    } else {
+        for (int i = threadIdx.x; i < n; i += blockDim.x) fw[i] = src[i];
+    }
     __syncthreads();
-    uint16_t* dst = wq + (long long)co * taps * CP;
-    const int total = taps * CP;
+    // One 16-byte vector = 8 consecutive packed channels of one tap.
+    uint4* dst = reinterpret_cast<uint4*>(wq + (long long)co * taps * CP);
+    const int cpv = CP >> 3, total = taps * cpv;
     for (int i = threadIdx.x; i < total; i += blockDim.x) {
-        const int t = i / CP, c = i - t * CP;
-        int ci, kh, kw;
-        if (im2win) { kw = t; kh = c / Ci8; ci = c - kh * Ci8; }
-        else        { kh = t / Kw; kw = t - kh * Kw; ci = c; }
-        dst[i] = (ci < Ci && kh < Kh) ? fw[ci * KK + kh * Kw + kw] : (uint16_t)0;
+        const int t = i / cpv, c0 = (i - t * cpv) * 8;
+        uint32_t v[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int c = c0 + j;
+            int ci, kh, kw;
+            if (im2win) { kw = t; kh = c / Ci8; ci = c - kh * Ci8; }
+            else        { kh = t / Kw; kw = t - kh * Kw; ci = c; }
+            const uint32_t h = (ci < Ci && kh < Kh) ? fw[ci * KK + kh * Kw + kw] : 0u;
+            v[j >> 1] |= h << (16 * (j & 1));
+        }
+        dst[i] = make_uint4(v[0], v[1], v[2], v[3]);
     }
 }
 

@@ -70,6 +70,12 @@ typedef enum { CONV2D_F32 = 0, CONV2D_F16 = 1, CONV2D_BF16 = 2 } conv2d_dtype;
  *                   of X when the input layout is NCHW.
  *  IMPLICIT_FP32_CC fp32 on CUDA cores, staging X's rows directly (no input
  *                   expansion); workspace: the repacked filter only.
+ *  PADDED_TC        fp16/bf16 on tcgen05 tensor cores, stride 1 and NCHW input
+ *                   only.  X is copied once into a zero-padded channels-last
+ *                   buffer; the GEMM rows walk the padded grid, so each filter
+ *                   tap's operand tile is one tiled TMA box at a constant
+ *                   shift (kh*pitch + kw) and the outputs at padded positions
+ *                   are discarded.  Workspace: repacked filter + padded copy.
  *  AUTO             resolved per shape when the descriptor is created
  *                   (conv2d_get_algo reports the choice). */
 typedef enum {
@@ -77,7 +83,8 @@ typedef enum {
     CONV2D_ALGO_IM2WIN_FP32_CC = 1,
     CONV2D_ALGO_IM2WIN_TC = 2,
     CONV2D_ALGO_IMPLICIT_TC = 3,
-    CONV2D_ALGO_IMPLICIT_FP32_CC = 4
+    CONV2D_ALGO_IMPLICIT_FP32_CC = 4,
+    CONV2D_ALGO_PADDED_TC = 5
 } conv2d_algo;
 
 /* Memory layout of X.  Y is always NCHW.  W is always [Cout][Cin][Kh][Kw]. */

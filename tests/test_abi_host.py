@@ -71,7 +71,9 @@ def test_out_dims_floor_rule(capi):
 def test_auto_choices_and_workspace(capi):
     cases = {
         # name: (shape, dtype, expected algo)
-        "resnet_f16": ((32, 64, 56, 56, 64, 3, 3, 1, 1), "f16", "implicit_tc"),
+        "resnet_f16": ((32, 64, 56, 56, 64, 3, 3, 1, 1), "f16", "padded_tc"),
+        "k1_f16": ((16, 128, 64, 64, 128, 1, 1, 1, 0), "f16", "padded_tc"),
+        "k3s2_f16": ((16, 128, 64, 64, 128, 3, 3, 2, 1), "f16", "implicit_tc"),
         "stem_f16": ((32, 3, 224, 224, 64, 7, 7, 2, 3), "f16", "im2win_tc"),
         "vgg_bf16": ((64, 512, 28, 28, 512, 3, 3, 1, 1), "bf16", "implicit_tc"),
         "resnet_f32": ((32, 64, 56, 56, 64, 3, 3, 1, 1), "f32", "im2win_fp32_cc"),
@@ -86,6 +88,10 @@ def test_auto_choices_and_workspace(capi):
             elem = 4 if dt == "f32" else 2
             im2win_tensor = N * Ci * Ho * (W + 2 * p) * Kh * elem
             assert ws > 0
+            if algo == "padded_tc":
+                ci8 = (Ci + 7) // 8 * 8
+                wq = (W + 2 * p + 3) // 4 * 4
+                assert ws >= N * (H + 2 * p) * wq * ci8 * 2    # zero-padded channels-last copy of X
             if algo == "implicit_tc":
                 ci8 = (Ci + 7) // 8 * 8
                 assert ws >= N * H * W * ci8 * 2          # channels-last copy of X
@@ -133,6 +139,21 @@ def test_fwd_argument_checks_before_launch(capi):
         with pytest.raises(capi.Conv2dError) as e:
             capi.conv2d_fwd(d, A, A, A, 0, ws)
         assert e.value.status == capi.ERR_NULL_PTR
+    finally:
+        capi.conv2d_desc_destroy(d)
+
+
+def test_padded_algo_limits(capi):
+    # Stride-1 only; NCHW input only.
+    with pytest.raises(capi.Conv2dError) as e:
+        capi.conv2d_desc_create(2, 64, 16, 16, 64, 3, 3, 2, 1, "f16", "padded_tc")
+    assert e.value.status == capi.ERR_UNSUPPORTED
+    d = capi.conv2d_desc_create(2, 64, 16, 16, 64, 3, 3, 1, 1, "f16", "padded_tc")
+    try:
+        with pytest.raises(capi.Conv2dError) as e:
+            capi.conv2d_desc_set_input_layout(d, "nhwc")
+        assert e.value.status == capi.ERR_UNSUPPORTED
+        assert capi.conv2d_launches_per_call(d) == 3
     finally:
         capi.conv2d_desc_destroy(d)
 

@@ -22,8 +22,8 @@ from tests.helpers import TOL, oracle_full, parity, run_gpu
 
 pytestmark = pytest.mark.gpu
 
-ALGOS = {"f32": ["im2win_fp32_cc", "implicit_fp32_cc"], "f16": ["im2win_tc", "implicit_tc"],
-         "bf16": ["im2win_tc", "implicit_tc"]}
+ALGOS = {"f32": ["im2win_fp32_cc", "implicit_fp32_cc"], "f16": ["im2win_tc", "implicit_tc", "padded_tc"],
+         "bf16": ["im2win_tc", "implicit_tc", "padded_tc"]}
 REDUCED_N = {"tiny": 1, "resnet_stage1": 2, "stem": 1, "vgg": 1, "sweep_k1": 1, "sweep_k3": 1,
              "sweep_k5": 1, "sweep_k7": 1, "sweep_k9": 1, "sweep_k11": 1, "sweep_k3_s2": 2}
 
@@ -50,6 +50,8 @@ def _cases():
     for name, wl in synth.WORKLOADS.items():
         for dt in wl.dtypes:
             for algo in ALGOS[dt]:
+                if algo == "padded_tc" and wl.stride != 1:
+                    continue                      # stride-1 algorithm
                 out.append((name, dt, algo))
     return out
 
@@ -83,7 +85,8 @@ def _full_cases():
         for dt in wl.dtypes:
             out.append((name, dt, "auto"))
     out += [("vgg", "f16", "im2win_tc"), ("resnet_stage1", "f16", "im2win_tc"), ("stem", "f16", "implicit_tc"),
-            ("stem", "f32", "implicit_fp32_cc")]
+            ("stem", "f32", "implicit_fp32_cc"), ("resnet_stage1", "f16", "implicit_tc"), ("vgg", "bf16", "padded_tc"),
+            ("sweep_k7", "f16", "padded_tc")]
     return out
 
 
