@@ -45,32 +45,40 @@ struct TcParams {
                         // tensor), 2 padded (tiled boxes over the zero-padded NHWC copy)
     int N, Wq, HpWq;    // padded mode: batch, row pitch and image pitch of the padded grid
     int vec_store;      // modes 0/1: Ho*Wo % 8 == 0 (16-byte stores); mode 2: Wo % 4 == 0 (8-byte stores)
+    int kpb;            // K chunks (of 64) per pipeline stage, fetched by one A and one B copy
+    int stages;         // depth of the shared-memory ring (<= kMaxStages)
+    int stage_bytes;    // kpb * (A chunk + B chunk)
+    int a3d;            // padded mode: A map is 3-D (64 channels, pixel rows, chunk) instead of 2-D
     void* y;
 };
 
+constexpr int kMaxStages = 8;
+constexpr int kSmemLimit = 232448;                               // 227 KB per block
+
 template <int BN>
 struct TcConfig {
-    static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
-    static constexpr int kABytes = kTcBlockM * kTcBlockK * 2;   // 16 KB
-    static constexpr int kBBytes = BN * kTcBlockK * 2;
-    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kABytes = kTcBlockM * kTcBlockK * 2;   // one 128 x 64 A chunk: 16 KB
+    static constexpr int kBBytes = BN * kTcBlockK * 2;          // one BN x 64 B chunk
+    static constexpr int kChunkBytes = kABytes + kBBytes;
     static constexpr int kTmemCols = 2 * BN;                    // two accumulators
-    static constexpr int kEpiOffset = kStages * kStageBytes;    // epilogue staging: 32 channels x 128 pixels
-    static constexpr int kEpiBytes = 32 * kTcBlockM * 2;
-    static constexpr int kBarOffset = kEpiOffset + kEpiBytes;
-    static constexpr int kSmemBytes = kBarOffset + 256 + 1024;  // barriers + alignment slack
+    static constexpr int kEpiBytes = 32 * kTcBlockM * 2;        // epilogue staging: 32 channels x 128 pixels
+    static constexpr int kTailBytes = kEpiBytes + 256 + 1024;   // staging + barriers + alignment slack
 };
+// Shared memory layout for a ring of `stages` stages of `stage_bytes`:
+//   [stage 0 .. stage S-1][epilogue staging][barriers]; a stage is
+//   [kpb A chunks][kpb B chunks], each chunk 1024-byte aligned (128-byte swizzle).
 
 template <int BN, bool BF16>
 __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__ CUtensorMap amap,
                                                          const __grid_constant__ CUtensorMap bmap,
                                                          const TcParams prm) {
     using Cfg = TcConfig<BN>;
-    constexpr int S = Cfg::kStages;
+    const int S = prm.stages;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzled operand tiles need 1024-byte alignment.
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOffset);
+    const int epi_off = S * prm.stage_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + epi_off + Cfg::kEpiBytes);
     // bars[0..S) full, [S..2S) empty, [2S..2S+2) accumulator full, [2S+2..2S+4) accumulator empty, [2S+4] drain
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -120,17 +128,22 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
                     ho = r / prm.Wo;
                     wo = r - ho * prm.Wo;
                 }
-                for (int kc = 0; kc < prm.n_kchunks; ++kc) {
+                for (int kc = 0; kc < prm.n_kchunks; kc += prm.kpb) {
                     const int t = kc / prm.n_cchunks;
-                    const int c0 = (kc - t * prm.n_cchunks) * kTcBlockK;
+                    const int cb = kc - t * prm.n_cchunks;
+                    const int c0 = cb * kTcBlockK;
                     if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
-                    const uint32_t a_dst = smem_addr(smem + stage * Cfg::kStageBytes);
-                    const uint32_t b_dst = a_dst + Cfg::kABytes;
+                    mbar_arrive_expect_tx(full_bar(stage), prm.stage_bytes);
+                    const uint32_t a_dst = smem_addr(smem + stage * prm.stage_bytes);
+                    const uint32_t b_dst = a_dst + prm.kpb * Cfg::kABytes;
                     if (prm.amode == 2) {
-                        // Virtual pixel q reads padded pixel q + kh*Wq + kw: one tiled box per tap.
+                        // Virtual pixel q reads padded pixel q + kh*Wq + kw.  The 3-D view
+                        // fetches kpb consecutive chunks in one copy: the next 64-channel
+                        // block of the same tap, or (64-channel pixels) the next tap kw+1,
+                        // both 128 bytes further on.
                         const int kh = t / prm.Kw, kw = t - kh * prm.Kw;
-                        tma_load_2d(a_dst, &amap, full_bar(stage), c0, m0 + kh * prm.Wq + kw);
+                        if (prm.a3d) tma_load_3d(a_dst, &amap, full_bar(stage), 0, m0 + kh * prm.Wq + kw, cb);
+                        else         tma_load_2d(a_dst, &amap, full_bar(stage), c0, m0 + kh * prm.Wq + kw);
                     } else if (prm.amode == 1) {
                         tma_load_im2col_4d(a_dst, &amap, full_bar(stage), c0, wo * prm.s, ho, img, (uint16_t)t, 0);
                     } else {
@@ -138,7 +151,8 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
                         tma_load_im2col_4d(a_dst, &amap, full_bar(stage), c0, wo * prm.s - prm.p,
                                            ho * prm.s - prm.p, img, (uint16_t)kw, (uint16_t)kh);
                     }
-                    tma_load_2d(b_dst, &bmap, full_bar(stage), t * prm.CP + c0, n0);
+                    // kpb consecutive 64-element K blocks of the repacked filter, one copy.
+                    tma_load_3d(b_dst, &bmap, full_bar(stage), 0, n0, kc);
                     ++issued;
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
@@ -165,15 +179,18 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
                 if (!mbar_wait(acce_bar(acc), acc_phase ^ 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kc = 0; kc < prm.n_kchunks; ++kc) {
+                for (int kc = 0; kc < prm.n_kchunks; kc += prm.kpb) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a_base = smem_addr(smem + stage * Cfg::kStageBytes);
-                    const uint32_t b_base = a_base + Cfg::kABytes;
+                    const uint32_t a_base = smem_addr(smem + stage * prm.stage_bytes);
+                    const uint32_t b_base = a_base + prm.kpb * Cfg::kABytes;
+                    for (int i = 0; i < prm.kpb; ++i) {
+                        const uint32_t a_sub = a_base + i * Cfg::kABytes, b_sub = b_base + i * Cfg::kBBytes;
 #pragma unroll
-                    for (int k = 0; k < kTcBlockK / 16; ++k) {
-                        umma_f16(d_tmem, sw128_kmajor_desc(a_base + 32 * k), sw128_kmajor_desc(b_base + 32 * k),
-                                 idesc, (kc > 0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < kTcBlockK / 16; ++k) {
+                            umma_f16(d_tmem, sw128_kmajor_desc(a_sub + 32 * k), sw128_kmajor_desc(b_sub + 32 * k),
+                                     idesc, (kc > 0 || i > 0 || k > 0) ? 1u : 0u);
+                        }
                     }
                     issued_any = true;
                     umma_commit(empty_bar(stage));
@@ -198,7 +215,7 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
         // barrier also ANDs the wait results so all four leave together.
         const int quarter = warp & 3;
         const int et = threadIdx.x - 64;                 // 0..127
-        uint16_t* stage_out = reinterpret_cast<uint16_t*>(smem + Cfg::kEpiOffset);
+        uint16_t* stage_out = reinterpret_cast<uint16_t*>(smem + epi_off);
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < prm.n_tiles; tile += gridDim.x) {
@@ -366,7 +383,7 @@ template <int BN, bool BF16>
 static cudaError_t launch_tc_inst(const CUtensorMap& a, const CUtensorMap& b, const TcParams& prm, int grid,
                                   cudaStream_t st) {
     auto kern = conv_tc_kernel<BN, BF16>;
-    const int smem = TcConfig<BN>::kSmemBytes;
+    const int smem = prm.stages * prm.stage_bytes + TcConfig<BN>::kTailBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return launch_after(kern, dim3(grid), dim3(192), smem, st, a, b, prm);
@@ -399,8 +416,37 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     }
     cuuint64_t adims[4] = {C, Wd, Hd, (cuuint64_t)d.N};
     cuuint64_t astr[3] = {C * 2, C * 2 * Wd, C * 2 * Wd * Hd};
+    // Chunks per stage and ring depth.  Several chunks per copy only in padded
+    // mode with whole 64-channel blocks: a copy costs about the same time
+    // whatever its size, so fewer, larger copies feed the MMAs faster.
+    const int n_cchunks = d.CP / kTcBlockK;
+    const int chunk_bytes = kTcBlockM * kTcBlockK * 2 + d.BN * kTcBlockK * 2;
+    const int tail = 32 * kTcBlockM * 2 + 256 + 1024;
+    int kpb = 1;
+    const bool a3d = amode == 2 && d.Ci8 % kTcBlockK == 0;
+    if (a3d) {
+        const int group = n_cchunks >= 2 ? n_cchunks : d.Kw;   // chunks reachable at a 128-byte step
+        for (int c = 4; c >= 2; --c)
+            if (group % c == 0 && (kSmemLimit - tail) / (c * chunk_bytes) >= 3) { kpb = c; break; }
+    }
+    int stages = (kSmemLimit - tail) / (kpb * chunk_bytes);
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < 2) return CONV2D_ERR_UNSUPPORTED;
+
     CUresult r;
-    if (amode == 2) {
+    if (amode == 2 && a3d) {
+        // Padded copy as (64 channels, pixel rows, chunk): chunk z is 128 bytes
+        // further on — the next channel block, or the next pixel (next tap)
+        // when a pixel holds exactly 64 channels.
+        const cuuint64_t zext = n_cchunks >= 2 ? (cuuint64_t)n_cchunks : (cuuint64_t)d.Kw;
+        cuuint64_t pdims[3] = {(cuuint64_t)kTcBlockK, (cuuint64_t)d.N * d.Hp * d.Wq, zext};
+        cuuint64_t pstr[2] = {(cuuint64_t)d.Ci8 * 2, (cuuint64_t)kTcBlockK * 2};
+        cuuint32_t pbox[3] = {(cuuint32_t)kTcBlockK, (cuuint32_t)kTcBlockM, (cuuint32_t)kpb};
+        cuuint32_t pestr[3] = {1, 1, 1};
+        r = enc_tiled(&amap, dt, 3, const_cast<void*>(src), pdims, pstr, pbox, pestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else if (amode == 2) {
         // Padded channels-last copy viewed as [N*Hp*Wq pixel rows][Ci8 channels].
         cuuint64_t pdims[2] = {(cuuint64_t)d.Ci8, (cuuint64_t)d.N * d.Hp * d.Wq};
         cuuint64_t pstr[1] = {(cuuint64_t)d.Ci8 * 2};
@@ -416,12 +462,12 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     }
     if (r != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
 
-    // B: repacked filter [Co][taps*CP], K-major, box 64 x BN.
-    cuuint64_t bdims[2] = {(cuuint64_t)d.taps * d.CP, (cuuint64_t)d.Co};
-    cuuint64_t bstr[1] = {(cuuint64_t)d.taps * d.CP * 2};
-    cuuint32_t bbox[2] = {(cuuint32_t)kTcBlockK, (cuuint32_t)d.BN};
-    cuuint32_t bestr[2] = {1, 1};
-    r = enc_tiled(&bmap, dt, 2, const_cast<void*>(wq), bdims, bstr, bbox, bestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    // B: repacked filter [Co][taps*CP] as (64 K, Co, K block): box 64 x BN x kpb.
+    cuuint64_t bdims[3] = {(cuuint64_t)kTcBlockK, (cuuint64_t)d.Co, (cuuint64_t)d.taps * n_cchunks};
+    cuuint64_t bstr[2] = {(cuuint64_t)d.taps * d.CP * 2, (cuuint64_t)kTcBlockK * 2};
+    cuuint32_t bbox[3] = {(cuuint32_t)kTcBlockK, (cuuint32_t)d.BN, (cuuint32_t)kpb};
+    cuuint32_t bestr[3] = {1, 1, 1};
+    r = enc_tiled(&bmap, dt, 3, const_cast<void*>(wq), bdims, bstr, bbox, bestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
@@ -440,6 +486,10 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     prm.n_kchunks = d.taps * prm.n_cchunks;
     prm.CP = d.CP; prm.Kw = d.Kw; prm.s = d.s; prm.p = d.p;
     prm.amode = amode;
+    prm.kpb = kpb;
+    prm.stages = stages;
+    prm.stage_bytes = kpb * chunk_bytes;
+    prm.a3d = a3d ? 1 : 0;
     prm.y = y;
     if (amode == 2)
         prm.vec_store = ((d.Wo % 4) == 0 && (d.Wq % 4) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) ? 1 : 0;
