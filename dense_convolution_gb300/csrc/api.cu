@@ -117,7 +117,7 @@ conv2d_status finalize(conv2d_desc& d) {
             const long long rows = (long long)d.N * d.Hp * d.Wq;
             if (rows + (long long)d.Kh * d.Wq + d.Kw + kTcBlockM > kMaxElems) return CONV2D_ERR_UNSUPPORTED;
             if (rows * d.Ci8 > kMaxElems * 4) return CONV2D_ERR_UNSUPPORTED;
-            d.ws_input = (size_t)((rows + d.Kw) * d.Ci8) * 2;   // + Kw zero pixels of read slack
+            d.ws_input = (size_t)(rows * d.Ci8) * 2;
         } else if (im2win) {
             const long long win = (long long)d.N * d.Ho * d.Wp * d.Kh * d.Ci8;
             if (win > kMaxElems * 4) return CONV2D_ERR_UNSUPPORTED;

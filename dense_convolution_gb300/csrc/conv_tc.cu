@@ -45,10 +45,13 @@ struct TcParams {
                         // tensor), 2 padded (tiled boxes over the zero-padded NHWC copy)
     int N, Wq, HpWq;    // padded mode: batch, row pitch and image pitch of the padded grid
     int vec_store;      // modes 0/1: Ho*Wo % 8 == 0 (16-byte stores); mode 2: Wo % 4 == 0 (8-byte stores)
-    int kpb;            // K chunks (of 64) per pipeline stage, fetched by one A and one B copy
+    int kpb;            // MMA chunks per pipeline stage (one A copy + one B copy per stage)
     int stages;         // depth of the shared-memory ring (<= kMaxStages)
-    int stage_bytes;    // kpb * (A chunk + B chunk)
-    int a3d;            // padded mode: A map is 3-D (64 channels, pixel rows, chunk) instead of 2-D
+    int stage_bytes;    // A region + kpb B chunks
+    int a_bytes;        // A region of a stage: one 128-row chunk, or a halo of 128 + kpb - 1 rows
+    int halo;           // padded mode: a stage holds kpb neighbouring taps kw0..kw0+kpb-1 of one
+                        // filter row, all read from one halo A tile at row offsets 0..kpb-1
+    int n_sp;           // pipeline stages per output tile
     void* y;
 };
 
@@ -128,22 +131,28 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
                     ho = r / prm.Wo;
                     wo = r - ho * prm.Wo;
                 }
-                for (int kc = 0; kc < prm.n_kchunks; kc += prm.kpb) {
-                    const int t = kc / prm.n_cchunks;
-                    const int cb = kc - t * prm.n_cchunks;
+                for (int sp = 0; sp < prm.n_sp; ++sp) {
+                    // Stage sp covers taps t..t+kpb-1 (halo) or chunk sp, channel block cb.
+                    int t, cb;
+                    if (prm.halo) {
+                        cb = sp % prm.n_cchunks;
+                        const int rest = sp / prm.n_cchunks, ngw = prm.Kw / prm.kpb;
+                        t = (rest / ngw) * prm.Kw + (rest % ngw) * prm.kpb;
+                    } else {
+                        t = sp / prm.n_cchunks;
+                        cb = sp - t * prm.n_cchunks;
+                    }
                     const int c0 = cb * kTcBlockK;
                     if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag)) { ok = false; break; }
                     mbar_arrive_expect_tx(full_bar(stage), prm.stage_bytes);
                     const uint32_t a_dst = smem_addr(smem + stage * prm.stage_bytes);
-                    const uint32_t b_dst = a_dst + prm.kpb * Cfg::kABytes;
+                    const uint32_t b_dst = a_dst + prm.a_bytes;
                     if (prm.amode == 2) {
-                        // Virtual pixel q reads padded pixel q + kh*Wq + kw.  The 3-D view
-                        // fetches kpb consecutive chunks in one copy: the next 64-channel
-                        // block of the same tap, or (64-channel pixels) the next tap kw+1,
-                        // both 128 bytes further on.
+                        // Virtual pixel q reads padded pixel q + kh*Wq + kw.  In halo mode
+                        // the box has 128 + kpb - 1 rows: taps kw..kw+kpb-1 are the same
+                        // rows shifted by one pixel each, so they share one copy.
                         const int kh = t / prm.Kw, kw = t - kh * prm.Kw;
-                        if (prm.a3d) tma_load_3d(a_dst, &amap, full_bar(stage), 0, m0 + kh * prm.Wq + kw, cb);
-                        else         tma_load_2d(a_dst, &amap, full_bar(stage), c0, m0 + kh * prm.Wq + kw);
+                        tma_load_2d(a_dst, &amap, full_bar(stage), c0, m0 + kh * prm.Wq + kw);
                     } else if (prm.amode == 1) {
                         tma_load_im2col_4d(a_dst, &amap, full_bar(stage), c0, wo * prm.s, ho, img, (uint16_t)t, 0);
                     } else {
@@ -151,8 +160,8 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
                         tma_load_im2col_4d(a_dst, &amap, full_bar(stage), c0, wo * prm.s - prm.p,
                                            ho * prm.s - prm.p, img, (uint16_t)kw, (uint16_t)kh);
                     }
-                    // kpb consecutive 64-element K blocks of the repacked filter, one copy.
-                    tma_load_3d(b_dst, &bmap, full_bar(stage), 0, n0, kc);
+                    // Filter chunks of taps t..t+kpb-1, channel block cb: one copy.
+                    tma_load_4d(b_dst, &bmap, full_bar(stage), 0, n0, cb, t);
                     ++issued;
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
@@ -179,17 +188,18 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
                 if (!mbar_wait(acce_bar(acc), acc_phase ^ 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kc = 0; kc < prm.n_kchunks; kc += prm.kpb) {
+                for (int sp = 0; sp < prm.n_sp; ++sp) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a_base = smem_addr(smem + stage * prm.stage_bytes);
-                    const uint32_t b_base = a_base + prm.kpb * Cfg::kABytes;
+                    const uint32_t b_base = a_base + prm.a_bytes;
                     for (int i = 0; i < prm.kpb; ++i) {
-                        const uint32_t a_sub = a_base + i * Cfg::kABytes, b_sub = b_base + i * Cfg::kBBytes;
+                        // Halo: tap kw0+i reads the A tile from row i (128 bytes per row).
+                        const uint32_t a_sub = a_base + i * 128u, b_sub = b_base + i * Cfg::kBBytes;
 #pragma unroll
                         for (int k = 0; k < kTcBlockK / 16; ++k) {
                             umma_f16(d_tmem, sw128_kmajor_desc(a_sub + 32 * k), sw128_kmajor_desc(b_sub + 32 * k),
-                                     idesc, (kc > 0 || i > 0 || k > 0) ? 1u : 0u);
+                                     idesc, (sp > 0 || i > 0 || k > 0) ? 1u : 0u);
                         }
                     }
                     issued_any = true;
@@ -416,41 +426,34 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     }
     cuuint64_t adims[4] = {C, Wd, Hd, (cuuint64_t)d.N};
     cuuint64_t astr[3] = {C * 2, C * 2 * Wd, C * 2 * Wd * Hd};
-    // Chunks per stage and ring depth.  Several chunks per copy only in padded
-    // mode with whole 64-channel blocks: a copy costs about the same time
-    // whatever its size, so fewer, larger copies feed the MMAs faster.
+    // Ring layout.  Padded mode groups kpb neighbouring taps of one filter row
+    // per stage around one halo A tile (128 + kpb - 1 pixel rows): the copy
+    // engine delivers about the same bytes per SM per second whatever the
+    // copy, so reusing overlapping rows from shared memory feeds more MMAs.
     const int n_cchunks = d.CP / kTcBlockK;
-    const int chunk_bytes = kTcBlockM * kTcBlockK * 2 + d.BN * kTcBlockK * 2;
+    const int b_chunk = d.BN * kTcBlockK * 2;
     const int tail = 32 * kTcBlockM * 2 + 256 + 1024;
-    int kpb = 1;
-    const bool a3d = amode == 2 && d.Ci8 % kTcBlockK == 0;
-    if (a3d) {
-        const int group = n_cchunks >= 2 ? n_cchunks : d.Kw;   // chunks reachable at a 128-byte step
-        for (int c = 4; c >= 2; --c)
-            if (group % c == 0 && (kSmemLimit - tail) / (c * chunk_bytes) >= 3) { kpb = c; break; }
+    const bool halo = amode == 2;
+    int kpb = 1, a_rows = kTcBlockM;
+    if (halo) {
+        for (int c = d.Kw; c >= 2; --c) {
+            if (d.Kw % c) continue;
+            const int rows = (kTcBlockM + c - 1 + 7) / 8 * 8;
+            if ((kSmemLimit - tail) / (rows * 128 + c * b_chunk) >= 3) { kpb = c; a_rows = rows; break; }
+        }
     }
-    int stages = (kSmemLimit - tail) / (kpb * chunk_bytes);
+    const int stage_bytes = a_rows * 128 + kpb * b_chunk;
+    int stages = (kSmemLimit - tail) / stage_bytes;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return CONV2D_ERR_UNSUPPORTED;
 
     CUresult r;
-    if (amode == 2 && a3d) {
-        // Padded copy as (64 channels, pixel rows, chunk): chunk z is 128 bytes
-        // further on — the next channel block, or the next pixel (next tap)
-        // when a pixel holds exactly 64 channels.
-        const cuuint64_t zext = n_cchunks >= 2 ? (cuuint64_t)n_cchunks : (cuuint64_t)d.Kw;
-        cuuint64_t pdims[3] = {(cuuint64_t)kTcBlockK, (cuuint64_t)d.N * d.Hp * d.Wq, zext};
-        cuuint64_t pstr[2] = {(cuuint64_t)d.Ci8 * 2, (cuuint64_t)kTcBlockK * 2};
-        cuuint32_t pbox[3] = {(cuuint32_t)kTcBlockK, (cuuint32_t)kTcBlockM, (cuuint32_t)kpb};
-        cuuint32_t pestr[3] = {1, 1, 1};
-        r = enc_tiled(&amap, dt, 3, const_cast<void*>(src), pdims, pstr, pbox, pestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    } else if (amode == 2) {
-        // Padded channels-last copy viewed as [N*Hp*Wq pixel rows][Ci8 channels].
+    if (amode == 2) {
+        // Padded channels-last copy viewed as [N*Hp*Wq pixel rows][Ci8 channels];
+        // box 64 channels x a_rows pixels (rows past the end read as zero).
         cuuint64_t pdims[2] = {(cuuint64_t)d.Ci8, (cuuint64_t)d.N * d.Hp * d.Wq};
         cuuint64_t pstr[1] = {(cuuint64_t)d.Ci8 * 2};
-        cuuint32_t pbox[2] = {(cuuint32_t)kTcBlockK, (cuuint32_t)kTcBlockM};
+        cuuint32_t pbox[2] = {(cuuint32_t)kTcBlockK, (cuuint32_t)a_rows};
         cuuint32_t pestr[2] = {1, 1};
         r = enc_tiled(&amap, dt, 2, const_cast<void*>(src), pdims, pstr, pbox, pestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -462,12 +465,13 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     }
     if (r != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
 
-    // B: repacked filter [Co][taps*CP] as (64 K, Co, K block): box 64 x BN x kpb.
-    cuuint64_t bdims[3] = {(cuuint64_t)kTcBlockK, (cuuint64_t)d.Co, (cuuint64_t)d.taps * n_cchunks};
-    cuuint64_t bstr[2] = {(cuuint64_t)d.taps * d.CP * 2, (cuuint64_t)kTcBlockK * 2};
-    cuuint32_t bbox[3] = {(cuuint32_t)kTcBlockK, (cuuint32_t)d.BN, (cuuint32_t)kpb};
-    cuuint32_t bestr[3] = {1, 1, 1};
-    r = enc_tiled(&bmap, dt, 3, const_cast<void*>(wq), bdims, bstr, bbox, bestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    // B: repacked filter [Co][taps][CP] as (64 K, Co, channel block, tap): box
+    // 64 x BN x 1 x kpb = the chunks of kpb consecutive taps for one block.
+    cuuint64_t bdims[4] = {(cuuint64_t)kTcBlockK, (cuuint64_t)d.Co, (cuuint64_t)n_cchunks, (cuuint64_t)d.taps};
+    cuuint64_t bstr[3] = {(cuuint64_t)d.taps * d.CP * 2, (cuuint64_t)kTcBlockK * 2, (cuuint64_t)d.CP * 2};
+    cuuint32_t bbox[4] = {(cuuint32_t)kTcBlockK, (cuuint32_t)d.BN, 1, (cuuint32_t)kpb};
+    cuuint32_t bestr[4] = {1, 1, 1, 1};
+    r = enc_tiled(&bmap, dt, 4, const_cast<void*>(wq), bdims, bstr, bbox, bestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
@@ -488,8 +492,10 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     prm.amode = amode;
     prm.kpb = kpb;
     prm.stages = stages;
-    prm.stage_bytes = kpb * chunk_bytes;
-    prm.a3d = a3d ? 1 : 0;
+    prm.stage_bytes = stage_bytes;
+    prm.a_bytes = a_rows * 128;
+    prm.halo = halo ? 1 : 0;
+    prm.n_sp = halo ? d.Kh * (d.Kw / kpb) * n_cchunks : d.taps * n_cchunks;
     prm.y = y;
     if (amode == 2)
         prm.vec_store = ((d.Wo % 4) == 0 && (d.Wq % 4) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) ? 1 : 0;

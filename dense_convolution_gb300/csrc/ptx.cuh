@@ -131,6 +131,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
 // im2col-mode load of a 4-D channels-innermost tensor (C, W, H, N): a column
 // of pixels walked W-then-H-then-N inside the map's bounding box, starting at
 // (w, h, n), each pixel read at (w + off_w, h + off_h), channels [c, c+box).
@@ -183,12 +192,16 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 // layout written by a TMA box whose rows are 128 bytes: 8-row groups are
 // 1024 bytes apart (stride byte offset); the leading byte offset is unused
 // for this layout; bit 46 is the descriptor version; swizzle code 2 = 128B.
+// The swizzle pattern repeats every 8 rows (1024 bytes); a start address that
+// is not on such a boundary (an operand that begins r rows into a tile)
+// carries the phase r = (addr >> 7) & 7 in the base-offset field (bits 49-51).
 __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
     d |= static_cast<uint64_t>(1u) << 16;
     d |= static_cast<uint64_t>(1024u >> 4) << 32;
     d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>((saddr >> 7) & 7u) << 49;
     d |= static_cast<uint64_t>(2u) << 61;
     return d;
 }

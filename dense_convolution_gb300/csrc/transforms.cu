@@ -131,14 +131,11 @@ cudaError_t launch_nchw_to_nhwc16(const void* x, void* out, int N, int C, int H,
 // channels: reads run along image rows, writes are 16-byte channel vectors.
 __global__ void __launch_bounds__(256) nchw_to_padded_nhwc16_kernel(const uint16_t* __restrict__ x,
                                                                     uint4* __restrict__ out, int C, int C8, int H,
-                                                                    int W, int Hp, int Wq, int p, int tail_px) {
+                                                                    int W, int Hp, int Wq, int p) {
     __shared__ uint32_t tile[kNhwcTile * kNhwcPitch / 2];
     uint16_t* t16 = reinterpret_cast<uint16_t*>(tile);
     pdl_launch_dependents();
     const int P = Hp * Wq;
-    // The last image also writes tail_px zero pixels after the grid (read
-    // slack for copies that step past the final row).
-    const int Pw = blockIdx.z == gridDim.z - 1 ? P + tail_px : P;
     const int p0 = blockIdx.x * kNhwcTile, c0 = blockIdx.y * kNhwcTile;
     const long long n = blockIdx.z;
     const int pl = threadIdx.x & 63;
@@ -158,7 +155,7 @@ __global__ void __launch_bounds__(256) nchw_to_padded_nhwc16_kernel(const uint16
     for (int i = 0; i < 2; ++i) {
         const int pl2 = threadIdx.x / 8 + 32 * i, cg = threadIdx.x % 8;
         const int pp = p0 + pl2, cc = c0 + cg * 8;
-        if (pp < Pw && cc < C8) {
+        if (pp < P && cc < C8) {
             uint32_t w[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -171,11 +168,11 @@ __global__ void __launch_bounds__(256) nchw_to_padded_nhwc16_kernel(const uint16
 }
 
 cudaError_t launch_nchw_to_padded_nhwc16(const void* x, void* out, const conv2d_desc& d, cudaStream_t st) {
-    const int P = d.Hp * d.Wq + d.Kw;   // grid plus the read slack written by the last image
+    const int P = d.Hp * d.Wq;
     dim3 grid((P + kNhwcTile - 1) / kNhwcTile, (d.Ci8 + kNhwcTile - 1) / kNhwcTile, d.N);
     if (grid.z > 65535 || grid.y > 65535) return cudaErrorInvalidConfiguration;
     return launch_after(nchw_to_padded_nhwc16_kernel, grid, dim3(256), 0, st, static_cast<const uint16_t*>(x),
-                        static_cast<uint4*>(out), d.Ci, d.Ci8, d.H, d.W, d.Hp, d.Wq, d.p, d.Kw);
+                        static_cast<uint4*>(out), d.Ci, d.Ci8, d.H, d.W, d.Hp, d.Wq, d.p);
 }
 
 // ---------------------------------------------------------------- 16-bit channels-innermost window
