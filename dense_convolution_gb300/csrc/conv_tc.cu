@@ -160,8 +160,11 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
                         tma_load_im2col_4d(a_dst, &amap, full_bar(stage), c0, wo * prm.s - prm.p,
                                            ho * prm.s - prm.p, img, (uint16_t)kw, (uint16_t)kh);
                     }
-                    // Filter chunks of taps t..t+kpb-1, channel block cb: one copy.
-                    tma_load_4d(b_dst, &bmap, full_bar(stage), 0, n0, cb, t);
+                    // Filter chunks of taps t..t+kpb-1, channel block cb: one copy (a 3-D
+                    // box in halo mode; higher-rank maps cost the copy engine more, so
+                    // the other modes keep a 2-D map).
+                    if (prm.halo) tma_load_3d(b_dst, &bmap, full_bar(stage), c0, n0, t);
+                    else          tma_load_2d(b_dst, &bmap, full_bar(stage), t * prm.CP + c0, n0);
                     ++issued;
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
@@ -465,15 +468,26 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     }
     if (r != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
 
-    // B: repacked filter [Co][taps][CP] as (64 K, Co, channel block, tap): box
-    // 64 x BN x 1 x kpb = the chunks of kpb consecutive taps for one block.
-    cuuint64_t bdims[4] = {(cuuint64_t)kTcBlockK, (cuuint64_t)d.Co, (cuuint64_t)n_cchunks, (cuuint64_t)d.taps};
-    cuuint64_t bstr[3] = {(cuuint64_t)d.taps * d.CP * 2, (cuuint64_t)kTcBlockK * 2, (cuuint64_t)d.CP * 2};
-    cuuint32_t bbox[4] = {(cuuint32_t)kTcBlockK, (cuuint32_t)d.BN, 1, (cuuint32_t)kpb};
-    cuuint32_t bestr[4] = {1, 1, 1, 1};
-    r = enc_tiled(&bmap, dt, 4, const_cast<void*>(wq), bdims, bstr, bbox, bestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    // B: repacked filter [Co][taps][CP].  Halo mode: (CP, Co, tap) with box
+    // 64 x BN x kpb = the chunks of kpb consecutive taps for one channel block;
+    // otherwise 2-D (taps*CP, Co) with box 64 x BN.
+    if (halo) {
+        cuuint64_t bdims[3] = {(cuuint64_t)d.CP, (cuuint64_t)d.Co, (cuuint64_t)d.taps};
+        cuuint64_t bstr[2] = {(cuuint64_t)d.taps * d.CP * 2, (cuuint64_t)d.CP * 2};
+        cuuint32_t bbox[3] = {(cuuint32_t)kTcBlockK, (cuuint32_t)d.BN, (cuuint32_t)kpb};
+        cuuint32_t bestr[3] = {1, 1, 1};
+        r = enc_tiled(&bmap, dt, 3, const_cast<void*>(wq), bdims, bstr, bbox, bestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t bdims[2] = {(cuuint64_t)d.taps * d.CP, (cuuint64_t)d.Co};
+        cuuint64_t bstr[1] = {(cuuint64_t)d.taps * d.CP * 2};
+        cuuint32_t bbox[2] = {(cuuint32_t)kTcBlockK, (cuuint32_t)d.BN};
+        cuuint32_t bestr[2] = {1, 1};
+        r = enc_tiled(&bmap, dt, 2, const_cast<void*>(wq), bdims, bstr, bbox, bestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (r != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
 
     TcParams prm{};

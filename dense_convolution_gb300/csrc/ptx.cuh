@@ -192,16 +192,17 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 // layout written by a TMA box whose rows are 128 bytes: 8-row groups are
 // 1024 bytes apart (stride byte offset); the leading byte offset is unused
 // for this layout; bit 46 is the descriptor version; swizzle code 2 = 128B.
-// The swizzle pattern repeats every 8 rows (1024 bytes); a start address that
-// is not on such a boundary (an operand that begins r rows into a tile)
-// carries the phase r = (addr >> 7) & 7 in the base-offset field (bits 49-51).
+// An operand may start r rows into a 1024-byte-aligned tile (the halo tiles
+// of the padded path): the swizzle phase is taken from the absolute shared
+// memory address, the same rule TMA uses when it writes the tile, so the
+// base-offset field (bits 49-51) stays 0.  Measured: setting it to r gives
+// wrong products, leaving it 0 is bit-exact.
 __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
     d |= static_cast<uint64_t>(1u) << 16;
     d |= static_cast<uint64_t>(1024u >> 4) << 32;
     d |= static_cast<uint64_t>(1u) << 46;
-    d |= static_cast<uint64_t>((saddr >> 7) & 7u) << 49;
     d |= static_cast<uint64_t>(2u) << 61;
     return d;
 }
