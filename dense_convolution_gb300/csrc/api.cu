@@ -59,9 +59,12 @@ bool tc_shape_ok(const conv2d_desc& d, bool im2win) {
 conv2d_algo resolve_auto(const conv2d_desc& d) {
     if (d.dtype == CONV2D_F32) return CONV2D_ALGO_IM2WIN_FP32_CC;
     if (d.layout == CONV2D_LAYOUT_NHWC) return CONV2D_ALGO_IMPLICIT_TC;
-    // Stride 1: tiled operand loads over a padded copy beat im2col-mode loads
-    // unless the padded grid adds too many junk rows (measured on GB300).
-    if (d.s == 1 && padded_waste(d) <= 0.15 && (d.Ci + 7) / 8 * 8 >= 64) return CONV2D_ALGO_PADDED_TC;
+    // Stride 1 with several taps per filter row: the padded path shares one
+    // halo operand tile among neighbouring taps, which wins unless the padded
+    // grid adds too many junk rows (measured on GB300: ResNet stage 1 and the
+    // K=3/5 sweep layers gain, 1x1 layers and VGG do not).
+    if (d.s == 1 && d.Kw >= 2 && padded_waste(d) <= 0.15 && (d.Ci + 7) / 8 * 8 >= 64)
+        return CONV2D_ALGO_PADDED_TC;
     const bool imp_ok = tc_shape_ok(d, false), win_ok = tc_shape_ok(d, true);
     if (imp_ok && (!win_ok || tc_k_efficiency(d, false) >= tc_k_efficiency(d, true)))
         return CONV2D_ALGO_IMPLICIT_TC;

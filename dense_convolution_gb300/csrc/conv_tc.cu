@@ -71,7 +71,10 @@ struct TcConfig {
 //   [stage 0 .. stage S-1][epilogue staging][barriers]; a stage is
 //   [kpb A chunks][kpb B chunks], each chunk 1024-byte aligned (128-byte swizzle).
 
-template <int BN, bool BF16>
+// MODE is the A source (0 implicit, 1 im2win, 2 padded with halo tiles);
+// each mode compiles to its own kernel so the producer and MMA loops carry no
+// run-time mode tests.
+template <int BN, bool BF16, int MODE>
 __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__ CUtensorMap amap,
                                                          const __grid_constant__ CUtensorMap bmap,
                                                          const TcParams prm) {
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
                 const int m0 = (tile / prm.n_n_tiles) * kTcBlockM;
                 const int n0 = (tile % prm.n_n_tiles) * BN;
                 int img = 0, ho = 0, wo = 0;
-                if (prm.amode != 2) {
+                if constexpr (MODE != 2) {
                     img = m0 / prm.HoWo;
                     const int r = m0 - img * prm.HoWo;
                     ho = r / prm.Wo;
@@ -134,7 +137,7 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
                 for (int sp = 0; sp < prm.n_sp; ++sp) {
                     // Stage sp covers taps t..t+kpb-1 (halo) or chunk sp, channel block cb.
                     int t, cb;
-                    if (prm.halo) {
+                    if constexpr (MODE == 2) {
                         cb = sp % prm.n_cchunks;
                         const int rest = sp / prm.n_cchunks, ngw = prm.Kw / prm.kpb;
                         t = (rest / ngw) * prm.Kw + (rest % ngw) * prm.kpb;
@@ -147,13 +150,13 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
                     mbar_arrive_expect_tx(full_bar(stage), prm.stage_bytes);
                     const uint32_t a_dst = smem_addr(smem + stage * prm.stage_bytes);
                     const uint32_t b_dst = a_dst + prm.a_bytes;
-                    if (prm.amode == 2) {
+                    if constexpr (MODE == 2) {
                         // Virtual pixel q reads padded pixel q + kh*Wq + kw.  In halo mode
                         // the box has 128 + kpb - 1 rows: taps kw..kw+kpb-1 are the same
                         // rows shifted by one pixel each, so they share one copy.
                         const int kh = t / prm.Kw, kw = t - kh * prm.Kw;
                         tma_load_2d(a_dst, &amap, full_bar(stage), c0, m0 + kh * prm.Wq + kw);
-                    } else if (prm.amode == 1) {
+                    } else if constexpr (MODE == 1) {
                         tma_load_im2col_4d(a_dst, &amap, full_bar(stage), c0, wo * prm.s, ho, img, (uint16_t)t, 0);
                     } else {
                         const int kh = t / prm.Kw, kw = t - kh * prm.Kw;
@@ -163,8 +166,8 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
                     // Filter chunks of taps t..t+kpb-1, channel block cb: one copy (a 3-D
                     // box in halo mode; higher-rank maps cost the copy engine more, so
                     // the other modes keep a 2-D map).
-                    if (prm.halo) tma_load_3d(b_dst, &bmap, full_bar(stage), c0, n0, t);
-                    else          tma_load_2d(b_dst, &bmap, full_bar(stage), t * prm.CP + c0, n0);
+                    if constexpr (MODE == 2) tma_load_3d(b_dst, &bmap, full_bar(stage), c0, n0, t);
+                    else                     tma_load_2d(b_dst, &bmap, full_bar(stage), t * prm.CP + c0, n0);
                     ++issued;
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
@@ -196,7 +199,8 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
                     tc_fence_after();
                     const uint32_t a_base = smem_addr(smem + stage * prm.stage_bytes);
                     const uint32_t b_base = a_base + prm.a_bytes;
-                    for (int i = 0; i < prm.kpb; ++i) {
+                    const int kpb = MODE == 2 ? prm.kpb : 1;
+                    for (int i = 0; i < kpb; ++i) {
                         // Halo: tap kw0+i reads the A tile from row i (128 bytes per row).
                         const uint32_t a_sub = a_base + i * 128u, b_sub = b_base + i * Cfg::kBBytes;
 #pragma unroll
@@ -238,7 +242,7 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
             const int m0 = (tile / prm.n_n_tiles) * kTcBlockM;
             const int n0 = (tile % prm.n_n_tiles) * BN;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
-            if (prm.amode == 2) {
+            if constexpr (MODE == 2) {
                 // Rows are virtual pixels of the padded grid [N][Hp][Wq]; only
                 // those with y < Ho and x < Wo are outputs.  With Wo % 4 == 0 a
                 // 4-pixel group is all-valid or all-junk: 8-byte stores.
@@ -392,14 +396,34 @@ typedef CUresult (*PFN_encodeIm2col_t)(CUtensorMap*, CUtensorMapDataType, cuuint
                                        const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                        CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-template <int BN, bool BF16>
+template <int BN, bool BF16, int MODE>
 static cudaError_t launch_tc_inst(const CUtensorMap& a, const CUtensorMap& b, const TcParams& prm, int grid,
                                   cudaStream_t st) {
-    auto kern = conv_tc_kernel<BN, BF16>;
+    auto kern = conv_tc_kernel<BN, BF16, MODE>;
     const int smem = prm.stages * prm.stage_bytes + TcConfig<BN>::kTailBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return launch_after(kern, dim3(grid), dim3(192), smem, st, a, b, prm);
+}
+
+template <bool BF16, int MODE>
+static cudaError_t launch_tc_bn(int BN, const CUtensorMap& a, const CUtensorMap& b, const TcParams& prm, int grid,
+                                cudaStream_t st) {
+    switch (BN) {
+        case 64:  return launch_tc_inst<64, BF16, MODE>(a, b, prm, grid, st);
+        case 128: return launch_tc_inst<128, BF16, MODE>(a, b, prm, grid, st);
+        default:  return launch_tc_inst<256, BF16, MODE>(a, b, prm, grid, st);
+    }
+}
+
+template <bool BF16>
+static cudaError_t launch_tc_mode(int BN, int amode, const CUtensorMap& a, const CUtensorMap& b, const TcParams& prm,
+                                  int grid, cudaStream_t st) {
+    switch (amode) {
+        case 0:  return launch_tc_bn<BF16, 0>(BN, a, b, prm, grid, st);
+        case 1:  return launch_tc_bn<BF16, 1>(BN, a, b, prm, grid, st);
+        default: return launch_tc_bn<BF16, 2>(BN, a, b, prm, grid, st);
+    }
 }
 
 conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* wq, void* y, int amode,
@@ -519,12 +543,8 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     if (grid > prm.n_tiles) grid = prm.n_tiles;
 
     const bool bf = d.dtype == CONV2D_BF16;
-    cudaError_t e;
-    switch (d.BN) {
-        case 64:  e = bf ? launch_tc_inst<64, true>(amap, bmap, prm, grid, st) : launch_tc_inst<64, false>(amap, bmap, prm, grid, st); break;
-        case 128: e = bf ? launch_tc_inst<128, true>(amap, bmap, prm, grid, st) : launch_tc_inst<128, false>(amap, bmap, prm, grid, st); break;
-        default:  e = bf ? launch_tc_inst<256, true>(amap, bmap, prm, grid, st) : launch_tc_inst<256, false>(amap, bmap, prm, grid, st); break;
-    }
+    cudaError_t e = bf ? launch_tc_mode<true>(d.BN, amode, amap, bmap, prm, grid, st)
+                       : launch_tc_mode<false>(d.BN, amode, amap, bmap, prm, grid, st);
     return e == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
 }
 

@@ -72,7 +72,7 @@ def test_auto_choices_and_workspace(capi):
     cases = {
         # name: (shape, dtype, expected algo)
         "resnet_f16": ((32, 64, 56, 56, 64, 3, 3, 1, 1), "f16", "padded_tc"),
-        "k1_f16": ((16, 128, 64, 64, 128, 1, 1, 1, 0), "f16", "padded_tc"),
+        "k1_f16": ((16, 128, 64, 64, 128, 1, 1, 1, 0), "f16", "implicit_tc"),
         "k3s2_f16": ((16, 128, 64, 64, 128, 3, 3, 2, 1), "f16", "implicit_tc"),
         "stem_f16": ((32, 3, 224, 224, 64, 7, 7, 2, 3), "f16", "im2win_tc"),
         "vgg_bf16": ((64, 512, 28, 28, 512, 3, 3, 1, 1), "bf16", "implicit_tc"),
