@@ -95,7 +95,10 @@ def test_auto_choices_and_workspace(capi):
             if algo == "implicit_tc":
                 ci8 = (Ci + 7) // 8 * 8
                 assert ws >= N * H * W * ci8 * 2          # channels-last copy of X
-                assert ws < im2win_tensor
+                # The copy never exceeds the im2win tensor (equal for 1x1 layers);
+                # the repacked filter comes on top.
+                packed = Co * Kh * Kw * ((ci8 + 63) // 64 * 64) * 2
+                assert ws <= im2win_tensor + packed + 1024
         finally:
             capi.conv2d_desc_destroy(d)
 
