@@ -79,13 +79,13 @@ conv2d_status finalize(conv2d_desc& d) {
     d.ws_weights = d.ws_input = d.ws_input_off = d.ws_total = 0;
     if (!tc) {
         d.Lp = (d.Wp * d.Kh + 3) & ~3;
-        d.cc_wpt = d.Wo <= 32 ? 1 : (d.Wo <= 64 ? 2 : 4);
-        int warps = (d.Co + 15) / 16;
-        if (warps > 8) warps = 8;
-        while (warps > 1 && (long long)d.Kh * d.Kw * 16 * warps * 4 > 64 * 1024) --warps;
+        // 32 output channels per warp, 1, 2 or 4 warps; fewer warps when one
+        // channel's filter slice for the block would not stay small.
+        int warps = d.Co > 64 ? 4 : (d.Co > 32 ? 2 : 1);
+        while (warps > 1 && (long long)d.Kh * d.Kw * 32 * warps * 4 > 24 * 1024) warps /= 2;
         d.cc_warps = warps;
-        if ((long long)d.Kh * d.Kw * 16 * 4 > 96 * 1024) return CONV2D_ERR_UNSUPPORTED;
-        const long long bco = 16LL * warps, ncb = (d.Co + bco - 1) / bco;
+        if ((long long)d.Kh * d.Kw * 32 * 4 > 96 * 1024) return CONV2D_ERR_UNSUPPORTED;
+        const long long bco = 32LL * warps, ncb = (d.Co + bco - 1) / bco;
         d.ws_weights = (size_t)(ncb * bco * d.Ci * d.Kh * d.Kw * 4);
         if (d.algo == CONV2D_ALGO_IM2WIN_FP32_CC) {
             const long long strips = (long long)d.N * d.Ci * d.Ho * d.Lp;
@@ -94,7 +94,7 @@ conv2d_status finalize(conv2d_desc& d) {
         } else {
             if (d.W % 4 != 0) return CONV2D_ERR_UNSUPPORTED;    // 16-byte row pitch for the row copies
             if (d.Kh > 256) return CONV2D_ERR_UNSUPPORTED;
-            if ((256 - 3 - d.Kw) / d.s + 1 < 1 || d.Kw > 250) return CONV2D_ERR_UNSUPPORTED;
+            if (63 * d.s + d.Kw + 6 > 256) return CONV2D_ERR_UNSUPPORTED;   // staged rows fit one box
         }
     } else {
         const bool im2win = d.algo == CONV2D_ALGO_IM2WIN_TC;

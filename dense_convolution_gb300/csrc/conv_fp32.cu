@@ -1,9 +1,11 @@
 // fp32 convolution on CUDA cores (FFMA only; no TF32 anywhere).
 //
-// Work split: a block computes one output row (n, ho), a run of up to 32*WPT
-// output columns, and 16*warps output channels.  Lane l of every warp owns
-// the WPT consecutive columns wo0 + l*WPT + t, and 16 channels (one warp's
-// slice); accumulators are WPT x 16 registers.
+// Work split: a block computes one output row (n, ho), 64 consecutive output
+// columns and 32*warps output channels.  A lane owns an 8 x 8 register tile:
+// 8 consecutive output columns (lane % 8 picks which 8) x 8 output channels
+// (lane / 8 and the warp pick which 8).  Per (input channel, filter row,
+// filter column) a lane does 64 FMAs for two 16-byte filter loads, which the
+// 8 lanes of a channel group share as a broadcast.
 //
 // K loop: input channels in chunks staged in shared memory, double-buffered,
 // by the asynchronous copy engine (completion on an mbarrier):
@@ -14,11 +16,11 @@
 //   direct mode  one 3-D tensor-map copy of the Kh input rows of the chunk,
 //                zero-filled outside the image (padding), x origin aligned
 //                down to 16 bytes.
-// plus one bulk copy of the chunk's repacked filter ([ci][kh][kw][16*warps]).
+// plus one bulk copy of the chunk's repacked filter ([ci][kh][kw][32*warps]).
 //
 // Reuse across output columns: for each (channel, filter row) a lane loads
-// only its own WPT*s window columns and takes the Kw - s overlapping columns
-// its windows share with the next lanes by warp shuffle.
+// only its own 8*s window columns and takes the Kw - s columns its windows
+// share with the next lanes of its group by warp shuffle.
 #include <cuda.h>
 
 #include "internal.h"
@@ -31,15 +33,17 @@ struct Fp32Params {
     const float* wq;    // packed filter
     float* y;
     int N, Ci, H, W, Co, Kh, Kw, s, p, Ho, Wo, Lp;
-    int BCO, n_cb, WB, n_wb, chunk, n_chunks;
+    int BCO, n_cb, n_wb, chunk, n_chunks;
     int pitch;          // floats per channel of staged input (im2win), or Kh*boxw (direct)
     int boxw;           // direct mode: staged row width (multiple of 4)
     int xs_floats;      // staged-input floats per stage (including read slack)
     int ws_floats;      // filter floats per stage
 };
 
-template <int KW, int S, int WPT, bool IM2WIN>
-__global__ void __launch_bounds__(256) conv_fp32_kernel(const Fp32Params prm,
+constexpr int kCcCols = 64;    // output columns per block (8 lanes x 8)
+
+template <int KW, int S, bool IM2WIN>
+__global__ void __launch_bounds__(128) conv_fp32_kernel(const Fp32Params prm,
                                                         const __grid_constant__ CUtensorMap xmap) {
     extern __shared__ uint8_t smem_raw[];
     // Tensor-map copies need 128-byte aligned destinations.
@@ -56,7 +60,8 @@ __global__ void __launch_bounds__(256) conv_fp32_kernel(const Fp32Params prm,
     const int Kh = prm.Kh;
     const int kw_n = KW > 0 ? KW : prm.Kw;
     const int sd = S > 0 ? S : prm.s;
-    const int wo0 = wb * prm.WB;
+    const int wo0 = wb * kCcCols;
+    const int wb_valid = min(kCcCols, prm.Wo - wo0);
     const int KK = Kh * kw_n;
     const int stage_floats = prm.xs_floats + prm.ws_floats;
 
@@ -64,7 +69,7 @@ __global__ void __launch_bounds__(256) conv_fp32_kernel(const Fp32Params prm,
     const int e0 = IM2WIN ? ((wo0 * sd * Kh) & ~3) : 0;
     int e1 = 0;
     if (IM2WIN) {
-        e1 = ((wo0 + prm.WB - 1) * sd + kw_n) * Kh;
+        e1 = ((wo0 + wb_valid - 1) * sd + kw_n) * Kh;
         e1 = (e1 + 3) & ~3;
         if (e1 > prm.Lp) e1 = prm.Lp;
     }
@@ -104,16 +109,17 @@ __global__ void __launch_bounds__(256) conv_fp32_kernel(const Fp32Params prm,
         bulk_load(smem_addr(ws), prm.wq + ((long long)cb * prm.Ci + ci0) * KK * prm.BCO, wbytes, bar);
     };
 
-    float acc[WPT][16];
+    const int lw = lane & 7, lc = lane >> 3;
+    float acc[8][8];
 #pragma unroll
-    for (int t = 0; t < WPT; ++t)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[t][j] = 0.f;
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
     // Padded column of this lane's first window.
-    const int cl = (wo0 + lane * WPT) * sd;
-    constexpr int C = WPT * (S > 0 ? S : 1);
-    constexpr int WIN = KW > 0 ? (WPT - 1) * S + KW : 1;
+    const int cl = (wo0 + 8 * lw) * sd;
+    constexpr int C = 8 * (S > 0 ? S : 1);
+    constexpr int WIN = KW > 0 ? 7 * S + KW : 1;
 
     if (tid == 0) issue(0);
     bool ok = true;
@@ -133,12 +139,12 @@ __global__ void __launch_bounds__(256) conv_fp32_kernel(const Fp32Params prm,
         const int nci = min(prm.chunk, prm.Ci - k * prm.chunk);
         for (int c = 0; c < nci; ++c) {
             for (int kh = 0; kh < Kh; ++kh) {
-                // row[col * XSTR] = padded input value at column col of this filter row.
+                // row[col * xstr] = padded input value at column col of this filter row.
                 const float* row;
                 int xstr;
                 if (IM2WIN) { row = xs + c * prm.pitch + kh - e0; xstr = Kh; }
                 else        { row = xs + (c * Kh + kh) * prm.boxw - prm.p - xbase; xstr = 1; }
-                const float* wr = ws + ((c * Kh + kh) * kw_n) * prm.BCO + warp * 16;
+                const float* wr = ws + ((c * Kh + kh) * kw_n) * prm.BCO + warp * 32 + lc * 8;
                 if constexpr (KW > 0) {
                     float v[WIN];
 #pragma unroll
@@ -146,39 +152,31 @@ __global__ void __launch_bounds__(256) conv_fp32_kernel(const Fp32Params prm,
 #pragma unroll
                     for (int j = C; j < WIN; ++j) {
                         float t = __shfl_down_sync(0xffffffffu, v[j % C], j / C);
-                        if (lane + j / C >= 32) t = row[(cl + j) * xstr];
+                        if (lw + j / C >= 8) t = row[(cl + j) * xstr];
                         v[j] = t;
                     }
 #pragma unroll
                     for (int kw = 0; kw < KW; ++kw) {
-                        const float4* w4 = reinterpret_cast<const float4*>(wr + kw * prm.BCO);
-                        float wv[16];
+                        const float4 wa = *reinterpret_cast<const float4*>(wr + kw * prm.BCO);
+                        const float4 wb4 = *reinterpret_cast<const float4*>(wr + kw * prm.BCO + 4);
+                        const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb4.x, wb4.y, wb4.z, wb4.w};
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            float4 f = w4[q];
-                            wv[4 * q] = f.x; wv[4 * q + 1] = f.y; wv[4 * q + 2] = f.z; wv[4 * q + 3] = f.w;
-                        }
+                        for (int i = 0; i < 8; ++i) {
+                            const float xv = v[i * S + kw];
 #pragma unroll
-                        for (int t = 0; t < WPT; ++t) {
-                            const float xv = v[t * S + kw];
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) acc[t][j] = fmaf(xv, wv[j], acc[t][j]);
+                            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(xv, wv[j], acc[i][j]);
                         }
                     }
                 } else {
                     for (int kw = 0; kw < kw_n; ++kw) {
-                        const float4* w4 = reinterpret_cast<const float4*>(wr + kw * prm.BCO);
-                        float wv[16];
+                        const float4 wa = *reinterpret_cast<const float4*>(wr + kw * prm.BCO);
+                        const float4 wb4 = *reinterpret_cast<const float4*>(wr + kw * prm.BCO + 4);
+                        const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb4.x, wb4.y, wb4.z, wb4.w};
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            float4 f = w4[q];
-                            wv[4 * q] = f.x; wv[4 * q + 1] = f.y; wv[4 * q + 2] = f.z; wv[4 * q + 3] = f.w;
-                        }
+                        for (int i = 0; i < 8; ++i) {
+                            const float xv = row[(cl + i * sd + kw) * xstr];
 #pragma unroll
-                        for (int t = 0; t < WPT; ++t) {
-                            const float xv = row[(cl + t * sd + kw) * xstr];
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) acc[t][j] = fmaf(xv, wv[j], acc[t][j]);
+                            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(xv, wv[j], acc[i][j]);
                         }
                     }
                 }
@@ -188,15 +186,23 @@ __global__ void __launch_bounds__(256) conv_fp32_kernel(const Fp32Params prm,
     }
     if (!ok) return;
 
-    const int co_base = cb * prm.BCO + warp * 16;
+    // Store: each channel row gets 8 consecutive columns (two 16-byte stores
+    // when the row is 16-byte aligned and all 8 columns are outputs).
+    const int co_base = cb * prm.BCO + warp * 32 + lc * 8;
+    const int wt = wo0 + 8 * lw;
+    const bool vec = (prm.Wo % 4) == 0 && wt + 8 <= prm.Wo;
 #pragma unroll
-    for (int t = 0; t < WPT; ++t) {
-        const int wo = wo0 + lane * WPT + t;
-        if (wo >= prm.Wo || wo >= wo0 + prm.WB) continue;
+    for (int j = 0; j < 8; ++j) {
+        const int co = co_base + j;
+        if (co >= prm.Co) continue;
+        float* out = prm.y + (((long long)n * prm.Co + co) * prm.Ho + ho) * prm.Wo + wt;
+        if (vec) {
+            reinterpret_cast<float4*>(out)[0] = make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
+            reinterpret_cast<float4*>(out)[1] = make_float4(acc[4][j], acc[5][j], acc[6][j], acc[7][j]);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int co = co_base + j;
-            if (co < prm.Co) prm.y[(((long long)n * prm.Co + co) * prm.Ho + ho) * prm.Wo + wo] = acc[t][j];
+            for (int i = 0; i < 8; ++i)
+                if (wt + i < prm.Wo) out[i] = acc[i][j];
         }
     }
 }
@@ -209,31 +215,20 @@ typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_
                                     CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 void* driver_entry(const char* name);   // conv_tc.cu
 
-template <int KW, int S, int WPT, bool IM2WIN>
+template <int KW, int S, bool IM2WIN>
 static cudaError_t launch_fp32_inst(const Fp32Params& prm, const CUtensorMap& map, int threads, size_t smem,
                                     long long blocks, cudaStream_t st) {
-    auto kern = conv_fp32_kernel<KW, S, WPT, IM2WIN>;
+    auto kern = conv_fp32_kernel<KW, S, IM2WIN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_after(kern, dim3((unsigned)blocks), dim3(threads), smem, st, prm, map);
 }
 
-template <int KW, int S, bool IM2WIN>
-static cudaError_t launch_fp32_wpt(int wpt, const Fp32Params& prm, const CUtensorMap& map, int threads,
-                                   size_t smem, long long blocks, cudaStream_t st) {
-    switch (wpt) {
-        case 1: return launch_fp32_inst<KW, S, 1, IM2WIN>(prm, map, threads, smem, blocks, st);
-        case 2: return launch_fp32_inst<KW, S, 2, IM2WIN>(prm, map, threads, smem, blocks, st);
-        default: return launch_fp32_inst<KW, S, 4, IM2WIN>(prm, map, threads, smem, blocks, st);
-    }
-}
-
 template <bool IM2WIN>
 static cudaError_t launch_fp32_shape(const conv2d_desc& d, const Fp32Params& prm, const CUtensorMap& map,
                                      int threads, size_t smem, long long blocks, cudaStream_t st) {
-    const int w = d.cc_wpt;
-#define CONV2D_FP32_CASE(KW_, S_)                                                               \
-    if (d.Kw == KW_ && d.s == S_) return launch_fp32_wpt<KW_, S_, IM2WIN>(w, prm, map, threads, smem, blocks, st);
+#define CONV2D_FP32_CASE(KW_, S_) \
+    if (d.Kw == KW_ && d.s == S_) return launch_fp32_inst<KW_, S_, IM2WIN>(prm, map, threads, smem, blocks, st);
     CONV2D_FP32_CASE(1, 1)
     CONV2D_FP32_CASE(3, 1)
     CONV2D_FP32_CASE(5, 1)
@@ -243,7 +238,7 @@ static cudaError_t launch_fp32_shape(const conv2d_desc& d, const Fp32Params& prm
     CONV2D_FP32_CASE(3, 2)
     CONV2D_FP32_CASE(7, 2)
 #undef CONV2D_FP32_CASE
-    return launch_fp32_wpt<0, 0, IM2WIN>(w, prm, map, threads, smem, blocks, st);
+    return launch_fp32_inst<0, 0, IM2WIN>(prm, map, threads, smem, blocks, st);
 }
 
 conv2d_status launch_conv_fp32(const conv2d_desc& d, const float* src, const float* wq, float* y, bool im2win,
@@ -252,26 +247,21 @@ conv2d_status launch_conv_fp32(const conv2d_desc& d, const float* src, const flo
     prm.src = src; prm.wq = wq; prm.y = y;
     prm.N = d.N; prm.Ci = d.Ci; prm.H = d.H; prm.W = d.W; prm.Co = d.Co; prm.Kh = d.Kh; prm.Kw = d.Kw;
     prm.s = d.s; prm.p = d.p; prm.Ho = d.Ho; prm.Wo = d.Wo; prm.Lp = d.Lp;
-    prm.BCO = 16 * d.cc_warps;
+    prm.BCO = 32 * d.cc_warps;
     prm.n_cb = (d.Co + prm.BCO - 1) / prm.BCO;
-    const int lanes_w = 32 * d.cc_wpt;
-    int WB = d.Wo < lanes_w ? d.Wo : lanes_w;
-    if (!im2win) {
-        const int maxwb = (256 - 3 - d.Kw) / d.s + 1;   // staged row width <= 256 (box limit)
-        if (WB > maxwb) WB = maxwb;
-    }
-    prm.WB = WB;
-    prm.n_wb = (d.Wo + WB - 1) / WB;
-    // Staged input per channel, with slack so that idle lanes read inside the buffer.
-    const int slack = lanes_w * d.s + d.Kw + 8;
+    prm.n_wb = (d.Wo + kCcCols - 1) / kCcCols;
+    // Staged input per channel, with slack so that lanes past Wo read inside the buffer.
+    const int span = (kCcCols - 1) * d.s + d.Kw;          // padded columns 64 windows touch
+    const int slack = kCcCols * d.s + d.Kw + 8;
     int per_ci_x;
     if (im2win) {
         // Staged range [e0, e1) is rounded out to 16 bytes on both ends (+6 at most).
-        prm.pitch = ((((lanes_w - 1) * d.s + d.Kw) * d.Kh + 8) + 3) & ~3;
+        prm.pitch = ((span * d.Kh + 8) + 3) & ~3;
         per_ci_x = prm.pitch;
         prm.boxw = 0;
     } else {
-        prm.boxw = (((WB - 1) * d.s + d.Kw + 3) + 3) & ~3;
+        prm.boxw = ((span + 3) + 3) & ~3;
+        if (prm.boxw > 256) return CONV2D_ERR_UNSUPPORTED;   // tensor-map box limit
         prm.pitch = d.Kh * prm.boxw;
         per_ci_x = prm.pitch;
     }

@@ -18,8 +18,7 @@ struct conv2d_desc {
     conv2d_algo algo;     // resolved (never AUTO)
     // fp32 CUDA-core paths.
     int Lp;               // im2win strip pitch in floats: Wp*Kh rounded up to 4
-    int cc_warps;         // warps per block (16 output channels each)
-    int cc_wpt;           // output columns per lane (1, 2 or 4)
+    int cc_warps;         // warps per block (32 output channels each)
     // Tensor-core paths.
     int Ci8;              // Ci rounded up to 8 (16-byte channel vectors)
     int taps;             // filter taps per K-chunk group: Kw (im2win) or Kh*Kw (implicit)

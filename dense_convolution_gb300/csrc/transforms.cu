@@ -322,7 +322,7 @@ cudaError_t launch_pack_filter_tc(const void* w, void* wq, const conv2d_desc& d,
 }
 
 // CUDA-core filter: wq[cb][ci][k][j] = w[cb*BCO + j][ci][k] (k = kh*Kw + kw),
-// BCO = 16 * warps output channels per block, zero past Co, so that a block's
+// BCO = 32 * warps output channels per block, zero past Co, so that a block's
 // slice for a run of input channels is one contiguous range.  One block per
 // (cb, ci): reads BCO runs of Kh*Kw floats, writes Kh*Kw*BCO floats in order.
 __global__ void __launch_bounds__(256) pack_filter_f32_kernel(const float* __restrict__ w, float* __restrict__ wq,
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(256) pack_filter_f32_kernel(const float* __res
 }
 
 cudaError_t launch_pack_filter_f32(const float* w, float* wq, const conv2d_desc& d, cudaStream_t st) {
-    const int BCO = 16 * d.cc_warps;
+    const int BCO = 32 * d.cc_warps;
     const int ncb = (d.Co + BCO - 1) / BCO;
     if (ncb > 65535) return cudaErrorInvalidConfiguration;
     pack_filter_f32_kernel<<<dim3(d.Ci, ncb), 256, 0, st>>>(w, wq, d.Co, d.Ci, d.Kh * d.Kw, BCO);
