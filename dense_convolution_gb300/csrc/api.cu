@@ -29,21 +29,34 @@ double padded_waste(const conv2d_desc& d) {
     return 1.0 - (double)d.Ho * d.Wo / grid;
 }
 
-// Fraction of the tensor-core K extent that holds real filter taps, for the
-// two operand sources (the rest is zero fill up to the 64-element chunk).
-double tc_k_efficiency(const conv2d_desc& d, bool im2win) {
+// im2win window tensor: channels per padded column (row, channel pairs).
+long long window_ck(const conv2d_desc& d) {
     const long long ci8 = (d.Ci + 7) / 8 * 8;
-    const long long chunk = im2win ? (long long)d.Kh * ci8 : ci8;
-    const long long padded = (chunk + kTcBlockK - 1) / kTcBlockK * kTcBlockK;
-    return (double)(im2win ? (long long)d.Kh * d.Ci : d.Ci) / (double)padded;
+    return ci8 <= 16 ? ((long long)d.Kh * d.Ci + 7) / 8 * 8 : (long long)d.Kh * ci8;
+}
+
+// Fraction of the tensor-core K extent that holds real filter taps, for the
+// two operand sources (the rest is zero fill up to the 64-element chunk):
+// implicit runs Kh*Kw taps of Ci8 channels, im2win one window of Kw*Ck.
+double tc_k_efficiency(const conv2d_desc& d, bool im2win) {
+    auto up64 = [](long long v) { return (v + kTcBlockK - 1) / kTcBlockK * kTcBlockK; };
+    if (im2win) return (double)d.Kh * d.Kw * d.Ci / (double)up64(d.Kw * window_ck(d));
+    return (double)d.Ci / (double)up64((d.Ci + 7) / 8 * 8);
+}
+
+// im2win virtual grid: Wq output slots per image row, Wq*s window columns per
+// row (at least W+2p), rounded up to 4 when Wo % 4 == 0 (8-byte stores).
+int window_grid_pitch(const conv2d_desc& d) {
+    int wq = (d.Wp + d.s - 1) / d.s;
+    if (wq < d.Wo) wq = d.Wo;
+    if (d.Wo % 4 == 0) wq = (wq + 3) / 4 * 4;
+    return wq;
 }
 
 // Shape limits of the tensor-core kernels (im2col-mode TMA corners are 8-bit
 // signed for a 4-D map; channel pitch must be a 16-byte multiple).
 bool tc_shape_ok(const conv2d_desc& d, bool im2win) {
-    if (im2win) {
-        if (d.Kw - 1 > 128) return false;
-    } else {
+    if (!im2win) {
         if (d.p > 128 || d.p - (d.Kw - 1) < -128 || d.p - (d.Kh - 1) < -128) return false;
         if (d.p - (d.Kw - 1) > 127 || d.p - (d.Kh - 1) > 127) return false;
         if (d.layout == CONV2D_LAYOUT_NHWC && d.Ci % 8 != 0) return false;
@@ -105,8 +118,10 @@ conv2d_status finalize(conv2d_desc& d) {
             return CONV2D_ERR_UNSUPPORTED;
         }
         d.Ci8 = (d.Ci + 7) / 8 * 8;
-        d.taps = im2win ? d.Kw : d.Kh * d.Kw;
-        const long long chunk = im2win ? (long long)d.Kh * d.Ci8 : d.Ci8;
+        if (window_ck(d) * d.Kw > kMaxElems) return CONV2D_ERR_UNSUPPORTED;
+        d.Ck = (int)window_ck(d);
+        d.taps = im2win ? 1 : d.Kh * d.Kw;
+        const long long chunk = im2win ? (long long)d.Kw * d.Ck : d.Ci8;
         d.CP = (int)((chunk + kTcBlockK - 1) / kTcBlockK * kTcBlockK);
         d.BN = d.Co <= 64 ? 64 : (d.Co <= 128 ? 128 : 256);
         if ((long long)d.Ci * d.Kh * d.Kw > 16384) return CONV2D_ERR_UNSUPPORTED;   // per-channel filter staging
@@ -122,7 +137,11 @@ conv2d_status finalize(conv2d_desc& d) {
             if (rows * d.Ci8 > kMaxElems * 4) return CONV2D_ERR_UNSUPPORTED;
             d.ws_input = (size_t)(rows * d.Ci8) * 2;
         } else if (im2win) {
-            const long long win = (long long)d.N * d.Ho * d.Wp * d.Kh * d.Ci8;
+            d.Hp = d.Ho;
+            d.Wq = window_grid_pitch(d);
+            const long long rows = (long long)d.N * d.Ho * d.Wq;
+            if (rows + kTcBlockM > kMaxElems) return CONV2D_ERR_UNSUPPORTED;
+            const long long win = rows * d.s * d.Ck;
             if (win > kMaxElems * 4) return CONV2D_ERR_UNSUPPORTED;
             d.ws_input = (size_t)win * 2;
         } else if (d.layout == CONV2D_LAYOUT_NCHW) {
@@ -240,7 +259,9 @@ conv2d_status fwd_impl(conv2d_desc_t dp, const void* x, const void* w, void* y, 
             break;
         case CONV2D_ALGO_IM2WIN_TC:
             e = launch_pack_filter_tc(w, wq, d, true, st);
-            if (e == cudaSuccess) e = launch_window_cl16(x, win, d.N, d.Ci, d.H, d.W, d.Ci8, d.Ho, d.Wp, d.Kh, d.s, d.p, st);
+            if (e == cudaSuccess)
+                e = launch_window_cl16(x, win, d.N, d.Ci, d.H, d.W, d.Ci8, d.Ck, d.Ho, d.Wq * d.s, d.Kh, d.s, d.p,
+                                       st);
             if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
             if (e == cudaSuccess) s = launch_conv_tc(d, win, wq, y, 1, st);
             break;

@@ -8,16 +8,24 @@
 //   N = Co output channels,
 //   K = taps x channel chunks, 64 16-bit elements per pipeline stage.
 //
-// A tile (128 pixels x 64 K) comes from one im2col-mode TMA load of a
-// channels-innermost tensor: the copy engine walks 128 consecutive output
-// pixels (across row and image boundaries) and, for each, reads 64 channels
-// at the pixel's window origin plus a filter-tap offset.
-//   im2win    source = the window tensor [N][Ho][W+2p][Kh*Ci8]; a window is
-//             Kw consecutive "pixels" of Kh*Ci8 channels (Eq. (2)/(3) of the
-//             im2win paper, NHWC variant); tap t = kw, offset (kw, 0).
-//   implicit  source = X in NHWC [N][H][W][Ci8]; tap t = (kh, kw), offset
-//             (kw, kh); the map's bounding box shifts by -p and the walk
-//             strides by s, so padding is the copy engine's zero fill.
+// A tile (128 pixels x 64 K) comes from one TMA load, in one of two forms:
+//   implicit  (kernel MODE 0) an im2col-mode load of X in NHWC [N][H][W][Ci8]:
+//             the copy engine walks 128 consecutive output pixels (across
+//             row and image boundaries) and reads 64 channels at each
+//             pixel's window origin plus the tap offset (kw, kh); the map's
+//             bounding box shifts by -p and the walk strides by s, so padding
+//             is the copy engine's zero fill.  Tap t = (kh, kw).
+//   grid      (kernel MODE 1) a tiled load of 128 consecutive rows of a
+//             "virtual pixel grid" [N][Hv][Wq]: row q is one output position,
+//             rows past Wo in an image row (or past Ho) are junk that the
+//             epilogue drops.  Two sources use it:
+//     padded  the zero-padded NHWC copy [N][H+2p][Wq][Ci8], stride 1: virtual
+//             row q reads pixel q + kh*Wq + kw for tap (kh, kw); kpb
+//             neighbouring taps share one halo box of 128 + kpb - 1 rows.
+//     im2win  the window tensor [N][Ho][Wq*s][Ck] (Eq. (2)/(3) of the im2win
+//             paper, channels-last): the whole window of output (ho, wo) is
+//             the Kw*Ck contiguous elements from column wo*s on, so the map's
+//             rows are s*Ck elements apart and overlap; one tap, K = Kw*Ck.
 // B tile (BN channels x 64 K) is a tiled TMA load of the repacked filter.
 //
 // Warp roles (192 threads, one CTA per SM, persistent over tiles):
@@ -41,10 +49,9 @@ struct TcParams {
     int M, HoWo, Ho, Wo, Co;
     int n_n_tiles, n_tiles;
     int n_cchunks, n_kchunks, CP, Kw, s, p;
-    int amode;          // A source: 0 implicit (im2col over NHWC X), 1 im2win (im2col over the window
-                        // tensor), 2 padded (tiled boxes over the zero-padded NHWC copy)
-    int N, Wq, HpWq;    // padded mode: batch, row pitch and image pitch of the padded grid
-    int vec_store;      // modes 0/1: Ho*Wo % 8 == 0 (16-byte stores); mode 2: Wo % 4 == 0 (8-byte stores)
+    int amode;          // A source: 0 implicit, 1 im2win, 2 padded (1 and 2 run kernel MODE 1)
+    int N, Wq, HpWq;    // grid modes: batch, row pitch and image pitch of the virtual pixel grid
+    int vec_store;      // MODE 0: Ho*Wo % 8 == 0 (16-byte stores); MODE 1: Wo % 4 == 0 (8-byte stores)
     int kpb;            // MMA chunks per pipeline stage (one A copy + one B copy per stage)
     int stages;         // depth of the shared-memory ring (<= kMaxStages)
     int stage_bytes;    // A region + kpb B chunks
@@ -71,9 +78,8 @@ struct TcConfig {
 //   [stage 0 .. stage S-1][epilogue staging][barriers]; a stage is
 //   [kpb A chunks][kpb B chunks], each chunk 1024-byte aligned (128-byte swizzle).
 
-// MODE is the A source (0 implicit, 1 im2win, 2 padded with halo tiles);
-// each mode compiles to its own kernel so the producer and MMA loops carry no
-// run-time mode tests.
+// MODE is the A addressing (0 im2col walk, 1 virtual-grid rows); each compiles
+// to its own kernel so the producer and MMA loops carry no run-time mode tests.
 template <int BN, bool BF16, int MODE>
 __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__ CUtensorMap amap,
                                                          const __grid_constant__ CUtensorMap bmap,
@@ -128,7 +134,7 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
                 const int m0 = (tile / prm.n_n_tiles) * kTcBlockM;
                 const int n0 = (tile % prm.n_n_tiles) * BN;
                 int img = 0, ho = 0, wo = 0;
-                if constexpr (MODE != 2) {
+                if constexpr (MODE == 0) {
                     img = m0 / prm.HoWo;
                     const int r = m0 - img * prm.HoWo;
                     ho = r / prm.Wo;
@@ -137,7 +143,7 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
                 for (int sp = 0; sp < prm.n_sp; ++sp) {
                     // Stage sp covers taps t..t+kpb-1 (halo) or chunk sp, channel block cb.
                     int t, cb;
-                    if constexpr (MODE == 2) {
+                    if constexpr (MODE == 1) {
                         cb = sp % prm.n_cchunks;
                         const int rest = sp / prm.n_cchunks, ngw = prm.Kw / prm.kpb;
                         t = (rest / ngw) * prm.Kw + (rest % ngw) * prm.kpb;
@@ -150,14 +156,13 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
                     mbar_arrive_expect_tx(full_bar(stage), prm.stage_bytes);
                     const uint32_t a_dst = smem_addr(smem + stage * prm.stage_bytes);
                     const uint32_t b_dst = a_dst + prm.a_bytes;
-                    if constexpr (MODE == 2) {
+                    if constexpr (MODE == 1) {
                         // Virtual pixel q reads padded pixel q + kh*Wq + kw.  In halo mode
                         // the box has 128 + kpb - 1 rows: taps kw..kw+kpb-1 are the same
-                        // rows shifted by one pixel each, so they share one copy.
+                        // rows shifted by one pixel each, so they share one copy.  (im2win:
+                        // one tap, t = 0.)
                         const int kh = t / prm.Kw, kw = t - kh * prm.Kw;
                         tma_load_2d(a_dst, &amap, full_bar(stage), c0, m0 + kh * prm.Wq + kw);
-                    } else if constexpr (MODE == 1) {
-                        tma_load_im2col_4d(a_dst, &amap, full_bar(stage), c0, wo * prm.s, ho, img, (uint16_t)t, 0);
                     } else {
                         const int kh = t / prm.Kw, kw = t - kh * prm.Kw;
                         tma_load_im2col_4d(a_dst, &amap, full_bar(stage), c0, wo * prm.s - prm.p,
@@ -166,7 +171,7 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
                     // Filter chunks of taps t..t+kpb-1, channel block cb: one copy (a 3-D
                     // box in halo mode; higher-rank maps cost the copy engine more, so
                     // the other modes keep a 2-D map).
-                    if constexpr (MODE == 2) tma_load_3d(b_dst, &bmap, full_bar(stage), c0, n0, t);
+                    if constexpr (MODE == 1) tma_load_3d(b_dst, &bmap, full_bar(stage), c0, n0, t);
                     else                     tma_load_2d(b_dst, &bmap, full_bar(stage), t * prm.CP + c0, n0);
                     ++issued;
                     if (++stage == S) { stage = 0; phase ^= 1; }
@@ -199,7 +204,7 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
                     tc_fence_after();
                     const uint32_t a_base = smem_addr(smem + stage * prm.stage_bytes);
                     const uint32_t b_base = a_base + prm.a_bytes;
-                    const int kpb = MODE == 2 ? prm.kpb : 1;
+                    const int kpb = MODE == 1 ? prm.kpb : 1;
                     for (int i = 0; i < kpb; ++i) {
                         // Halo: tap kw0+i reads the A tile from row i (128 bytes per row).
                         const uint32_t a_sub = a_base + i * 128u, b_sub = b_base + i * Cfg::kBBytes;
@@ -242,8 +247,8 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
             const int m0 = (tile / prm.n_n_tiles) * kTcBlockM;
             const int n0 = (tile % prm.n_n_tiles) * BN;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
-            if constexpr (MODE == 2) {
-                // Rows are virtual pixels of the padded grid [N][Hp][Wq]; only
+            if constexpr (MODE == 1) {
+                // Rows are virtual pixels of the grid [N][Hv][Wq]; only
                 // those with y < Ho and x < Wo are outputs.  With Wo % 4 == 0 a
                 // 4-pixel group is all-valid or all-junk: 8-byte stores.
                 const int g = et & 31;
@@ -419,11 +424,7 @@ static cudaError_t launch_tc_bn(int BN, const CUtensorMap& a, const CUtensorMap&
 template <bool BF16>
 static cudaError_t launch_tc_mode(int BN, int amode, const CUtensorMap& a, const CUtensorMap& b, const TcParams& prm,
                                   int grid, cudaStream_t st) {
-    switch (amode) {
-        case 0:  return launch_tc_bn<BF16, 0>(BN, a, b, prm, grid, st);
-        case 1:  return launch_tc_bn<BF16, 1>(BN, a, b, prm, grid, st);
-        default: return launch_tc_bn<BF16, 2>(BN, a, b, prm, grid, st);
-    }
+    return amode == 0 ? launch_tc_bn<BF16, 0>(BN, a, b, prm, grid, st) : launch_tc_bn<BF16, 1>(BN, a, b, prm, grid, st);
 }
 
 conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* wq, void* y, int amode,
@@ -436,23 +437,6 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
         d.dtype == CONV2D_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 
     CUtensorMap amap, bmap;
-    // A: im2col view of a channels-innermost tensor (C, W, H, N).
-    cuuint64_t C, Wd, Hd;
-    int lower[2], upper[2];
-    cuuint32_t estr[4];
-    if (im2win) {
-        C = (cuuint64_t)d.Kh * d.Ci8; Wd = d.Wp; Hd = d.Ho;
-        lower[0] = 0; lower[1] = 0;
-        upper[0] = -(d.Kw - 1); upper[1] = 0;
-        estr[0] = 1; estr[1] = d.s; estr[2] = 1; estr[3] = 1;
-    } else {
-        C = d.Ci8; Wd = d.W; Hd = d.H;
-        lower[0] = -d.p; lower[1] = -d.p;
-        upper[0] = d.p - (d.Kw - 1); upper[1] = d.p - (d.Kh - 1);
-        estr[0] = 1; estr[1] = d.s; estr[2] = d.s; estr[3] = 1;
-    }
-    cuuint64_t adims[4] = {C, Wd, Hd, (cuuint64_t)d.N};
-    cuuint64_t astr[3] = {C * 2, C * 2 * Wd, C * 2 * Wd * Hd};
     // Ring layout.  Padded mode groups kpb neighbouring taps of one filter row
     // per stage around one halo A tile (128 + kpb - 1 pixel rows): the copy
     // engine delivers about the same bytes per SM per second whatever the
@@ -461,6 +445,9 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     const int b_chunk = d.BN * kTcBlockK * 2;
     const int tail = 32 * kTcBlockM * 2 + 256 + 1024;
     const bool halo = amode == 2;
+    const bool grid_rows = amode != 0;
+    // Last virtual row that is an output, plus one (grid modes).
+    const int m_end = grid_rows ? (d.N - 1) * d.Hp * d.Wq + (d.Ho - 1) * d.Wq + d.Wo : 0;
     int kpb = 1, a_rows = kTcBlockM;
     if (halo) {
         for (int c = d.Kw; c >= 2; --c) {
@@ -475,7 +462,18 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     if (stages < 2) return CONV2D_ERR_UNSUPPORTED;
 
     CUresult r;
-    if (amode == 2) {
+    if (im2win) {
+        // Window tensor rows of Ck elements, Wq*s per image row: virtual row q
+        // starts s*Ck elements after row q-1 and spans Kw*Ck elements.  Rows
+        // at or past m_end read as zero, so no copy runs off the tensor's end.
+        cuuint64_t wdims[2] = {(cuuint64_t)d.Kw * d.Ck, (cuuint64_t)m_end};
+        cuuint64_t wstr[1] = {(cuuint64_t)d.s * d.Ck * 2};
+        cuuint32_t wbox[2] = {(cuuint32_t)kTcBlockK, (cuuint32_t)kTcBlockM};
+        cuuint32_t westr[2] = {1, 1};
+        r = enc_tiled(&amap, dt, 2, const_cast<void*>(src), wdims, wstr, wbox, westr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else if (amode == 2) {
         // Padded channels-last copy viewed as [N*Hp*Wq pixel rows][Ci8 channels];
         // box 64 channels x a_rows pixels (rows past the end read as zero).
         cuuint64_t pdims[2] = {(cuuint64_t)d.Ci8, (cuuint64_t)d.N * d.Hp * d.Wq};
@@ -486,16 +484,21 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else {
+        // im2col view of X in NHWC, dims (Ci8, W, H, N).
+        cuuint64_t adims[4] = {(cuuint64_t)d.Ci8, (cuuint64_t)d.W, (cuuint64_t)d.H, (cuuint64_t)d.N};
+        cuuint64_t astr[3] = {adims[0] * 2, adims[0] * 2 * adims[1], adims[0] * 2 * adims[1] * adims[2]};
+        int lower[2] = {-d.p, -d.p}, upper[2] = {d.p - (d.Kw - 1), d.p - (d.Kh - 1)};
+        cuuint32_t estr[4] = {1, (cuuint32_t)d.s, (cuuint32_t)d.s, 1};
         r = enc_im2col(&amap, dt, 4, const_cast<void*>(src), adims, astr, lower, upper, kTcBlockK, kTcBlockM, estr,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     if (r != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
 
-    // B: repacked filter [Co][taps][CP].  Halo mode: (CP, Co, tap) with box
+    // B: repacked filter [Co][taps][CP].  Grid modes: (CP, Co, tap) with box
     // 64 x BN x kpb = the chunks of kpb consecutive taps for one channel block;
     // otherwise 2-D (taps*CP, Co) with box 64 x BN.
-    if (halo) {
+    if (grid_rows) {
         cuuint64_t bdims[3] = {(cuuint64_t)d.CP, (cuuint64_t)d.Co, (cuuint64_t)d.taps};
         cuuint64_t bstr[2] = {(cuuint64_t)d.taps * d.CP * 2, (cuuint64_t)d.CP * 2};
         cuuint32_t bbox[3] = {(cuuint32_t)kTcBlockK, (cuuint32_t)d.BN, (cuuint32_t)kpb};
@@ -515,8 +518,8 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     if (r != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
 
     TcParams prm{};
-    // M runs over output pixels, or over the padded grid up to the last output (padded mode).
-    prm.M = amode == 2 ? (d.N - 1) * d.Hp * d.Wq + (d.Ho - 1) * d.Wq + d.Wo : d.N * d.Ho * d.Wo;
+    // M runs over output pixels, or over the virtual grid up to the last output (grid modes).
+    prm.M = grid_rows ? m_end : d.N * d.Ho * d.Wo;
     prm.N = d.N;
     prm.Wq = d.Wq;
     prm.HpWq = d.Hp * d.Wq;
@@ -535,7 +538,7 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     prm.halo = halo ? 1 : 0;
     prm.n_sp = halo ? d.Kh * (d.Kw / kpb) * n_cchunks : d.taps * n_cchunks;
     prm.y = y;
-    if (amode == 2)
+    if (grid_rows)
         prm.vec_store = ((d.Wo % 4) == 0 && (d.Wq % 4) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) ? 1 : 0;
     else
         prm.vec_store = ((prm.HoWo % 8) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) ? 1 : 0;

@@ -21,10 +21,15 @@ struct conv2d_desc {
     int cc_warps;         // warps per block (32 output channels each)
     // Tensor-core paths.
     int Ci8;              // Ci rounded up to 8 (16-byte channel vectors)
+    int Ck;               // im2win window: channels per padded column.  Ci8 <= 16: the Kh*Ci
+                          // (row, channel) pairs packed densely, c = u*Ci + ci, rounded up to 8;
+                          // otherwise Kh*Ci8 with c = u*Ci8 + ci
     int taps;             // filter taps per K-chunk group: Kw (im2win) or Kh*Kw (implicit)
     int CP;               // channel extent per tap, padded to the 64-element K chunk
     int BN;               // output channels per MMA tile (64, 128 or 256)
-    int Hp, Wq;           // padded algorithm: padded height H+2p, row pitch (W+2p rounded up to 4 when Wo % 4 == 0)
+    int Hp, Wq;           // virtual pixel grid [N][Hp][Wq] of the grid-row tensor-core paths.  Padded:
+                          // H+2p rows of pitch W+2p (rounded up to 4 when Wo % 4 == 0).  im2win: Ho rows
+                          // of Wq output slots (window tensor rows hold Wq*s columns)
     // Workspace layout (bytes): packed filter at 0, input-side tensor after it.
     size_t ws_weights, ws_input_off, ws_input, ws_total;
 };
@@ -59,8 +64,8 @@ inline cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block,
 
 // transforms.cu
 cudaError_t launch_im2win_strips_f32(const float* x, float* xw, const conv2d_desc& d, cudaStream_t st);
-cudaError_t launch_window_cl16(const void* x, void* out, int N, int Ci, int H, int W, int Ci8, int R, int Wq,
-                               int Kh, int s, int p, cudaStream_t st);
+cudaError_t launch_window_cl16(const void* x, void* out, int N, int Ci, int H, int W, int Ci8, int Ck, int R,
+                               int Wq, int Kh, int s, int p, cudaStream_t st);
 cudaError_t launch_nchw_to_nhwc16(const void* x, void* out, int N, int C, int H, int W, int C8, cudaStream_t st);
 cudaError_t launch_nchw_to_padded_nhwc16(const void* x, void* out, const conv2d_desc& d, cudaStream_t st);
 cudaError_t launch_pack_filter_tc(const void* w, void* wq, const conv2d_desc& d, bool im2win, cudaStream_t st);

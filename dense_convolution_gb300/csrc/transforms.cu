@@ -221,29 +221,35 @@ __global__ void __launch_bounds__(256) window_cl16_tiled_kernel(const uint16_t* 
     pdl_wait();   // complete only after the filter repack launched before us
 }
 
-// Small-channel version (Ci8 <= 16): one thread builds one 8-channel vector;
-// consecutive threads write consecutive vectors.
+// Small-channel version (Ci8 <= 16): the Kh*Ci (row, channel) pairs of a
+// padded column are packed densely, c = u*Ci + ci, and rounded up to Ck (a
+// multiple of 8); one thread builds one 8-element vector, consecutive
+// threads write consecutive vectors.  With Ci a multiple of 8 this is the
+// same layout as the tiled version.
 __global__ void __launch_bounds__(256) window_cl16_small_kernel(const uint16_t* __restrict__ x,
                                                                 uint4* __restrict__ out, int Ci, int H, int W,
-                                                                int Ci8, int R, int Wq, int Kh, int s, int p,
+                                                                int Ck, int R, int Wq, int Kh, int s, int p,
                                                                 long long total_vec) {
     pdl_launch_dependents();
-    const int cgs = Ci8 / 8;
+    const int cgs = Ck / 8;
+    const int KC = Kh * Ci;
     for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total_vec;
          q += (long long)gridDim.x * blockDim.x) {
         long long t = q;
         const int cg = (int)(t % cgs); t /= cgs;
-        const int u = (int)(t % Kh);   t /= Kh;
         const int kx = (int)(t % Wq);  t /= Wq;
         const int r = (int)(t % R);
         const long long n = t / R;
-        const int y = r * s + u - p, xx = kx - p;
+        const int xx = kx - p;
         uint32_t w[4] = {0, 0, 0, 0};
-        if (y >= 0 && y < H && xx >= 0 && xx < W) {
+        if (xx >= 0 && xx < W) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                int c = cg * 8 + j;
-                uint32_t v = c < Ci ? x[((n * Ci + c) * H + y) * (long long)W + xx] : 0u;
+                const int c = cg * 8 + j;
+                const int u = c / Ci, ci = c - u * Ci;
+                const int y = r * s + u - p;
+                uint32_t v = 0;
+                if (c < KC && y >= 0 && y < H) v = x[((n * Ci + ci) * H + y) * (long long)W + xx];
                 w[j >> 1] |= v << (16 * (j & 1));
             }
         }
@@ -252,16 +258,16 @@ __global__ void __launch_bounds__(256) window_cl16_small_kernel(const uint16_t* 
     pdl_wait();   // complete only after the filter repack launched before us
 }
 
-cudaError_t launch_window_cl16(const void* x, void* out, int N, int Ci, int H, int W, int Ci8, int R, int Wq,
-                               int Kh, int s, int p, cudaStream_t st) {
+cudaError_t launch_window_cl16(const void* x, void* out, int N, int Ci, int H, int W, int Ci8, int Ck, int R,
+                               int Wq, int Kh, int s, int p, cudaStream_t st) {
     const uint16_t* xi = static_cast<const uint16_t*>(x);
     uint4* o = static_cast<uint4*>(out);
     if (Ci8 <= 16) {
-        long long total_vec = (long long)N * R * Wq * Kh * (Ci8 / 8);
+        long long total_vec = (long long)N * R * Wq * (Ck / 8);
         long long blocks = (total_vec + 255) / 256, cap = (long long)device_sm_count() * 16;
         int grid = (int)(blocks < cap ? blocks : cap);
         return launch_after(window_cl16_small_kernel, dim3(grid < 1 ? 1 : grid), dim3(256), 0, st, xi, o, Ci, H, W,
-                            Ci8, R, Wq, Kh, s, p, total_vec);
+                            Ck, R, Wq, Kh, s, p, total_vec);
     } else {
         int n_xt = (Wq + kWinTileX - 1) / kWinTileX, n_ct = (Ci8 + kWinTileC - 1) / kWinTileC;
         long long blocks = (long long)n_xt * n_ct * Kh * N * R;
@@ -273,7 +279,9 @@ cudaError_t launch_window_cl16(const void* x, void* out, int N, int Ci, int H, i
 
 // ---------------------------------------------------------------- filter repacks
 // Tensor-core filter: wq[co][t][c], c in [0, CP).
-//   im2win   t = kw, c = u*Ci8 + ci  (the window tensor's (u, ci) column order)
+//   im2win   one tap; c = kw*Ck + u*cdiv + ci, the order of a window in the
+//            window tensor (cdiv = Ci when its (u, ci) pairs are packed
+//            densely, Ci8 otherwise)
 //   implicit t = kh*Kw + kw, c = ci
 // Entries outside the real filter are zero.  One block per output channel:
 // the channel's Ci*Kh*Kw filter (contiguous) is staged in shared memory, then
@@ -282,7 +290,7 @@ constexpr int kPackSmemElems = 16384;   // 32 KB of 16-bit filter per output cha
 
 __global__ void __launch_bounds__(256) pack_filter_tc_kernel(const uint16_t* __restrict__ w,
                                                              uint16_t* __restrict__ wq, int Ci, int Kh, int Kw,
-                                                             int Ci8, int taps, int CP, int im2win) {
+                                                             int cdiv, int ck, int taps, int CP, int im2win) {
     __shared__ __align__(16) uint16_t fw[kPackSmemElems];
     pdl_launch_dependents();
     const int co = blockIdx.x;
@@ -305,9 +313,14 @@ __global__ void __launch_bounds__(256) pack_filter_tc_kernel(const uint16_t* __r
         for (int j = 0; j < 8; ++j) {
             const int c = c0 + j;
             int ci, kh, kw;
-            if (im2win) { kw = t; kh = c / Ci8; ci = c - kh * Ci8; }
-            else        { kh = t / Kw; kw = t - kh * Kw; ci = c; }
-            const uint32_t h = (ci < Ci && kh < Kh) ? fw[ci * KK + kh * Kw + kw] : 0u;
+            if (im2win) {
+                kw = c / ck;
+                const int cc = c - kw * ck;
+                kh = cc / cdiv; ci = cc - kh * cdiv;
+            } else {
+                kh = t / Kw; kw = t - kh * Kw; ci = c;
+            }
+            const uint32_t h = (ci < Ci && kh < Kh && kw < Kw) ? fw[ci * KK + kh * Kw + kw] : 0u;
             v[j >> 1] |= h << (16 * (j & 1));
         }
         dst[i] = make_uint4(v[0], v[1], v[2], v[3]);
@@ -316,8 +329,9 @@ __global__ void __launch_bounds__(256) pack_filter_tc_kernel(const uint16_t* __r
 
 cudaError_t launch_pack_filter_tc(const void* w, void* wq, const conv2d_desc& d, bool im2win, cudaStream_t st) {
     if ((long long)d.Ci * d.Kh * d.Kw > kPackSmemElems) return cudaErrorInvalidValue;
+    const int cdiv = d.Ci8 <= 16 ? d.Ci : d.Ci8;
     pack_filter_tc_kernel<<<d.Co, 256, 0, st>>>(static_cast<const uint16_t*>(w), static_cast<uint16_t*>(wq), d.Ci,
-                                                d.Kh, d.Kw, d.Ci8, d.taps, d.CP, im2win ? 1 : 0);
+                                                d.Kh, d.Kw, cdiv, d.Ck, d.taps, d.CP, im2win ? 1 : 0);
     return cudaGetLastError();
 }
 
