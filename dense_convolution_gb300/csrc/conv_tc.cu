@@ -28,12 +28,14 @@
 //             rows are s*Ck elements apart and overlap; one tap, K = Kw*Ck.
 // B tile (BN channels x 64 K) is a tiled TMA load of the repacked filter.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over tiles):
+// Warp roles (192 threads; one CTA per SM, two for tiles up to 128 channels wide; persistent over tiles):
 //   warp 0     TMA producer (one elected lane), STAGES-deep shared-memory ring
 //   warp 1     TMEM allocation + MMA issue (one lane): 4 x (128xBNx16) per stage
 //   warps 2-5  epilogue: tcgen05.ld of their 32-lane TMEM quarter, round to the
 //              output type, store NCHW (32 consecutive pixels per store)
-// Two TMEM accumulators let the epilogue of tile i overlap the MMAs of i+1.
+// Two TMEM accumulators let the epilogue of tile i overlap the MMAs of i+1
+// (with 256-wide tiles and two CTAs per SM, one each: the other CTA's MMAs
+// fill the gap).
 // Every wait is bounded (ptx.cuh); on a timeout the CTA drains what it issued,
 // frees its TMEM and exits with the device status word set.
 #include <cuda.h>
@@ -59,18 +61,20 @@ struct TcParams {
     int halo;           // padded mode: a stage holds kpb neighbouring taps kw0..kw0+kpb-1 of one
                         // filter row, all read from one halo A tile at row offsets 0..kpb-1
     int n_sp;           // pipeline stages per output tile
+    int n_acc;          // TMEM accumulators (BN columns each): 2 lets the epilogue of one tile
+                        // overlap the MMAs of the next; 1 when two CTAs share an SM's TMEM
     void* y;
 };
 
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448;                               // 227 KB per block
+constexpr int kSmemPerSm = 233472;                               // 228 KB per SM, 1 KB of it reserved per block
 
 template <int BN>
 struct TcConfig {
     static constexpr int kABytes = kTcBlockM * kTcBlockK * 2;   // one 128 x 64 A chunk: 16 KB
     static constexpr int kBBytes = BN * kTcBlockK * 2;          // one BN x 64 B chunk
     static constexpr int kChunkBytes = kABytes + kBBytes;
-    static constexpr int kTmemCols = 2 * BN;                    // two accumulators
     static constexpr int kEpiBytes = 32 * kTcBlockM * 2;        // epilogue staging: 32 channels x 128 pixels
     static constexpr int kTailBytes = kEpiBytes + 256 + 1024;   // staging + barriers + alignment slack
 };
@@ -81,7 +85,7 @@ struct TcConfig {
 // MODE is the A addressing (0 im2col walk, 1 virtual-grid rows); each compiles
 // to its own kernel so the producer and MMA loops carry no run-time mode tests.
 template <int BN, bool BF16, int MODE>
-__global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__ CUtensorMap amap,
+__global__ void __launch_bounds__(192, 2) conv_tc_kernel(const __grid_constant__ CUtensorMap amap,
                                                          const __grid_constant__ CUtensorMap bmap,
                                                          const TcParams prm) {
     using Cfg = TcConfig<BN>;
@@ -112,7 +116,7 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
         tma_prefetch_desc(&bmap);
     }
     if (warp == 1) {
-        tmem_alloc(smem_addr(tmem_slot), Cfg::kTmemCols);
+        tmem_alloc(smem_addr(tmem_slot), prm.n_acc * BN);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -220,7 +224,7 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
                 }
                 if (!ok) break;
                 umma_commit(accf_bar(acc));
-                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+                if (++acc == prm.n_acc) { acc = 0; acc_phase ^= 1; }
             }
             if (!ok && issued_any) {
                 int dummy = 0;
@@ -356,7 +360,7 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(acc));
-            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            if (++acc == prm.n_acc) { acc = 0; acc_phase ^= 1; }
         }
     }
 
@@ -365,7 +369,7 @@ __global__ void __launch_bounds__(192, 1) conv_tc_kernel(const __grid_constant__
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, Cfg::kTmemCols);
+        tmem_dealloc(tmem_base, prm.n_acc * BN);
     }
 }
 
@@ -438,9 +442,9 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
 
     CUtensorMap amap, bmap;
     // Ring layout.  Padded mode groups kpb neighbouring taps of one filter row
-    // per stage around one halo A tile (128 + kpb - 1 pixel rows): the copy
-    // engine delivers about the same bytes per SM per second whatever the
-    // copy, so reusing overlapping rows from shared memory feeds more MMAs.
+    // per stage around one halo A tile (128 + kpb - 1 pixel rows): each stage
+    // costs the producer and MMA threads a fixed run of waits, copies and a
+    // commit, so fewer stages with more MMAs each feed the tensor core better.
     const int n_cchunks = d.CP / kTcBlockK;
     const int b_chunk = d.BN * kTcBlockK * 2;
     const int tail = 32 * kTcBlockM * 2 + 256 + 1024;
@@ -448,18 +452,39 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     const bool grid_rows = amode != 0;
     // Last virtual row that is an output, plus one (grid modes).
     const int m_end = grid_rows ? (d.N - 1) * d.Hp * d.Wq + (d.Ho - 1) * d.Wq + d.Wo : 0;
-    int kpb = 1, a_rows = kTcBlockM;
-    if (halo) {
-        for (int c = d.Kw; c >= 2; --c) {
-            if (d.Kw % c) continue;
-            const int rows = (kTcBlockM + c - 1 + 7) / 8 * 8;
-            if ((kSmemLimit - tail) / (rows * 128 + c * b_chunk) >= 3) { kpb = c; a_rows = rows; break; }
+    // Ring plan for a shared-memory budget: halo width kpb (largest divisor of
+    // Kw leaving at least min_halo stages), stage size and depth.
+    auto plan = [&](int budget, int min_halo, int& kpb_o, int& rows_o, int& stages_o) {
+        kpb_o = 1; rows_o = kTcBlockM;
+        if (halo) {
+            for (int c = d.Kw; c >= 2; --c) {
+                if (d.Kw % c) continue;
+                const int rows = (kTcBlockM + c - 1 + 7) / 8 * 8;
+                if ((budget - tail) / (rows * 128 + c * b_chunk) >= min_halo) { kpb_o = c; rows_o = rows; break; }
+            }
         }
+        stages_o = (budget - tail) / (rows_o * 128 + kpb_o * b_chunk);
+        if (stages_o > kMaxStages) stages_o = kMaxStages;
+    };
+    // Two CTAs per SM where both fit in half the SM's shared memory (TMEM: two
+    // BN-column accumulators each, or one for 256-wide tiles): a CTA's TMA
+    // producer and MMA issuer are single threads whose per-instruction
+    // latency, not the copy engine or the tensor core, bounds narrow tiles,
+    // and a second CTA doubles the issue rate (measured on GB300: about 81
+    // cycles per tcgen05.mma in one thread, while a 128x64x16 MMA executes in
+    // 32; 100-140 cycles per TMA copy, wait or commit).  Each CTA keeps at
+    // least 3 stages, or 2 when a stage holds several taps' MMAs (halo) or
+    // 256-wide ones.
+    int kpb, a_rows, stages, ctas_per_sm = 1, n_acc = 2;
+    plan(kSmemPerSm / 2 - 1024, 2, kpb, a_rows, stages);
+    if (stages >= (kpb > 1 || d.BN == 256 ? 2 : 3)) {
+        ctas_per_sm = 2;
+        if (d.BN == 256) n_acc = 1;
+    } else {
+        plan(kSmemLimit, 3, kpb, a_rows, stages);
     }
-    const int stage_bytes = a_rows * 128 + kpb * b_chunk;
-    int stages = (kSmemLimit - tail) / stage_bytes;
-    if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return CONV2D_ERR_UNSUPPORTED;
+    const int stage_bytes = a_rows * 128 + kpb * b_chunk;
 
     CUresult r;
     if (im2win) {
@@ -537,12 +562,13 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     prm.a_bytes = a_rows * 128;
     prm.halo = halo ? 1 : 0;
     prm.n_sp = halo ? d.Kh * (d.Kw / kpb) * n_cchunks : d.taps * n_cchunks;
+    prm.n_acc = n_acc;
     prm.y = y;
     if (grid_rows)
         prm.vec_store = ((d.Wo % 4) == 0 && (d.Wq % 4) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) ? 1 : 0;
     else
         prm.vec_store = ((prm.HoWo % 8) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) ? 1 : 0;
-    int grid = device_sm_count();
+    int grid = device_sm_count() * ctas_per_sm;
     if (grid > prm.n_tiles) grid = prm.n_tiles;
 
     const bool bf = d.dtype == CONV2D_BF16;
