@@ -127,52 +127,79 @@ cudaError_t launch_nchw_to_nhwc16(const void* x, void* out, int N, int C, int H,
 // ---------------------------------------------------------------- 16-bit NCHW -> zero-padded NHWC
 // out[n][yy][xx][c] = X[n][c][yy-p][xx-p] (zero outside the image and for
 // c >= C), yy in [0, Hp), xx in [0, Wq): every output pixel of the padded
-// grid is written, borders included.  A block covers 64 padded pixels x 64
-// channels: reads run along image rows, writes are 16-byte channel vectors.
+// grid is written, borders included.  A block covers one padded row, 64
+// channels and kRowTileX output columns.  It reads the 64 channel rows of the
+// image row as 16-byte vectors (8 pixels; when W % 8 == 0) and scatters them
+// into a pixel-major shared tile [pixel][64 channels], then writes each
+// pixel's channels as 16-byte vectors, consecutive threads on consecutive
+// vectors.  The tile's 16-byte channel chunks are XOR-swizzled by the pixel's
+// 8-pixel group so that both phases run free of bank conflicts.
+constexpr int kRowTileX = 128;
+constexpr int kRowTileRows = kRowTileX + 8;   // staged pixels: the tile plus the 8-alignment slack
+
+__device__ __forceinline__ int row_tile_index(int x, int c) {
+    return x * 64 + ((((c >> 3) ^ (x >> 3)) & 7) << 3) + (c & 7);
+}
+
 __global__ void __launch_bounds__(256) nchw_to_padded_nhwc16_kernel(const uint16_t* __restrict__ x,
                                                                     uint4* __restrict__ out, int C, int C8, int H,
-                                                                    int W, int Hp, int Wq, int p) {
-    __shared__ uint32_t tile[kNhwcTile * kNhwcPitch / 2];
-    uint16_t* t16 = reinterpret_cast<uint16_t*>(tile);
+                                                                    int W, int Hp, int Wq, int p, int n_xt,
+                                                                    int vec_ok) {
+    __shared__ __align__(16) uint16_t tile[kRowTileRows * 64];
     pdl_launch_dependents();
-    const int P = Hp * Wq;
-    const int p0 = blockIdx.x * kNhwcTile, c0 = blockIdx.y * kNhwcTile;
+    const int xt = blockIdx.x % n_xt, yy = blockIdx.x / n_xt;
+    const int c0 = blockIdx.y * 64;
     const long long n = blockIdx.z;
-    const int pl = threadIdx.x & 63;
-    const int q = p0 + pl;
-    const int yy = q / Wq, xx = q - yy * Wq;
-    const int y = yy - p, xw = xx - p;
-    const bool in = q < P && y >= 0 && y < H && xw >= 0 && xw < W;
-    const uint16_t* src = x + n * (long long)C * H * W + (in ? y * W + xw : 0);
-#pragma unroll 4
-    for (int i = 0; i < 16; ++i) {
-        const int c = (threadIdx.x >> 6) + 4 * i;
-        const int cc = c0 + c;
-        t16[c * kNhwcPitch + pl] = (in && cc < C) ? src[(long long)cc * H * W] : (uint16_t)0;
+    const int xq0 = xt * kRowTileX;                          // first output column of the tile
+    const int xq_n = min(kRowTileX, Wq - xq0);
+    const int cg_n = min(64, C8 - c0) / 8;                   // channel vectors per pixel in this block
+    const int y = yy - p;
+    const bool row_in = y >= 0 && y < H;
+    // Image columns [xa, xhi) cover the tile's interior pixels; xa is xlo
+    // rounded down to 8 so that vector loads stay 16-byte aligned.
+    const int xlo = max(xq0 - p, 0), xhi = min(xq0 + xq_n - p, W);
+    const int xa = xlo & ~7;
+    if (row_in && xhi > xlo) {
+        const uint16_t* src = x + ((n * C + c0) * H + y) * (long long)W + xa;
+        if (vec_ok) {
+            const int nv = (xhi - xa + 7) >> 3;              // W % 8 == 0: never past the row end
+            for (int i = threadIdx.x; i < 64 * nv; i += blockDim.x) {
+                const int c = i / nv, v = i - c * nv;
+                uint4 val = make_uint4(0, 0, 0, 0);
+                if (c0 + c < C) val = __ldg(reinterpret_cast<const uint4*>(src + (long long)c * H * W) + v);
+                const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    tile[row_tile_index(8 * v + k, c)] = (uint16_t)(w[k >> 1] >> (16 * (k & 1)));
+            }
+        } else {
+            const int span = xhi - xa;
+            for (int i = threadIdx.x; i < 64 * span; i += blockDim.x) {
+                const int c = i / span, v = i - c * span;
+                tile[row_tile_index(v, c)] = (c0 + c < C && xa + v >= xlo) ? src[(long long)c * H * W + v] : 0;
+            }
+        }
     }
     __syncthreads();
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int pl2 = threadIdx.x / 8 + 32 * i, cg = threadIdx.x % 8;
-        const int pp = p0 + pl2, cc = c0 + cg * 8;
-        if (pp < P && cc < C8) {
-            uint32_t w[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                w[j] = (uint32_t)t16[(cg * 8 + 2 * j) * kNhwcPitch + pl2] |
-                       ((uint32_t)t16[(cg * 8 + 2 * j + 1) * kNhwcPitch + pl2] << 16);
-            out[((n * P + pp) * C8 + cc) >> 3] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
+    uint4* dst = out + (((n * Hp + yy) * Wq + xq0) * C8 + c0) / 8;
+    for (int i = threadIdx.x; i < xq_n * cg_n; i += blockDim.x) {
+        const int xl = i / cg_n, g = i - xl * cg_n;
+        const int xw = xq0 + xl - p;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (row_in && xw >= 0 && xw < W) v = *reinterpret_cast<const uint4*>(tile + row_tile_index(xw - xa, 8 * g));
+        dst[(long long)xl * (C8 / 8) + g] = v;
     }
     pdl_wait();   // complete only after the filter repack launched before us
 }
 
 cudaError_t launch_nchw_to_padded_nhwc16(const void* x, void* out, const conv2d_desc& d, cudaStream_t st) {
-    const int P = d.Hp * d.Wq;
-    dim3 grid((P + kNhwcTile - 1) / kNhwcTile, (d.Ci8 + kNhwcTile - 1) / kNhwcTile, d.N);
-    if (grid.z > 65535 || grid.y > 65535) return cudaErrorInvalidConfiguration;
+    const int n_xt = (d.Wq + kRowTileX - 1) / kRowTileX;
+    const long long gx = (long long)n_xt * d.Hp;
+    const int vec_ok = (d.W % 8 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) ? 1 : 0;
+    dim3 grid((unsigned)gx, (d.Ci8 + 63) / 64, d.N);
+    if (gx > 0x7fffffffLL || grid.z > 65535 || grid.y > 65535) return cudaErrorInvalidConfiguration;
     return launch_after(nchw_to_padded_nhwc16_kernel, grid, dim3(256), 0, st, static_cast<const uint16_t*>(x),
-                        static_cast<uint4*>(out), d.Ci, d.Ci8, d.H, d.W, d.Hp, d.Wq, d.p);
+                        static_cast<uint4*>(out), d.Ci, d.Ci8, d.H, d.W, d.Hp, d.Wq, d.p, n_xt, vec_ok);
 }
 
 // ---------------------------------------------------------------- 16-bit channels-innermost window
