@@ -32,7 +32,7 @@
 //   warp 0     TMA producer (one elected lane), STAGES-deep shared-memory ring
 //   warp 1     TMEM allocation + MMA issue (one lane): 4 x (128xBNx16) per stage
 //   warps 2-5  epilogue: tcgen05.ld of their 32-lane TMEM quarter, round to the
-//              output type, store NCHW (32 consecutive pixels per store)
+//              output type, transpose through shared memory, store NCHW
 // Two TMEM accumulators let the epilogue of tile i overlap the MMAs of i+1
 // (with 256-wide tiles and two CTAs per SM, one each: the other CTA's MMAs
 // fill the gap).
@@ -49,74 +49,93 @@ namespace conv2d_gb300 {
 
 struct TcParams {
     int M, HoWo, Ho, Wo, Co;
-    int n_n_tiles, n_tiles;
-    int n_cchunks, n_kchunks, CP, Kw, s, p;
+    int n_n_tiles;      // output-channel tiles (BN wide)
+    int group;          // tiles per group (1 or kIssuers): consecutive 128-pixel tiles of one channel tile
+    int n_groups;       // tile groups
+    int n_m_tiles;      // 128-pixel tiles (groups past the end are padded with empty tiles)
+    int n_cchunks, CP, Kw, s, p;
     int amode;          // A source: 0 implicit, 1 im2win, 2 padded (1 and 2 run kernel MODE 1)
     int N, Wq, HpWq;    // grid modes: batch, row pitch and image pitch of the virtual pixel grid
     int vec_store;      // MODE 0: Ho*Wo % 8 == 0 (16-byte stores); MODE 1: Wo % 4 == 0 (8-byte stores)
-    int kpb;            // MMA chunks per pipeline stage (one A copy + one B copy per stage)
+    int kpb;            // taps per pipeline stage (halo mode), else 1
     int stages;         // depth of the shared-memory ring (<= kMaxStages)
-    int stage_bytes;    // A region + kpb B chunks
-    int a_bytes;        // A region of a stage: one 128-row chunk, or a halo of 128 + kpb - 1 rows
-    int halo;           // padded mode: a stage holds kpb neighbouring taps kw0..kw0+kpb-1 of one
-                        // filter row, all read from one halo A tile at row offsets 0..kpb-1
-    int n_sp;           // pipeline stages per output tile
-    int n_acc;          // TMEM accumulators (BN columns each): 2 lets the epilogue of one tile
-                        // overlap the MMAs of the next; 1 when two CTAs share an SM's TMEM
+    int stage_bytes;    // `group` A regions (+ the stage's B chunks unless B is resident)
+    int a_bytes;        // one A region: a 128-row chunk, or a halo of 128 + kpb - 1 rows
+    int n_sp;           // pipeline stages per tile group
+    int n_acc;          // TMEM accumulators per issuer (BN columns each)
+    int taps;           // filter taps of the repacked filter
+    int b_res;          // 1: the whole filter slice of the (single) channel tile stays in shared memory
+    int b_res_off;      // byte offsets in the aligned dynamic shared memory
+    int epi_off;
     void* y;
 };
 
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448;                               // 227 KB per block
-constexpr int kSmemPerSm = 233472;                               // 228 KB per SM, 1 KB of it reserved per block
+constexpr int kIssuers = 2;                                      // MMA-issuing threads (one tile each)
+constexpr int kEpiWarpBytes = 32 * 32 * 2;                       // epilogue staging per warp: 32 ch x 32 px
+constexpr int kEpiBytes = 2 * 4 * kEpiWarpBytes;                 // two epilogue groups of four warps
+constexpr int kBarBytes = 512;
+constexpr int kTcThreads = 32 * (1 + kIssuers + 8);              // producer, issuers, 8 epilogue warps
 
 template <int BN>
 struct TcConfig {
-    static constexpr int kABytes = kTcBlockM * kTcBlockK * 2;   // one 128 x 64 A chunk: 16 KB
     static constexpr int kBBytes = BN * kTcBlockK * 2;          // one BN x 64 B chunk
-    static constexpr int kChunkBytes = kABytes + kBBytes;
-    static constexpr int kEpiBytes = 32 * kTcBlockM * 2;        // epilogue staging: 32 channels x 128 pixels
-    static constexpr int kTailBytes = kEpiBytes + 256 + 1024;   // staging + barriers + alignment slack
 };
-// Shared memory layout for a ring of `stages` stages of `stage_bytes`:
-//   [stage 0 .. stage S-1][epilogue staging][barriers]; a stage is
-//   [kpb A chunks][kpb B chunks], each chunk 1024-byte aligned (128-byte swizzle).
+// Dynamic shared memory (1024-byte aligned): [stage 0 .. stage S-1][resident
+// filter][epilogue staging][barriers].  A stage is [A region of issuer 0]
+// [A region of issuer 1][kpb B chunks, unless the filter is resident]; every
+// region is a multiple of 1024 bytes (128-byte swizzle atoms).
 
 // MODE is the A addressing (0 im2col walk, 1 virtual-grid rows); each compiles
 // to its own kernel so the producer and MMA loops carry no run-time mode tests.
+//
+// Tiles are taken in groups of kIssuers consecutive 128-pixel tiles of one
+// channel tile (single tiles when there are fewer than two tiles per SM).  A stage holds the A chunks of every tile in the group and
+// one B chunk they share, so B is read once per group; issuer i runs the MMAs
+// of tile i of the group into its own TMEM accumulators.  One thread issuing
+// tcgen05.mma takes about 81 cycles per instruction (measured on GB300), while
+// a 128x64x16 MMA executes in 32: two issuers keep narrow tiles fed.  When the
+// whole filter slice fits (one channel tile), it is loaded once per CTA and
+// stays resident, and stages carry A only.
 template <int BN, bool BF16, int MODE>
-__global__ void __launch_bounds__(192, 2) conv_tc_kernel(const __grid_constant__ CUtensorMap amap,
-                                                         const __grid_constant__ CUtensorMap bmap,
-                                                         const TcParams prm) {
+__global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_constant__ CUtensorMap amap,
+                                                                const __grid_constant__ CUtensorMap bmap,
+                                                                const TcParams prm) {
     using Cfg = TcConfig<BN>;
     const int S = prm.stages;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzled operand tiles need 1024-byte alignment.
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int epi_off = S * prm.stage_bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + epi_off + Cfg::kEpiBytes);
-    // bars[0..S) full, [S..2S) empty, [2S..2S+2) accumulator full, [2S+2..2S+4) accumulator empty, [2S+4] drain
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + prm.epi_off + kEpiBytes);
+    // bars: [0, S) full, [S, 2S) empty, then per issuer i: accf[i][0..n_acc),
+    // acce[i][0..n_acc), then the resident-filter barrier and kIssuers drain barriers.
+    const int nacc = prm.n_acc;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4 * kIssuers + 1 + kIssuers);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto full_bar = [&](int i) { return smem_addr(&bars[i]); };
     auto empty_bar = [&](int i) { return smem_addr(&bars[S + i]); };
-    auto accf_bar = [&](int i) { return smem_addr(&bars[2 * S + i]); };
-    auto acce_bar = [&](int i) { return smem_addr(&bars[2 * S + 2 + i]); };
-    const uint32_t drain_bar = smem_addr(&bars[2 * S + 4]);
+    auto accf_bar = [&](int is, int a) { return smem_addr(&bars[2 * S + is * 2 * nacc + a]); };
+    auto acce_bar = [&](int is, int a) { return smem_addr(&bars[2 * S + is * 2 * nacc + nacc + a]); };
+    const uint32_t bres_bar = smem_addr(&bars[2 * S + 2 * kIssuers * nacc]);
+    auto drain_bar = [&](int is) { return smem_addr(&bars[2 * S + 2 * kIssuers * nacc + 1 + is]); };
+    const uint32_t tmem_cols = kIssuers * nacc * BN;
 
     if (warp == 0 && lane == 0) {
-        for (int i = 0; i < S; ++i) { mbar_init(full_bar(i), 1); mbar_init(empty_bar(i), 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(accf_bar(i), 1); mbar_init(acce_bar(i), 4); }
-        mbar_init(drain_bar, 1);
+        for (int i = 0; i < S; ++i) { mbar_init(full_bar(i), 1); mbar_init(empty_bar(i), prm.group); }
+        for (int is = 0; is < kIssuers; ++is)
+            for (int a = 0; a < nacc; ++a) { mbar_init(accf_bar(is, a), 1); mbar_init(acce_bar(is, a), 4); }
+        mbar_init(bres_bar, 1);
+        for (int is = 0; is < kIssuers; ++is) mbar_init(drain_bar(is), 1);
         *abort_flag = 0;
         mbar_fence_init();
         tma_prefetch_desc(&amap);
         tma_prefetch_desc(&bmap);
     }
     if (warp == 1) {
-        tmem_alloc(smem_addr(tmem_slot), prm.n_acc * BN);
+        tmem_alloc(smem_addr(tmem_slot), tmem_cols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -127,58 +146,89 @@ __global__ void __launch_bounds__(192, 2) conv_tc_kernel(const __grid_constant__
     // launched just before this one; the set-up above overlapped their tail.
     pdl_wait();
 
+    const int kpb = MODE == 1 ? prm.kpb : 1;
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
+            bool ok = true;
+            if (prm.b_res) {
+                // The filter slice of channel tile 0: chunk (cb, t) at ((cb*taps + t) * kBBytes).
+                const uint32_t bdst = smem_addr(smem + prm.b_res_off);
+                mbar_arrive_expect_tx(bres_bar, (uint32_t)(prm.n_cchunks * prm.taps * Cfg::kBBytes));
+                for (int cb = 0; cb < prm.n_cchunks; ++cb)
+                    for (int t = 0; t < prm.taps; t += kpb) {
+                        const uint32_t dst = bdst + (uint32_t)((cb * prm.taps + t) * Cfg::kBBytes);
+                        if constexpr (MODE == 1) tma_load_3d(dst, &bmap, bres_bar, cb * kTcBlockK, 0, t);
+                        else                     tma_load_2d(dst, &bmap, bres_bar, t * prm.CP + cb * kTcBlockK, 0);
+                    }
+            }
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; tile < prm.n_tiles && ok; tile += gridDim.x) {
-                const int m0 = (tile / prm.n_n_tiles) * kTcBlockM;
-                const int n0 = (tile % prm.n_n_tiles) * BN;
-                int img = 0, ho = 0, wo = 0;
-                if constexpr (MODE == 0) {
-                    img = m0 / prm.HoWo;
-                    const int r = m0 - img * prm.HoWo;
-                    ho = r / prm.Wo;
-                    wo = r - ho * prm.Wo;
+            bool free_now = false;
+            for (int g = blockIdx.x; g < prm.n_groups && ok; g += gridDim.x) {
+                const int n0 = (g % prm.n_n_tiles) * BN;
+                const int mt0 = (g / prm.n_n_tiles) * prm.group;
+                int m0[kIssuers], img[kIssuers], ho[kIssuers], wo[kIssuers];
+                bool val[kIssuers];
+                int n_val = 0;
+#pragma unroll
+                for (int i = 0; i < kIssuers; ++i) {
+                    m0[i] = (mt0 + i) * kTcBlockM;
+                    val[i] = i < prm.group && mt0 + i < prm.n_m_tiles;
+                    n_val += val[i] ? 1 : 0;
+                    img[i] = ho[i] = wo[i] = 0;
+                    if constexpr (MODE == 0) {
+                        if (val[i]) {
+                            img[i] = m0[i] / prm.HoWo;
+                            const int r = m0[i] - img[i] * prm.HoWo;
+                            ho[i] = r / prm.Wo;
+                            wo[i] = r - ho[i] * prm.Wo;
+                        }
+                    }
                 }
+                const uint32_t tx = (uint32_t)(n_val * prm.a_bytes + (prm.b_res ? 0 : kpb * Cfg::kBBytes));
+                // Stage coordinates advance incrementally (no divisions in the loop):
+                // channel block cb, first tap t = kh*Kw + kw of the stage's kpb taps.
+                int cb = 0, t = 0, kw = 0, kh = 0;
                 for (int sp = 0; sp < prm.n_sp; ++sp) {
-                    // Stage sp covers taps t..t+kpb-1 (halo) or chunk sp, channel block cb.
-                    int t, cb;
-                    if constexpr (MODE == 1) {
-                        cb = sp % prm.n_cchunks;
-                        const int rest = sp / prm.n_cchunks, ngw = prm.Kw / prm.kpb;
-                        t = (rest / ngw) * prm.Kw + (rest % ngw) * prm.kpb;
-                    } else {
-                        t = sp / prm.n_cchunks;
-                        cb = sp - t * prm.n_cchunks;
-                    }
+                    if (!free_now && !mbar_wait(empty_bar(stage), phase ^ 1, abort_flag)) { ok = false; break; }
+                    // Probe the next slot now; the answer is used one stage later, so
+                    // the probe's latency hides behind this stage's copies.
+                    const int nstage = stage + 1 == S ? 0 : stage + 1;
+                    const uint32_t nphase = stage + 1 == S ? phase ^ 1 : phase;
+                    const bool free_next = mbar_test_wait(empty_bar(nstage), nphase ^ 1);
                     const int c0 = cb * kTcBlockK;
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(full_bar(stage), prm.stage_bytes);
+                    mbar_arrive_expect_tx(full_bar(stage), tx);
                     const uint32_t a_dst = smem_addr(smem + stage * prm.stage_bytes);
-                    const uint32_t b_dst = a_dst + prm.a_bytes;
-                    if constexpr (MODE == 1) {
-                        // Virtual pixel q reads padded pixel q + kh*Wq + kw.  In halo mode
-                        // the box has 128 + kpb - 1 rows: taps kw..kw+kpb-1 are the same
-                        // rows shifted by one pixel each, so they share one copy.  (im2win:
-                        // one tap, t = 0.)
-                        const int kh = t / prm.Kw, kw = t - kh * prm.Kw;
-                        tma_load_2d(a_dst, &amap, full_bar(stage), c0, m0 + kh * prm.Wq + kw);
-                    } else {
-                        const int kh = t / prm.Kw, kw = t - kh * prm.Kw;
-                        tma_load_im2col_4d(a_dst, &amap, full_bar(stage), c0, wo * prm.s - prm.p,
-                                           ho * prm.s - prm.p, img, (uint16_t)kw, (uint16_t)kh);
+#pragma unroll
+                    for (int i = 0; i < kIssuers; ++i) {
+                        if (!val[i]) continue;     // empty tile of a short last group: no copy
+                        const uint32_t dst = a_dst + (uint32_t)(i * prm.a_bytes);
+                        if constexpr (MODE == 1) {
+                            // Virtual pixel q reads padded pixel q + kh*Wq + kw.  In halo
+                            // mode the box has 128 + kpb - 1 rows: taps kw..kw+kpb-1 are the
+                            // same rows shifted by one pixel each, so they share one copy.
+                            // (im2win: one tap, t = 0.)
+                            tma_load_2d(dst, &amap, full_bar(stage), c0, m0[i] + kh * prm.Wq + kw);
+                        } else {
+                            tma_load_im2col_4d(dst, &amap, full_bar(stage), c0, wo[i] * prm.s - prm.p,
+                                               ho[i] * prm.s - prm.p, img[i], (uint16_t)kw, (uint16_t)kh);
+                        }
                     }
-                    // Filter chunks of taps t..t+kpb-1, channel block cb: one copy (a 3-D
-                    // box in halo mode; higher-rank maps cost the copy engine more, so
-                    // the other modes keep a 2-D map).
-                    if constexpr (MODE == 1) tma_load_3d(b_dst, &bmap, full_bar(stage), c0, n0, t);
-                    else                     tma_load_2d(b_dst, &bmap, full_bar(stage), t * prm.CP + c0, n0);
+                    if (!prm.b_res) {
+                        // Filter chunks of taps t..t+kpb-1, channel block cb: one copy (a 3-D
+                        // box in the grid modes; the implicit mode keeps a 2-D map).
+                        const uint32_t b_dst = a_dst + (uint32_t)(prm.group * prm.a_bytes);
+                        if constexpr (MODE == 1) tma_load_3d(b_dst, &bmap, full_bar(stage), c0, n0, t);
+                        else                     tma_load_2d(b_dst, &bmap, full_bar(stage), t * prm.CP + c0, n0);
+                    }
                     ++issued;
-                    if (++stage == S) { stage = 0; phase ^= 1; }
+                    stage = nstage; phase = nphase; free_now = free_next;
+                    if (++cb == prm.n_cchunks) {
+                        cb = 0; t += kpb; kw += kpb;
+                        if (kw == prm.Kw) { kw = 0; ++kh; }
+                    }
                 }
             }
             if (!ok) {
@@ -191,176 +241,170 @@ __global__ void __launch_bounds__(192, 2) conv_tc_kernel(const __grid_constant__
                     mbar_wait(full_bar(st), ph, &dummy);
                 }
             }
+            if (prm.b_res) {
+                int dummy = 0;
+                mbar_wait(bres_bar, 0, &dummy);
+            }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+    } else if (warp <= kIssuers) {
+        // ------------------------------------------------------------ MMA issuers
+        const int is = warp - 1;
+        if (lane == 0 && is < prm.group) {
             constexpr uint32_t idesc = umma_idesc_f16(BF16, kTcBlockM, BN);
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
-            bool ok = true, issued_any = false;
-            for (int tile = blockIdx.x; tile < prm.n_tiles && ok; tile += gridDim.x) {
-                if (!mbar_wait(acce_bar(acc), acc_phase ^ 1, abort_flag)) { ok = false; break; }
+            bool ok = true, issued_any = false, ready_now = false;
+            if (prm.b_res && !mbar_wait(bres_bar, 0, abort_flag)) ok = false;
+            const uint32_t bres_base = smem_addr(smem + prm.b_res_off);
+            for (int g = blockIdx.x; g < prm.n_groups && ok; g += gridDim.x) {
+                if (!mbar_wait(acce_bar(is, acc), acc_phase ^ 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * BN;
+                const uint32_t d_tmem = tmem_base + (uint32_t)((is * nacc + acc) * BN);
+                int cb = 0, t = 0;
                 for (int sp = 0; sp < prm.n_sp; ++sp) {
-                    if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
+                    if (!ready_now && !mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
+                    // Probe the next slot before issuing this stage's MMAs (its answer
+                    // is used one stage later).
+                    const int nstage = stage + 1 == S ? 0 : stage + 1;
+                    const uint32_t nphase = stage + 1 == S ? phase ^ 1 : phase;
+                    const bool ready_next = mbar_test_wait(full_bar(nstage), nphase);
                     tc_fence_after();
-                    const uint32_t a_base = smem_addr(smem + stage * prm.stage_bytes);
-                    const uint32_t b_base = a_base + prm.a_bytes;
-                    const int kpb = MODE == 1 ? prm.kpb : 1;
+                    const uint32_t st_base = smem_addr(smem + stage * prm.stage_bytes);
+                    const uint64_t a_desc = sw128_kmajor_desc(st_base + (uint32_t)(is * prm.a_bytes));
+                    const uint64_t b_desc = sw128_kmajor_desc(
+                        prm.b_res ? bres_base + (uint32_t)((cb * prm.taps + t) * Cfg::kBBytes)
+                                  : st_base + (uint32_t)(prm.group * prm.a_bytes));
                     for (int i = 0; i < kpb; ++i) {
                         // Halo: tap kw0+i reads the A tile from row i (128 bytes per row).
-                        const uint32_t a_sub = a_base + i * 128u, b_sub = b_base + i * Cfg::kBBytes;
+                        // Descriptor start addresses are in 16-byte units.
 #pragma unroll
                         for (int k = 0; k < kTcBlockK / 16; ++k) {
-                            umma_f16(d_tmem, sw128_kmajor_desc(a_sub + 32 * k), sw128_kmajor_desc(b_sub + 32 * k),
-                                     idesc, (sp > 0 || i > 0 || k > 0) ? 1u : 0u);
+                            umma_f16(d_tmem, a_desc + (uint64_t)(i * 8 + 2 * k),
+                                     b_desc + (uint64_t)(i * (Cfg::kBBytes >> 4) + 2 * k), idesc,
+                                     (sp > 0 || i > 0 || k > 0) ? 1u : 0u);
                         }
                     }
                     issued_any = true;
                     umma_commit(empty_bar(stage));
-                    if (++stage == S) { stage = 0; phase ^= 1; }
+                    stage = nstage; phase = nphase; ready_now = ready_next;
+                    if (++cb == prm.n_cchunks) { cb = 0; t += kpb; }
                 }
                 if (!ok) break;
-                umma_commit(accf_bar(acc));
-                if (++acc == prm.n_acc) { acc = 0; acc_phase ^= 1; }
+                umma_commit(accf_bar(is, acc));
+                if (++acc == nacc) { acc = 0; acc_phase ^= 1; }
             }
             if (!ok && issued_any) {
                 int dummy = 0;
-                umma_commit(drain_bar);
-                mbar_wait(drain_bar, 0, &dummy);
+                umma_commit(drain_bar(is));
+                mbar_wait(drain_bar(is), 0, &dummy);
             }
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        // Each 32-column chunk of the accumulator (32 output channels x 128
-        // pixels) is rounded, staged in shared memory as [channel][pixel] and
-        // written as whole 256-byte channel rows with 16-byte stores.  The
-        // four epilogue warps synchronise on named barrier 1; the per-tile
-        // barrier also ANDs the wait results so all four leave together.
-        const int quarter = warp & 3;
-        const int et = threadIdx.x - 64;                 // 0..127
-        uint16_t* stage_out = reinterpret_cast<uint16_t*>(smem + epi_off);
+        // Two groups of four warps; group e drains the accumulators of issuer
+        // e.  Warp q of a group owns TMEM lanes 32q..32q+31, i.e. pixels
+        // 32q..32q+31 of the tile, and works on its own: each 32-column chunk
+        // (32 channels x its 32 pixels) is rounded, transposed through the
+        // warp's 2 KB of shared memory as [channel][pixel] and written as
+        // 64-byte runs of one channel (16-byte stores; 8-byte stores over the
+        // virtual grid, where a 4-pixel group is all-valid or all-junk when
+        // Wo % 4 == 0).  Two chunks are loaded from TMEM per wait.  The
+        // per-tile barrier only ANDs the wait results so that a group's four
+        // warps leave together.
+        const int ew = warp - 1 - kIssuers;             // 0..7
+        const int eg = ew >> 2;                         // epilogue group = issuer
+        const int quarter = warp & 3;                   // TMEM lane quarter this warp may access
+        uint16_t* wst = reinterpret_cast<uint16_t*>(smem + prm.epi_off + ew * kEpiWarpBytes);
+        uint16_t* const yout = static_cast<uint16_t*>(prm.y);
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < prm.n_tiles; tile += gridDim.x) {
-            const bool got = mbar_wait(accf_bar(acc), acc_phase, abort_flag);
-            if (!named_bar_and(1, 128, got)) break;
+        for (int g = blockIdx.x; g < prm.n_groups && eg < prm.group; g += gridDim.x) {
+            const bool got = mbar_wait(accf_bar(eg, acc), acc_phase, abort_flag);
+            if (!named_bar_and(1 + eg, 128, got)) break;
             tc_fence_after();
-            const int m0 = (tile / prm.n_n_tiles) * kTcBlockM;
-            const int n0 = (tile % prm.n_n_tiles) * BN;
-            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+            const int n0 = (g % prm.n_n_tiles) * BN;
+            const int m0 = ((g / prm.n_n_tiles) * prm.group + eg) * kTcBlockM;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   (uint32_t)((eg * nacc + acc) * BN);
+            const int mw = m0 + quarter * 32;
+            // Store geometry: this lane's piece of the warp's 32 pixels (vector
+            // paths) or its own pixel (scalar path).
+            bool v_ok, p_ok;
+            uint16_t *vbase, *pbase;
+            int vpc, vrow0;
             if constexpr (MODE == 1) {
-                // Rows are virtual pixels of the grid [N][Hv][Wq]; only
-                // those with y < Ho and x < Wo are outputs.  With Wo % 4 == 0 a
-                // 4-pixel group is all-valid or all-junk: 8-byte stores.
-                const int g = et & 31;
-                const int qg = m0 + 4 * g;
+                vpc = lane & 7; vrow0 = lane >> 3;
+                const int qg = mw + 4 * vpc;
                 const int ng = qg / prm.HpWq, rg = qg - ng * prm.HpWq;
                 const int yg = rg / prm.Wq, xg = rg - yg * prm.Wq;
-                const bool g_ok = ng < prm.N && yg < prm.Ho && xg < prm.Wo;
-                uint16_t* gbase = static_cast<uint16_t*>(prm.y) + (long long)ng * prm.Co * prm.HoWo + yg * prm.Wo + xg;
-                const int qp = m0 + et;                      // scalar fallback: one pixel per thread
+                v_ok = ng < prm.N && yg < prm.Ho && xg < prm.Wo;
+                vbase = yout + (long long)ng * prm.Co * prm.HoWo + yg * prm.Wo + xg;
+                const int qp = mw + lane;
                 const int np = qp / prm.HpWq, rp = qp - np * prm.HpWq;
                 const int yp = rp / prm.Wq, xp = rp - yp * prm.Wq;
-                const bool p_ok = np < prm.N && yp < prm.Ho && xp < prm.Wo;
-                uint16_t* pbase = static_cast<uint16_t*>(prm.y) + (long long)np * prm.Co * prm.HoWo + yp * prm.Wo + xp;
-#pragma unroll 1
-                for (int cc = 0; cc < BN / 32; ++cc) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(t_row + cc * 32, v);
-                    tmem_ld_wait();
+                p_ok = np < prm.N && yp < prm.Ho && xp < prm.Wo;
+                pbase = yout + (long long)np * prm.Co * prm.HoWo + yp * prm.Wo + xp;
+            } else {
+                vpc = lane & 3; vrow0 = lane >> 2;
+                const int mg = mw + 8 * vpc;
+                v_ok = mg < prm.M;
+                const int img = v_ok ? mg / prm.HoWo : 0;
+                const int r = v_ok ? mg - img * prm.HoWo : 0;
+                vbase = yout + ((long long)img * prm.Co) * prm.HoWo + r;
+                const int m = mw + lane;
+                p_ok = m < prm.M;
+                const int imgp = p_ok ? m / prm.HoWo : 0;
+                const int rp = p_ok ? m - imgp * prm.HoWo : 0;
+                pbase = yout + ((long long)imgp * prm.Co) * prm.HoWo + rp;
+            }
+            auto cvt = [](uint32_t u) -> uint16_t {
+                const float f = __uint_as_float(u);
+                if (BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+                return __half_as_ushort(__float2half_rn(f));
+            };
+            auto emit = [&](const uint32_t (&v)[32], int cc) {
+                const int cob = n0 + cc * 32;
+                if (prm.vec_store) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float f = __uint_as_float(v[j]);
-                        uint16_t h;
-                        if (BF16) h = __bfloat16_as_ushort(__float2bfloat16_rn(f));
-                        else      h = __half_as_ushort(__float2half_rn(f));
-                        stage_out[j * kTcBlockM + quarter * 32 + lane] = h;
-                    }
-                    named_bar_sync(1, 128);
-                    if (prm.vec_store) {
+                    for (int j = 0; j < 32; ++j) wst[j * 32 + lane] = cvt(v[j]);
+                    __syncwarp();
+                    if constexpr (MODE == 1) {
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
-                            const int row = (et >> 5) + 4 * i;
-                            const int co = n0 + cc * 32 + row;
-                            if (g_ok && co < prm.Co)
-                                *reinterpret_cast<uint2*>(gbase + (long long)co * prm.HoWo) =
-                                    *reinterpret_cast<const uint2*>(stage_out + row * kTcBlockM + 4 * g);
+                            const int row = vrow0 + 4 * i;
+                            if (v_ok && cob + row < prm.Co)
+                                *reinterpret_cast<uint2*>(vbase + (long long)(cob + row) * prm.HoWo) =
+                                    *reinterpret_cast<const uint2*>(wst + row * 32 + 4 * vpc);
                         }
-                    } else if (p_ok) {
-#pragma unroll 4
-                        for (int row = 0; row < 32; ++row) {
-                            const int co = n0 + cc * 32 + row;
-                            if (co < prm.Co) pbase[(long long)co * prm.HoWo] = stage_out[row * kTcBlockM + et];
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int row = vrow0 + 8 * i;
+                            if (v_ok && cob + row < prm.Co)
+                                *reinterpret_cast<uint4*>(vbase + (long long)(cob + row) * prm.HoWo) =
+                                    *reinterpret_cast<const uint4*>(wst + row * 32 + 8 * vpc);
                         }
                     }
-                    named_bar_sync(1, 128);
+                    __syncwarp();
+                } else if (p_ok) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (cob + j < prm.Co) pbase[(long long)(cob + j) * prm.HoWo] = cvt(v[j]);
                 }
-            } else if (prm.vec_store) {
-                const int grp = et & 15;                    // this thread's 8-pixel group
-                const int mg = m0 + 8 * grp;
-                const bool g_ok = mg < prm.M;
-                const int img = g_ok ? mg / prm.HoWo : 0;
-                const int r = g_ok ? mg - img * prm.HoWo : 0;
-                uint16_t* gbase = static_cast<uint16_t*>(prm.y) + ((long long)img * prm.Co) * prm.HoWo + r;
+            };
 #pragma unroll 1
-                for (int cc = 0; cc < BN / 32; ++cc) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(t_row + cc * 32, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float f = __uint_as_float(v[j]);
-                        uint16_t h;
-                        if (BF16) h = __bfloat16_as_ushort(__float2bfloat16_rn(f));
-                        else      h = __half_as_ushort(__float2half_rn(f));
-                        stage_out[j * kTcBlockM + quarter * 32 + lane] = h;
-                    }
-                    named_bar_sync(1, 128);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int row = (et >> 4) + 8 * i;
-                        const int co = n0 + cc * 32 + row;
-                        if (g_ok && co < prm.Co) {
-                            const uint4 val = *reinterpret_cast<const uint4*>(stage_out + row * kTcBlockM + 8 * grp);
-                            *reinterpret_cast<uint4*>(gbase + (long long)co * prm.HoWo) = val;
-                        }
-                    }
-                    named_bar_sync(1, 128);
-                }
-            } else {
-                const int m = m0 + quarter * 32 + lane;
-                const bool m_ok = m < prm.M;
-                const int img = m_ok ? m / prm.HoWo : 0;
-                const int r = m_ok ? m - img * prm.HoWo : 0;
-                uint16_t* out = static_cast<uint16_t*>(prm.y) + ((long long)img * prm.Co) * prm.HoWo + r;
-#pragma unroll 1
-                for (int cc = 0; cc < BN / 32; ++cc) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(t_row + cc * 32, v);
-                    tmem_ld_wait();
-                    const int cob = n0 + cc * 32;
-                    if (m_ok) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int co = cob + j;
-                            if (co < prm.Co) {
-                                const float f = __uint_as_float(v[j]);
-                                uint16_t h;
-                                if (BF16) h = __bfloat16_as_ushort(__float2bfloat16_rn(f));
-                                else      h = __half_as_ushort(__float2half_rn(f));
-                                out[(long long)co * prm.HoWo] = h;
-                            }
-                        }
-                    }
-                }
+            for (int cc = 0; cc < BN / 32; cc += 2) {
+                uint32_t v0[32], v1[32];
+                tmem_ld_32x32b_x32(t_row + cc * 32, v0);
+                tmem_ld_32x32b_x32(t_row + (cc + 1) * 32, v1);
+                tmem_ld_wait();
+                emit(v0, cc);
+                emit(v1, cc + 1);
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acce_bar(acc));
-            if (++acc == prm.n_acc) { acc = 0; acc_phase ^= 1; }
+            if (lane == 0) mbar_arrive(acce_bar(eg, acc));
+            if (++acc == nacc) { acc = 0; acc_phase ^= 1; }
         }
     }
 
@@ -369,7 +413,7 @@ __global__ void __launch_bounds__(192, 2) conv_tc_kernel(const __grid_constant__
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, prm.n_acc * BN);
+        tmem_dealloc(tmem_base, tmem_cols);
     }
 }
 
@@ -407,28 +451,28 @@ typedef CUresult (*PFN_encodeIm2col_t)(CUtensorMap*, CUtensorMapDataType, cuuint
 
 template <int BN, bool BF16, int MODE>
 static cudaError_t launch_tc_inst(const CUtensorMap& a, const CUtensorMap& b, const TcParams& prm, int grid,
-                                  cudaStream_t st) {
+                                  int smem, cudaStream_t st) {
     auto kern = conv_tc_kernel<BN, BF16, MODE>;
-    const int smem = prm.stages * prm.stage_bytes + TcConfig<BN>::kTailBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_after(kern, dim3(grid), dim3(192), smem, st, a, b, prm);
+    return launch_after(kern, dim3(grid), dim3(kTcThreads), smem, st, a, b, prm);
 }
 
 template <bool BF16, int MODE>
 static cudaError_t launch_tc_bn(int BN, const CUtensorMap& a, const CUtensorMap& b, const TcParams& prm, int grid,
-                                cudaStream_t st) {
+                                int smem, cudaStream_t st) {
     switch (BN) {
-        case 64:  return launch_tc_inst<64, BF16, MODE>(a, b, prm, grid, st);
-        case 128: return launch_tc_inst<128, BF16, MODE>(a, b, prm, grid, st);
-        default:  return launch_tc_inst<256, BF16, MODE>(a, b, prm, grid, st);
+        case 64:  return launch_tc_inst<64, BF16, MODE>(a, b, prm, grid, smem, st);
+        case 128: return launch_tc_inst<128, BF16, MODE>(a, b, prm, grid, smem, st);
+        default:  return launch_tc_inst<256, BF16, MODE>(a, b, prm, grid, smem, st);
     }
 }
 
 template <bool BF16>
 static cudaError_t launch_tc_mode(int BN, int amode, const CUtensorMap& a, const CUtensorMap& b, const TcParams& prm,
-                                  int grid, cudaStream_t st) {
-    return amode == 0 ? launch_tc_bn<BF16, 0>(BN, a, b, prm, grid, st) : launch_tc_bn<BF16, 1>(BN, a, b, prm, grid, st);
+                                  int grid, int smem, cudaStream_t st) {
+    return amode == 0 ? launch_tc_bn<BF16, 0>(BN, a, b, prm, grid, smem, st)
+                      : launch_tc_bn<BF16, 1>(BN, a, b, prm, grid, smem, st);
 }
 
 conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* wq, void* y, int amode,
@@ -441,50 +485,53 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
         d.dtype == CONV2D_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 
     CUtensorMap amap, bmap;
-    // Ring layout.  Padded mode groups kpb neighbouring taps of one filter row
-    // per stage around one halo A tile (128 + kpb - 1 pixel rows): each stage
+    // Ring layout.  A stage holds the A chunks of the tiles of a group and,
+    // unless the filter is resident, the B chunks they share.
+    // Padded mode puts kpb neighbouring taps of one filter row in a stage,
+    // around one halo A tile (128 + kpb - 1 pixel rows) per tile: each stage
     // costs the producer and MMA threads a fixed run of waits, copies and a
     // commit, so fewer stages with more MMAs each feed the tensor core better.
     const int n_cchunks = d.CP / kTcBlockK;
     const int b_chunk = d.BN * kTcBlockK * 2;
-    const int tail = 32 * kTcBlockM * 2 + 256 + 1024;
     const bool halo = amode == 2;
     const bool grid_rows = amode != 0;
+    const int n_n_tiles = (d.Co + d.BN - 1) / d.BN;
+    const int n_sm = device_sm_count();
     // Last virtual row that is an output, plus one (grid modes).
     const int m_end = grid_rows ? (d.N - 1) * d.Hp * d.Wq + (d.Ho - 1) * d.Wq + d.Wo : 0;
-    // Ring plan for a shared-memory budget: halo width kpb (largest divisor of
-    // Kw leaving at least min_halo stages), stage size and depth.
-    auto plan = [&](int budget, int min_halo, int& kpb_o, int& rows_o, int& stages_o) {
+    const int n_m_tiles = ((grid_rows ? m_end : d.N * d.Ho * d.Wo) + kTcBlockM - 1) / kTcBlockM;
+    // Pairs of tiles share B and keep two MMA issuers busy; with fewer than
+    // two tiles per SM, single tiles keep every SM busy instead.
+    const int group = (long long)n_m_tiles * n_n_tiles >= 2LL * n_sm ? kIssuers : 1;
+    const int budget = kSmemLimit - 1024 - kEpiBytes - kBarBytes;
+    // Ring plan for a budget: halo width kpb (largest divisor of Kw leaving at
+    // least 3 stages), stage size and depth.
+    auto plan = [&](int bud, bool bres, int& kpb_o, int& rows_o, int& stages_o) {
         kpb_o = 1; rows_o = kTcBlockM;
+        auto stage_of = [&](int rows, int c) { return group * rows * 128 + (bres ? 0 : c * b_chunk); };
         if (halo) {
             for (int c = d.Kw; c >= 2; --c) {
                 if (d.Kw % c) continue;
                 const int rows = (kTcBlockM + c - 1 + 7) / 8 * 8;
-                if ((budget - tail) / (rows * 128 + c * b_chunk) >= min_halo) { kpb_o = c; rows_o = rows; break; }
+                if (bud / stage_of(rows, c) >= 3) { kpb_o = c; rows_o = rows; break; }
             }
         }
-        stages_o = (budget - tail) / (rows_o * 128 + kpb_o * b_chunk);
+        stages_o = bud / stage_of(rows_o, kpb_o);
         if (stages_o > kMaxStages) stages_o = kMaxStages;
     };
-    // Two CTAs per SM where both fit in half the SM's shared memory (TMEM: two
-    // BN-column accumulators each, or one for 256-wide tiles): a CTA's TMA
-    // producer and MMA issuer are single threads whose per-instruction
-    // latency, not the copy engine or the tensor core, bounds narrow tiles,
-    // and a second CTA doubles the issue rate (measured on GB300: about 81
-    // cycles per tcgen05.mma in one thread, while a 128x64x16 MMA executes in
-    // 32; 100-140 cycles per TMA copy, wait or commit).  Each CTA keeps at
-    // least 3 stages, or 2 when a stage holds several taps' MMAs (halo) or
-    // 256-wide ones.
-    int kpb, a_rows, stages, ctas_per_sm = 1, n_acc = 2;
-    plan(kSmemPerSm / 2 - 1024, 2, kpb, a_rows, stages);
-    if (stages >= (kpb > 1 || d.BN == 256 ? 2 : 3)) {
-        ctas_per_sm = 2;
-        if (d.BN == 256) n_acc = 1;
-    } else {
-        plan(kSmemLimit, 3, kpb, a_rows, stages);
+    // The filter slice stays resident when there is one channel tile and the
+    // ring keeps at least 3 stages beside it.
+    const int bres_bytes = n_cchunks * d.taps * b_chunk;
+    int kpb = 1, a_rows = kTcBlockM, stages = 0;
+    bool b_res = false;
+    if (n_n_tiles == 1 && bres_bytes < budget) {
+        plan(budget - bres_bytes, true, kpb, a_rows, stages);
+        b_res = stages >= 3;
     }
+    if (!b_res) plan(budget, false, kpb, a_rows, stages);
     if (stages < 2) return CONV2D_ERR_UNSUPPORTED;
-    const int stage_bytes = a_rows * 128 + kpb * b_chunk;
+    const int stage_bytes = group * a_rows * 128 + (b_res ? 0 : kpb * b_chunk);
+    const int n_acc = 2 * kIssuers * d.BN <= 512 ? 2 : 1;
 
     CUresult r;
     if (im2win) {
@@ -549,31 +596,39 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     prm.Wq = d.Wq;
     prm.HpWq = d.Hp * d.Wq;
     prm.HoWo = d.Ho * d.Wo; prm.Ho = d.Ho; prm.Wo = d.Wo; prm.Co = d.Co;
-    prm.n_n_tiles = (d.Co + d.BN - 1) / d.BN;
-    const int n_m_tiles = (prm.M + kTcBlockM - 1) / kTcBlockM;
-    prm.n_tiles = n_m_tiles * prm.n_n_tiles;
-    prm.n_cchunks = d.CP / kTcBlockK;
-    prm.n_kchunks = d.taps * prm.n_cchunks;
+    prm.n_n_tiles = n_n_tiles;
+    prm.n_m_tiles = n_m_tiles;
+    prm.group = group;
+    prm.n_groups = (n_m_tiles + group - 1) / group * n_n_tiles;
+    prm.n_cchunks = n_cchunks;
     prm.CP = d.CP; prm.Kw = d.Kw; prm.s = d.s; prm.p = d.p;
     prm.amode = amode;
     prm.kpb = kpb;
     prm.stages = stages;
     prm.stage_bytes = stage_bytes;
     prm.a_bytes = a_rows * 128;
-    prm.halo = halo ? 1 : 0;
     prm.n_sp = halo ? d.Kh * (d.Kw / kpb) * n_cchunks : d.taps * n_cchunks;
     prm.n_acc = n_acc;
+    prm.taps = d.taps;
+    prm.b_res = b_res ? 1 : 0;
+    prm.b_res_off = stages * stage_bytes;
+    prm.epi_off = prm.b_res_off + (b_res ? bres_bytes : 0);
     prm.y = y;
     if (grid_rows)
         prm.vec_store = ((d.Wo % 4) == 0 && (d.Wq % 4) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) ? 1 : 0;
     else
         prm.vec_store = ((prm.HoWo % 8) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) ? 1 : 0;
-    int grid = device_sm_count() * ctas_per_sm;
-    if (grid > prm.n_tiles) grid = prm.n_tiles;
+    // At least half the SM's shared memory, so that one CTA runs per SM (it
+    // may take all of TMEM).
+    int smem = prm.epi_off + kEpiBytes + kBarBytes + 1024;
+    if (smem > kSmemLimit) return CONV2D_ERR_UNSUPPORTED;
+    if (smem < kSmemLimit / 2 + 4096) smem = kSmemLimit / 2 + 4096;
+    int grid = n_sm;
+    if (grid > prm.n_groups) grid = prm.n_groups;
 
     const bool bf = d.dtype == CONV2D_BF16;
-    cudaError_t e = bf ? launch_tc_mode<true>(d.BN, amode, amap, bmap, prm, grid, st)
-                       : launch_tc_mode<false>(d.BN, amode, amap, bmap, prm, grid, st);
+    cudaError_t e = bf ? launch_tc_mode<true>(d.BN, amode, amap, bmap, prm, grid, smem, st)
+                       : launch_tc_mode<false>(d.BN, amode, amap, bmap, prm, grid, smem, st);
     return e == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
 }
 
