@@ -105,8 +105,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
     using Cfg = TcConfig<BN>;
     const int S = prm.stages;
     extern __shared__ uint8_t smem_raw[];
-    // 128-byte swizzled operand tiles need 1024-byte alignment.
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 128-byte swizzled operand tiles need 1024-byte alignment.  (Offsetting
+    // the shared array itself keeps pointers in the shared address space.)
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + prm.epi_off + kEpiBytes);
     // bars: [0, S) full, [S, 2S) empty, then per issuer i: accf[i][0..n_acc),
     // acce[i][0..n_acc), then the resident-filter barrier and kIssuers drain barriers.

@@ -239,3 +239,29 @@ def test_repeated_calls_and_streams():
         err, _ = parity(o.double().cpu().numpy(), Y, S)
         assert err <= TOL["f16"]
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+# Padded-source edge cases with one channel tile (resident filter): channel
+# counts below the tile width, Kw = 2 with 128-wide tiles, odd widths (scalar
+# stores), Kh = 1, padding wider than the filter's reach, several images.
+PADDED_EDGE_SHAPES = [
+    # N, Ci, H, W, Co, Kh, Kw, s, p
+    (3, 64, 23, 21, 64, 3, 3, 1, 1),
+    (2, 32, 16, 16, 128, 2, 2, 1, 1),
+    (1, 24, 40, 36, 40, 3, 3, 1, 0),
+    (1, 8, 9, 9, 64, 1, 3, 1, 1),
+    (4, 72, 12, 12, 17, 3, 3, 1, 2),
+]
+
+
+@pytest.mark.parametrize("shape", PADDED_EDGE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_padded_single_channel_tile(shape, dtype):
+    N, Ci, H, W, Co, Kh, Kw, s, p = shape
+    seed = sum(shape) * 13 + len(dtype)
+    X, X64 = synth.round_to(synth.normal(seed, 0, (N, Ci, H, W)), dtype)
+    Wt, W64 = synth.round_to(synth.normal(seed, 1, (Co, Ci, Kh, Kw)), dtype)
+    Y, S = oracle_full(X64, W64, s, p)
+    y, used, _ = run_gpu(X, Wt, s, p, dtype, "padded_tc")
+    err, bad0 = parity(y, Y, S)
+    assert bad0 == 0 and err <= TOL[dtype], (shape, dtype, err)
