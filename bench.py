@@ -40,6 +40,14 @@ import synth  # noqa: E402
 METRIC = "conv fwd TFLOP/s (2*N*Cout*Ho*Wo*Cin*Kh*Kw/t), % of roofline, workspace MB"
 L2_FLUSH_BYTES = 512 << 20
 L2_BYTES = 129 << 20
+# DRAM bytes (read + write) per launch of the contraction kernel, from the ncu
+# captures summarised under profiles/ (launch lists where there is one, else
+# the full capture); null for workloads without a capture of the current kernel.
+NCU_TRAFFIC_BYTES = {
+    ("resnet_stage1", "f16", "padded_tc"): 14.37e6,      # profiles/launches_resnet_stage1_f16.md
+    ("vgg", "f16", "implicit_tc"): 61.83e6,              # profiles/launches_vgg_f16.md
+    ("resnet_stage1", "f32", "im2win_fp32_cc"): 84.13e6,  # profiles/conv_fp32_resnet_stage1_f32.md
+}
 ROTATION_BYTES = 3 * L2_BYTES         # rotating sets: together at least three L2s
 
 
@@ -307,7 +315,8 @@ def run_gpu(args, rank, world):
                    "im2win_tensor_mb": wl.N * wl.Ci * Ho * (wl.W + 2 * wl.pad) * wl.Kh * elem / 2 ** 20,
                    "parallelism": f"independent batch per GPU x{world}"},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None, "kernel": "contraction kernel",
+                     "frac": achieved / peak, "traffic": NCU_TRAFFIC_BYTES.get((wl.name, dtype, op.algo)),
+                     "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)", "kernel": "contraction kernel",
                      "kernel_ms": kms, "peak_source": psrc,
                      "step_frac": (flops / (ms * 1e-3) / 1e12) / peak},
         "gpu_launches": launches * K,
