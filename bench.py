@@ -292,16 +292,30 @@ def run_gpu(args, rank, world):
     value = flops * world / (ms * 1e-3) / 1e12
     peaks, src = _peaks()
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
-    if dtype == "f32":
-        peak = fp32_alu_peak_tflops(sm_count, peaks.get("sm_max_mhz", 2070.0))
-        bound, psrc = "alu", "derived: SMs x 128 FFMA lanes x 2 x max SM clock"
-    else:
-        peak = peaks["bf16_tflops"]
-        bound, psrc = "tensor", f"{src} bf16 dense burst (fp16 rate equal)"
-    achieved = flops / (kms * 1e-3) / 1e12
-    clocks = clk.summary()
     elem = 4 if dtype == "f32" else 2
     Ho, Wo = wl.out_hw()
+    # Algorithmic bytes: X, W and Y once each at their dtypes.
+    alg_bytes = (wl.N * wl.Ci * wl.H * wl.W + wl.Co * wl.Ci * wl.Kh * wl.Kw + wl.N * wl.Co * Ho * Wo) * elem
+    if dtype == "f32":
+        cpeak = fp32_alu_peak_tflops(sm_count, peaks.get("sm_max_mhz", 2070.0))
+        cbound, csrc = "alu", "derived: SMs x 128 FFMA lanes x 2 x max SM clock"
+    else:
+        cpeak = peaks["bf16_tflops"]
+        cbound, csrc = "tensor", f"{src} bf16 dense burst (fp16 rate equal)"
+    # Roofline: a layer whose arithmetic intensity (FLOP per algorithmic byte)
+    # is below the ridge (compute peak / measured HBM copy bandwidth) is
+    # reported against HBM with its algorithmic bytes, else against compute.
+    hbm = peaks["hbm_gbs"]
+    intensity = flops / alg_bytes
+    if intensity < cpeak * 1e12 / (hbm * 1e9):
+        bound, peak, unit, psrc = "hbm", hbm, "GB/s", f"{src} HBM copy bandwidth"
+        achieved = alg_bytes / (kms * 1e-3) / 1e9
+        step_frac = alg_bytes / (ms * 1e-3) / 1e9 / peak
+    else:
+        bound, peak, unit, psrc = cbound, cpeak, "TFLOP/s", csrc
+        achieved = flops / (kms * 1e-3) / 1e12
+        step_frac = (flops / (ms * 1e-3) / 1e12) / peak
+    clocks = clk.summary()
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -314,11 +328,12 @@ def run_gpu(args, rank, world):
                    "workspace_mb": op.workspace_bytes / 2 ** 20,
                    "im2win_tensor_mb": wl.N * wl.Ci * Ho * (wl.W + 2 * wl.pad) * wl.Kh * elem / 2 ** 20,
                    "parallelism": f"independent batch per GPU x{world}"},
-        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": NCU_TRAFFIC_BYTES.get((wl.name, dtype, op.algo)),
                      "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)", "kernel": "contraction kernel",
                      "kernel_ms": kms, "peak_source": psrc,
-                     "step_frac": (flops / (ms * 1e-3) / 1e12) / peak},
+                     "step_frac": step_frac, "intensity_flop_per_byte": intensity,
+                     "algorithmic_bytes": alg_bytes},
         "gpu_launches": launches * K,
         "e2e": {"value": flops * world / (e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": xh.numel() * xh.element_size() + wh.numel() * wh.element_size(),

@@ -285,10 +285,93 @@ __global__ void __launch_bounds__(256) window_cl16_small_kernel(const uint16_t* 
     pdl_wait();   // complete only after the filter repack launched before us
 }
 
+// Small-channel version staged through shared memory: a block covers
+// kWinRowsPerBlock consecutive window rows r0.. of one image and kWinRowX
+// output columns.  It loads the input rows those window rows need once (they
+// overlap: (rows - 1)*s + Kh rows per channel; staged row yi*Ci + ci holds
+// X[n][ci][r0*s - p + yi][.], zero outside the image), as 16-byte vectors
+// where aligned, then builds each 8-element vector of packed (row, channel)
+// pairs from shared memory: pair c = u*Ci + ci of window row r is staged row
+// (r - r0)*s*Ci + c.  The row pitch kWinRowPitch (not a multiple of 8 halves)
+// spreads rows 8 apart over different banks.
+constexpr int kWinRowX = 128;                 // output columns per block
+constexpr int kWinRowCols = kWinRowX + 8;     // staged input columns (the 8-alignment slack)
+constexpr int kWinRowPitch = kWinRowCols + 2;
+constexpr int kWinRowsPerBlock = 4;
+
+__global__ void __launch_bounds__(256) window_cl16_rows_kernel(const uint16_t* __restrict__ x,
+                                                               uint4* __restrict__ out, int Ci, int H, int W, int Ck,
+                                                               int R, int Wq, int Kh, int s, int p, int n_xt,
+                                                               int n_rb, int vec_ok) {
+    extern __shared__ __align__(16) uint16_t rows[];         // [n_y*Ci][kWinRowPitch]
+    pdl_launch_dependents();
+    const int tid = threadIdx.x;
+    const int xt = blockIdx.x % n_xt;
+    const int rb = (blockIdx.x / n_xt) % n_rb;
+    const int n = blockIdx.x / (n_xt * n_rb);
+    const int r0 = rb * kWinRowsPerBlock, nrows = min(kWinRowsPerBlock, R - r0);
+    const int kx0 = xt * kWinRowX, kx_n = min(kWinRowX, Wq - kx0);
+    const int KC = Kh * Ci;
+    const int n_y = (nrows - 1) * s + Kh;                    // staged input rows per channel
+    const int y_lo = r0 * s - p;
+    int xa = kx0 - p;
+    xa = (xa >= 0) ? (xa & ~7) : -((-xa + 7) & ~7);          // floor to a multiple of 8
+    constexpr int nv = kWinRowCols / 8;
+    const long long plane = (long long)H * W;
+    for (int i = tid; i < n_y * Ci * nv; i += 256) {
+        const int row = i / nv, v = i - row * nv;
+        const int yi = row / Ci, ci = row - yi * Ci;
+        const int y = y_lo + yi, x0 = xa + 8 * v;
+        uint32_t w[4] = {0, 0, 0, 0};
+        if (y >= 0 && y < H) {
+            const uint16_t* src = x + ((long long)n * Ci + ci) * plane + (long long)y * W;
+            if (vec_ok && x0 >= 0 && x0 + 8 <= W) {
+                const uint4 val = __ldg(reinterpret_cast<const uint4*>(src + x0));
+                w[0] = val.x; w[1] = val.y; w[2] = val.z; w[3] = val.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (x0 + e >= 0 && x0 + e < W) w[e >> 1] |= (uint32_t)__ldg(src + x0 + e) << (16 * (e & 1));
+            }
+        }
+        uint32_t* dst = reinterpret_cast<uint32_t*>(rows + row * kWinRowPitch + 8 * v);
+        dst[0] = w[0]; dst[1] = w[1]; dst[2] = w[2]; dst[3] = w[3];
+    }
+    __syncthreads();
+    const int cgs = Ck / 8;
+    const int per_row = kx_n * cgs;
+    for (int i = tid; i < nrows * per_row; i += 256) {
+        const int rr = i / per_row, j = i - rr * per_row;
+        const int kxl = j / cgs, cg = j - kxl * cgs;
+        const int col = kx0 + kxl - p - xa;                  // in [0, kWinRowCols)
+        const uint16_t* base = rows + (rr * s * Ci) * kWinRowPitch + col;
+        uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int c = cg * 8 + e;
+            if (c < KC) w[e >> 1] |= (uint32_t)base[c * kWinRowPitch] << (16 * (e & 1));
+        }
+        out[(((long long)n * R + r0 + rr) * Wq + kx0 + kxl) * cgs + cg] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    pdl_wait();   // complete only after the filter repack launched before us
+}
+
 cudaError_t launch_window_cl16(const void* x, void* out, int N, int Ci, int H, int W, int Ci8, int Ck, int R,
                                int Wq, int Kh, int s, int p, cudaStream_t st) {
     const uint16_t* xi = static_cast<const uint16_t*>(x);
     uint4* o = static_cast<uint4*>(out);
+    const long long row_smem = (long long)((kWinRowsPerBlock - 1) * s + Kh) * Ci * kWinRowPitch * 2;
+    const int n_xr = (Wq + kWinRowX - 1) / kWinRowX;
+    const int n_rb = (R + kWinRowsPerBlock - 1) / kWinRowsPerBlock;
+    const long long blocks = (long long)N * n_rb * n_xr;
+    if (Ci8 <= 16 && row_smem <= 96 * 1024 && blocks <= 0x7fffffffLL) {
+        cudaError_t e = cudaFuncSetAttribute(window_cl16_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)row_smem);
+        if (e != cudaSuccess) return e;
+        const int vec_ok = (W % 8 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) ? 1 : 0;
+        return launch_after(window_cl16_rows_kernel, dim3((unsigned)blocks), dim3(256), (size_t)row_smem, st, xi, o,
+                            Ci, H, W, Ck, R, Wq, Kh, s, p, n_xr, n_rb, vec_ok);
+    }
     if (Ci8 <= 16) {
         long long total_vec = (long long)N * R * Wq * (Ck / 8);
         long long blocks = (total_vec + 255) / 256, cap = (long long)device_sm_count() * 16;
