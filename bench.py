@@ -151,6 +151,22 @@ def cpu_oracle_baseline(wl, dtype, budget_s=12.0, threads=None, inputs=None):
                       f"{flops / 1e9:.2f} GFLOP in {dt:.2f} s, fp64 7-loop on {threads} threads"}
 
 
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """The largest of every rank's x (one all-reduce; identity on one rank)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank's independent batch over the slowest rank's time."""
+    return flops_per_rank * world / (ms * 1e-3) / 1e12
+
+
 def _workload(args):
     wl = synth.WORKLOADS[args.workload]
     dtype = args.dtype or wl.dtypes[0]
@@ -264,10 +280,7 @@ def run_gpu(args, rank, world):
     assert capi.conv2d_device_status(sp) == 0
     ms = ev[0].elapsed_time(ev[1]) / K
     kms = sum(kern_ms) / K
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
 
     # End to end through the public API: pinned host X and W in, Y out, every step.
     e2e_ms = []
@@ -283,13 +296,10 @@ def run_gpu(args, rank, world):
         torch.cuda.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
     e2e = sum(e2e_ms[1:]) / max(1, len(e2e_ms) - 1)
-    if world > 1:
-        t = torch.tensor([e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e = float(t.item())
+    e2e = max_over_ranks(e2e, world, dev)
 
     flops = wl.flops()
-    value = flops * world / (ms * 1e-3) / 1e12
+    value = job_tflops(flops, world, ms)
     peaks, src = _peaks()
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
     elem = 4 if dtype == "f32" else 2
@@ -335,7 +345,7 @@ def run_gpu(args, rank, world):
                      "step_frac": step_frac, "intensity_flop_per_byte": intensity,
                      "algorithmic_bytes": alg_bytes},
         "gpu_launches": launches * K,
-        "e2e": {"value": flops * world / (e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_tflops(flops, world, e2e), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": xh.numel() * xh.element_size() + wh.numel() * wh.element_size(),
                 "d2h_bytes_per_step": yh.numel() * yh.element_size(), "ms_per_step": e2e},
         "clocks": clocks,
