@@ -90,6 +90,7 @@ conv2d_status finalize(conv2d_desc& d) {
     if (tc != (d.dtype != CONV2D_F32)) return CONV2D_ERR_BAD_PARAM;
     if (d.layout == CONV2D_LAYOUT_NHWC && d.algo != CONV2D_ALGO_IMPLICIT_TC) return CONV2D_ERR_UNSUPPORTED;
     d.ws_weights = d.ws_input = d.ws_input_off = d.ws_total = 0;
+    d.gemm1x1 = false;
     if (!tc) {
         d.Lp = (d.Wp * d.Kh + 3) & ~3;
         // 32 output channels per warp, 1, 2 or 4 warps; fewer warps when one
@@ -124,12 +125,19 @@ conv2d_status finalize(conv2d_desc& d) {
         const long long chunk = im2win ? (long long)d.Kw * d.Ck : d.Ci8;
         d.CP = (int)((chunk + kTcBlockK - 1) / kTcBlockK * kTcBlockK);
         d.BN = d.Co <= 64 ? 64 : (d.Co <= 128 ? 128 : 256);
+        // A 1x1 layer is a GEMM on the NCHW tensors themselves: the TMA maps
+        // read X as [N][Ci][H*W] and the filter as [Co][Ci] (16-byte strides).
+        d.gemm1x1 = d.algo == CONV2D_ALGO_IMPLICIT_TC && d.layout == CONV2D_LAYOUT_NCHW && d.Kh == 1 &&
+                    d.Kw == 1 && d.s == 1 && d.p == 0 && d.Ci % 8 == 0 && ((long long)d.H * d.W) % 8 == 0;
+        if (d.gemm1x1) d.BN = 128;   // 128 output channels x 128 pixels per MMA tile
         if ((long long)d.Ci * d.Kh * d.Kw > 16384) return CONV2D_ERR_UNSUPPORTED;   // per-channel filter staging
         if (d.N > 65535) return CONV2D_ERR_UNSUPPORTED;
         const long long wq = (long long)d.Co * d.taps * d.CP;
         if (wq > kMaxElems) return CONV2D_ERR_UNSUPPORTED;
-        d.ws_weights = (size_t)wq * 2;
-        if (padded) {
+        d.ws_weights = d.gemm1x1 ? 0 : (size_t)wq * 2;
+        if (d.gemm1x1) {
+            // No workspace: X and the filter are read in place.
+        } else if (padded) {
             d.Hp = d.H + 2 * d.p;
             d.Wq = padded_pitch(d);
             const long long rows = (long long)d.N * d.Hp * d.Wq;
@@ -266,6 +274,11 @@ conv2d_status fwd_impl(conv2d_desc_t dp, const void* x, const void* w, void* y, 
             if (e == cudaSuccess) s = launch_conv_tc(d, win, wq, y, 1, st);
             break;
         case CONV2D_ALGO_IMPLICIT_TC: {
+            if (d.gemm1x1) {   // no repack, no copy: one launch on the caller's tensors
+                if (!record(ev0, st)) return CONV2D_ERR_CUDA;
+                s = launch_conv_tc(d, x, w, y, 3, st);
+                break;
+            }
             e = launch_pack_filter_tc(w, wq, d, false, st);
             const void* src = x;
             if (e == cudaSuccess && d.layout == CONV2D_LAYOUT_NCHW) {
@@ -305,6 +318,10 @@ CONV2D_API conv2d_status conv2d_fwd_profiled(conv2d_desc_t d, const void* x, con
 
 CONV2D_API conv2d_status conv2d_launches_per_call(conv2d_desc_t d, int* launches) {
     if (!d || !launches) return CONV2D_ERR_NULL_PTR;
+    if (d->gemm1x1) {   // the contraction alone
+        *launches = 1;
+        return CONV2D_OK;
+    }
     int n = 2;   // filter repack + contraction
     if (d->algo == CONV2D_ALGO_IM2WIN_FP32_CC || d->algo == CONV2D_ALGO_IM2WIN_TC || d->algo == CONV2D_ALGO_PADDED_TC ||
         (d->algo == CONV2D_ALGO_IMPLICIT_TC && d->layout == CONV2D_LAYOUT_NCHW))

@@ -28,6 +28,14 @@
 //             rows are s*Ck elements apart and overlap; one tap, K = Kw*Ck.
 // B tile (BN channels x 64 K) is a tiled TMA load of the repacked filter.
 //
+// 1x1 layers (stride 1, no padding; kernel MODE 3) need no transform at all:
+// per image Y[co][p] = sum_ci W[co][ci] X[ci][p] is a plain GEMM on the NCHW
+// tensors.  The MMA runs with M = 128 output channels (W, K-major, straight
+// from the caller's filter) and N = 128 pixels (X, read as [ci][p] rows:
+// the "MN-major" operand layout, two 64-pixel boxes per chunk), so each
+// accumulator lane is one output channel and its columns are consecutive
+// pixels: the epilogue stores them straight from registers.
+//
 // Warp roles (192 threads; one CTA per SM, two for tiles up to 128 channels wide; persistent over tiles):
 //   warp 0     TMA producer (one elected lane), STAGES-deep shared-memory ring
 //   warp 1     TMEM allocation + MMA issue (one lane): 4 x (128xBNx16) per stage
@@ -67,6 +75,7 @@ struct TcParams {
     int b_res;          // 1: the whole filter slice of the (single) channel tile stays in shared memory
     int b_res_off;      // byte offsets in the aligned dynamic shared memory
     int epi_off;
+    int n_pt;           // MODE 3: 128-pixel tiles per image
     void* y;
 };
 
@@ -75,6 +84,10 @@ constexpr int kSmemLimit = 232448;                               // 227 KB per b
 constexpr int kIssuers = 2;                                      // MMA-issuing threads (one tile each)
 constexpr int kEpiWarpBytes = 32 * 32 * 2;                       // epilogue staging per warp: 32 ch x 32 px
 constexpr int kEpiBytes = 2 * 4 * kEpiWarpBytes;                 // two epilogue groups of four warps
+constexpr int kEpi1x1WarpBytes = 32 * 64 * 2;                      // MODE 3: one 32 ch x 64 px store box per warp
+constexpr int kEpi1x1Bytes = 2 * 4 * kEpi1x1WarpBytes;
+template <int MODE>
+__host__ __device__ constexpr int epi_bytes() { return MODE == 3 ? kEpi1x1Bytes : kEpiBytes; }
 constexpr int kBarBytes = 512;
 constexpr int kTcThreads = 32 * (1 + kIssuers + 8);              // producer, issuers, 8 epilogue warps
 
@@ -87,8 +100,9 @@ struct TcConfig {
 // [A region of issuer 1][kpb B chunks, unless the filter is resident]; every
 // region is a multiple of 1024 bytes (128-byte swizzle atoms).
 
-// MODE is the A addressing (0 im2col walk, 1 virtual-grid rows); each compiles
-// to its own kernel so the producer and MMA loops carry no run-time mode tests.
+// MODE is the A addressing (0 im2col walk, 1 virtual-grid rows, 3 1x1 GEMM
+// on NCHW); each compiles to its own kernel so the producer and MMA loops
+// carry no run-time mode tests.
 //
 // Tiles are taken in groups of kIssuers consecutive 128-pixel tiles of one
 // channel tile (single tiles when there are fewer than two tiles per SM).  A stage holds the A chunks of every tile in the group and
@@ -101,6 +115,7 @@ struct TcConfig {
 template <int BN, bool BF16, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_constant__ CUtensorMap amap,
                                                                 const __grid_constant__ CUtensorMap bmap,
+                                                                const __grid_constant__ CUtensorMap ymap,
                                                                 const TcParams prm) {
     using Cfg = TcConfig<BN>;
     const int S = prm.stages;
@@ -108,7 +123,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
     // 128-byte swizzled operand tiles need 1024-byte alignment.  (Offsetting
     // the shared array itself keeps pointers in the shared address space.)
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + prm.epi_off + kEpiBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + prm.epi_off + epi_bytes<MODE>());
     // bars: [0, S) full, [S, 2S) empty, then per issuer i: accf[i][0..n_acc),
     // acce[i][0..n_acc), then the resident-filter barrier and kIssuers drain barriers.
     const int nacc = prm.n_acc;
@@ -134,6 +149,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
         mbar_fence_init();
         tma_prefetch_desc(&amap);
         tma_prefetch_desc(&bmap);
+        if constexpr (MODE == 3) tma_prefetch_desc(&ymap);
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(tmem_slot), tmem_cols);
@@ -146,6 +162,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
     // Operands (window / NHWC tensor, repacked filter) come from the kernels
     // launched just before this one; the set-up above overlapped their tail.
     pdl_wait();
+    // A kernel launched after this one as a programmatic dependent may now be
+    // scheduled: its CTAs take SMs as ours leave and run their set-up there,
+    // and its own wait still holds it until this grid has completed.
+    pdl_launch_dependents();
 
     const int kpb = MODE == 1 ? prm.kpb : 1;
     if (warp == 0) {
@@ -186,6 +206,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
                             ho[i] = r / prm.Wo;
                             wo[i] = r - ho[i] * prm.Wo;
                         }
+                    } else if constexpr (MODE == 3) {
+                        if (val[i]) {                      // image and first pixel of the tile
+                            img[i] = (mt0 + i) / prm.n_pt;
+                            wo[i] = ((mt0 + i) - img[i] * prm.n_pt) * kTcBlockM;
+                        }
                     }
                 }
                 const uint32_t tx = (uint32_t)(n_val * prm.a_bytes + (prm.b_res ? 0 : kpb * Cfg::kBBytes));
@@ -212,6 +237,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
                             // same rows shifted by one pixel each, so they share one copy.
                             // (im2win: one tap, t = 0.)
                             tma_load_2d(dst, &amap, full_bar(stage), c0, m0[i] + kh * prm.Wq + kw);
+                        } else if constexpr (MODE == 3) {
+                            // X[img][c0..c0+63][p0..p0+127] as two 64-pixel boxes.
+                            tma_load_3d(dst, &amap, full_bar(stage), wo[i], c0, img[i]);
+                            tma_load_3d(dst + 8192u, &amap, full_bar(stage), wo[i] + 64, c0, img[i]);
                         } else {
                             tma_load_im2col_4d(dst, &amap, full_bar(stage), c0, wo[i] * prm.s - prm.p,
                                                ho[i] * prm.s - prm.p, img[i], (uint16_t)kw, (uint16_t)kh);
@@ -251,7 +280,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
         // ------------------------------------------------------------ MMA issuers
         const int is = warp - 1;
         if (lane == 0 && is < prm.group) {
-            constexpr uint32_t idesc = umma_idesc_f16(BF16, kTcBlockM, BN);
+            // MODE 3: the pixel operand is MN-major (instruction descriptor bit 16).
+            constexpr uint32_t idesc = umma_idesc_f16(BF16, kTcBlockM, BN) | (MODE == 3 ? (1u << 16) : 0u);
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true, issued_any = false, ready_now = false;
@@ -275,14 +305,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
                     const uint64_t b_desc = sw128_kmajor_desc(
                         prm.b_res ? bres_base + (uint32_t)((cb * prm.taps + t) * Cfg::kBBytes)
                                   : st_base + (uint32_t)(prm.group * prm.a_bytes));
-                    for (int i = 0; i < kpb; ++i) {
-                        // Halo: tap kw0+i reads the A tile from row i (128 bytes per row).
-                        // Descriptor start addresses are in 16-byte units.
+                    if constexpr (MODE == 3) {
+                        // M = output channels (the filter chunk, K-major), N = pixels
+                        // (this tile's X chunk, MN-major: 16 K rows = 2 KB per step).
+                        const uint64_t x_desc = sw128_mnmajor_desc(st_base + (uint32_t)(is * prm.a_bytes), 8192u);
 #pragma unroll
-                        for (int k = 0; k < kTcBlockK / 16; ++k) {
-                            umma_f16(d_tmem, a_desc + (uint64_t)(i * 8 + 2 * k),
-                                     b_desc + (uint64_t)(i * (Cfg::kBBytes >> 4) + 2 * k), idesc,
-                                     (sp > 0 || i > 0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < kTcBlockK / 16; ++k)
+                            umma_f16(d_tmem, b_desc + (uint64_t)(2 * k), x_desc + (uint64_t)(128 * k), idesc,
+                                     (sp > 0 || k > 0) ? 1u : 0u);
+                    } else {
+                        for (int i = 0; i < kpb; ++i) {
+                            // Halo: tap kw0+i reads the A tile from row i (128 bytes per row).
+                            // Descriptor start addresses are in 16-byte units.
+#pragma unroll
+                            for (int k = 0; k < kTcBlockK / 16; ++k) {
+                                umma_f16(d_tmem, a_desc + (uint64_t)(i * 8 + 2 * k),
+                                         b_desc + (uint64_t)(i * (Cfg::kBBytes >> 4) + 2 * k), idesc,
+                                         (sp > 0 || i > 0 || k > 0) ? 1u : 0u);
+                            }
                         }
                     }
                     issued_any = true;
@@ -327,6 +367,54 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
             const int m0 = ((g / prm.n_n_tiles) * prm.group + eg) * kTcBlockM;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    (uint32_t)((eg * nacc + acc) * BN);
+            if constexpr (MODE == 3) {
+                // Lane = output channel co0 + lane; columns = the tile's pixels p0..
+                // of one image.  Each 64-pixel half goes through the warp's 4 KB
+                // box in shared memory (128-byte rows, 128-byte swizzle, so the
+                // 16-byte writes of 8 lanes cover all banks) and leaves as one TMA
+                // store of 32 channels x 64 pixels; the store clips the pixel and
+                // channel tails.
+                const int mt = m0 / kTcBlockM;
+                const int img = mt / prm.n_pt, p0 = (mt - img * prm.n_pt) * kTcBlockM;
+                const int co0 = n0 + quarter * 32;
+                const bool live = img < prm.N && co0 < prm.Co;
+                const uint32_t wbuf = smem_addr(smem + prm.epi_off + ew * kEpi1x1WarpBytes);
+#pragma unroll 1
+                for (int h = 0; h < BN / 64; ++h) {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld_32x32b_x32(t_row + h * 64, v0);
+                    tmem_ld_32x32b_x32(t_row + h * 64 + 32, v1);
+                    tmem_ld_wait();
+                    if (!live || p0 + h * 64 >= prm.HoWo) continue;   // warp-uniform
+                    if (lane == 0) bulk_wait_read_all();              // the box is free again
+                    __syncwarp();
+                    const uint32_t row = wbuf + (uint32_t)lane * 128u;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t(&v)[32] = c < 4 ? v0 : v1;
+                        uint32_t h4[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float lo = __uint_as_float(v[(c & 3) * 8 + 2 * j]);
+                            const float hi = __uint_as_float(v[(c & 3) * 8 + 2 * j + 1]);
+                            if (BF16) {
+                                const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                                h4[j] = *reinterpret_cast<const uint32_t*>(&b2);
+                            } else {
+                                const __half2 f2 = __floats2half2_rn(lo, hi);
+                                h4[j] = *reinterpret_cast<const uint32_t*>(&f2);
+                            }
+                        }
+                        st_shared_v4(row + (uint32_t)((c ^ (lane & 7)) * 16), h4[0], h4[1], h4[2], h4[3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&ymap, wbuf, p0 + h * 64, co0, img);
+                        bulk_commit_group();
+                    }
+                }
+            } else {
             const int mw = m0 + quarter * 32;
             // Store geometry: this lane's piece of the warp's 32 pixels (vector
             // paths) or its own pixel (scalar path).
@@ -402,10 +490,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
                 emit(v0, cc);
                 emit(v1, cc + 1);
             }
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(eg, acc));
             if (++acc == nacc) { acc = 0; acc_phase ^= 1; }
+        }
+        // MODE 3: the TMA stores of this warp complete before the CTA exits.
+        if constexpr (MODE == 3) {
+            if (lane == 0) bulk_wait_all();
         }
     }
 
@@ -451,29 +544,36 @@ typedef CUresult (*PFN_encodeIm2col_t)(CUtensorMap*, CUtensorMapDataType, cuuint
                                        CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 template <int BN, bool BF16, int MODE>
-static cudaError_t launch_tc_inst(const CUtensorMap& a, const CUtensorMap& b, const TcParams& prm, int grid,
-                                  int smem, cudaStream_t st) {
+static cudaError_t launch_tc_inst(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y,
+                                  const TcParams& prm, int grid, int smem, cudaStream_t st) {
     auto kern = conv_tc_kernel<BN, BF16, MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_after(kern, dim3(grid), dim3(kTcThreads), smem, st, a, b, prm);
+    return launch_after(kern, dim3(grid), dim3(kTcThreads), smem, st, a, b, y, prm);
 }
 
 template <bool BF16, int MODE>
-static cudaError_t launch_tc_bn(int BN, const CUtensorMap& a, const CUtensorMap& b, const TcParams& prm, int grid,
-                                int smem, cudaStream_t st) {
-    switch (BN) {
-        case 64:  return launch_tc_inst<64, BF16, MODE>(a, b, prm, grid, smem, st);
-        case 128: return launch_tc_inst<128, BF16, MODE>(a, b, prm, grid, smem, st);
-        default:  return launch_tc_inst<256, BF16, MODE>(a, b, prm, grid, smem, st);
+static cudaError_t launch_tc_bn(int BN, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y,
+                                const TcParams& prm, int grid, int smem, cudaStream_t st) {
+    if constexpr (MODE == 3) {                 // 128 output channels x 128 pixels only
+        return BN == 128 ? launch_tc_inst<128, BF16, 3>(a, b, y, prm, grid, smem, st) : cudaErrorInvalidValue;
+    } else {
+        switch (BN) {
+            case 64:  return launch_tc_inst<64, BF16, MODE>(a, b, y, prm, grid, smem, st);
+            case 128: return launch_tc_inst<128, BF16, MODE>(a, b, y, prm, grid, smem, st);
+            default:  return launch_tc_inst<256, BF16, MODE>(a, b, y, prm, grid, smem, st);
+        }
     }
 }
 
 template <bool BF16>
-static cudaError_t launch_tc_mode(int BN, int amode, const CUtensorMap& a, const CUtensorMap& b, const TcParams& prm,
-                                  int grid, int smem, cudaStream_t st) {
-    return amode == 0 ? launch_tc_bn<BF16, 0>(BN, a, b, prm, grid, smem, st)
-                      : launch_tc_bn<BF16, 1>(BN, a, b, prm, grid, smem, st);
+static cudaError_t launch_tc_mode(int BN, int amode, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y,
+                                  const TcParams& prm, int grid, int smem, cudaStream_t st) {
+    switch (amode) {
+        case 0:  return launch_tc_bn<BF16, 0>(BN, a, b, y, prm, grid, smem, st);
+        case 3:  return launch_tc_bn<BF16, 3>(BN, a, b, y, prm, grid, smem, st);
+        default: return launch_tc_bn<BF16, 1>(BN, a, b, y, prm, grid, smem, st);
+    }
 }
 
 conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* wq, void* y, int amode,
@@ -485,7 +585,7 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     const CUtensorMapDataType dt =
         d.dtype == CONV2D_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 
-    CUtensorMap amap, bmap;
+    CUtensorMap amap, bmap, ymap;
     // Ring layout.  A stage holds the A chunks of the tiles of a group and,
     // unless the filter is resident, the B chunks they share.
     // Padded mode puts kpb neighbouring taps of one filter row in a stage,
@@ -495,16 +595,20 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     const int n_cchunks = d.CP / kTcBlockK;
     const int b_chunk = d.BN * kTcBlockK * 2;
     const bool halo = amode == 2;
-    const bool grid_rows = amode != 0;
+    const bool grid_rows = amode == 1 || amode == 2;
+    const bool gemm1x1 = amode == 3;
+    const int n_pt = (d.H * d.W + kTcBlockM - 1) / kTcBlockM;   // 1x1 GEMM: pixel tiles per image
     const int n_n_tiles = (d.Co + d.BN - 1) / d.BN;
     const int n_sm = device_sm_count();
     // Last virtual row that is an output, plus one (grid modes).
     const int m_end = grid_rows ? (d.N - 1) * d.Hp * d.Wq + (d.Ho - 1) * d.Wq + d.Wo : 0;
-    const int n_m_tiles = ((grid_rows ? m_end : d.N * d.Ho * d.Wo) + kTcBlockM - 1) / kTcBlockM;
+    const int n_m_tiles =
+        gemm1x1 ? d.N * n_pt : ((grid_rows ? m_end : d.N * d.Ho * d.Wo) + kTcBlockM - 1) / kTcBlockM;
     // Pairs of tiles share B and keep two MMA issuers busy; with fewer than
     // two tiles per SM, single tiles keep every SM busy instead.
     const int group = (long long)n_m_tiles * n_n_tiles >= 2LL * n_sm ? kIssuers : 1;
-    const int budget = kSmemLimit - 1024 - kEpiBytes - kBarBytes;
+    const int epi_region = gemm1x1 ? kEpi1x1Bytes : kEpiBytes;
+    const int budget = kSmemLimit - 1024 - epi_region - kBarBytes;
     // Ring plan for a budget: halo width kpb (largest divisor of Kw leaving at
     // least 2 stages: a halo stage holds kpb taps' MMAs, so two of them keep
     // the pipe busier than three narrow ones; measured on the K=3 layer with
@@ -548,6 +652,16 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
         r = enc_tiled(&amap, dt, 2, const_cast<void*>(src), wdims, wstr, wbox, westr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else if (gemm1x1) {
+        // X as [N][Ci][P]: boxes of 64 pixels x 64 channels (rows past P or Ci read as zero).
+        const cuuint64_t P = (cuuint64_t)d.H * d.W;
+        cuuint64_t xdims[3] = {P, (cuuint64_t)d.Ci, (cuuint64_t)d.N};
+        cuuint64_t xstr[2] = {P * 2, P * 2 * (cuuint64_t)d.Ci};
+        cuuint32_t xbox[3] = {64, (cuuint32_t)kTcBlockK, 1};
+        cuuint32_t xestr[3] = {1, 1, 1};
+        r = enc_tiled(&amap, dt, 3, const_cast<void*>(src), xdims, xstr, xbox, xestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else if (amode == 2) {
         // Padded channels-last copy viewed as [N*Hp*Wq pixel rows][Ci8 channels];
         // box 64 channels x a_rows pixels (rows past the end read as zero).
@@ -573,7 +687,16 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     // B: repacked filter [Co][taps][CP].  Grid modes: (CP, Co, tap) with box
     // 64 x BN x kpb = the chunks of kpb consecutive taps for one channel block;
     // otherwise 2-D (taps*CP, Co) with box 64 x BN.
-    if (grid_rows) {
+    if (gemm1x1) {
+        // The caller's filter [Co][Ci] as is (no repack): boxes of 64 channels x 128 output channels.
+        cuuint64_t bdims[2] = {(cuuint64_t)d.Ci, (cuuint64_t)d.Co};
+        cuuint64_t bstr[1] = {(cuuint64_t)d.Ci * 2};
+        cuuint32_t bbox[2] = {(cuuint32_t)kTcBlockK, (cuuint32_t)d.BN};
+        cuuint32_t bestr[2] = {1, 1};
+        r = enc_tiled(&bmap, dt, 2, const_cast<void*>(wq), bdims, bstr, bbox, bestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else if (grid_rows) {
         cuuint64_t bdims[3] = {(cuuint64_t)d.CP, (cuuint64_t)d.Co, (cuuint64_t)d.taps};
         cuuint64_t bstr[2] = {(cuuint64_t)d.taps * d.CP * 2, (cuuint64_t)d.CP * 2};
         cuuint32_t bbox[3] = {(cuuint32_t)kTcBlockK, (cuuint32_t)d.BN, (cuuint32_t)kpb};
@@ -591,6 +714,19 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     if (r != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
+    if (gemm1x1) {
+        // Y as [N][Co][P]: store boxes of 64 pixels x 32 channels (one epilogue warp's lanes).
+        const cuuint64_t P = (cuuint64_t)d.H * d.W;
+        cuuint64_t ydims[3] = {P, (cuuint64_t)d.Co, (cuuint64_t)d.N};
+        cuuint64_t ystr[2] = {P * 2, P * 2 * (cuuint64_t)d.Co};
+        cuuint32_t ybox[3] = {64, 32, 1};
+        cuuint32_t yestr[3] = {1, 1, 1};
+        r = enc_tiled(&ymap, dt, 3, y, ydims, ystr, ybox, yestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
+    } else {
+        ymap = amap;   // unused by the other modes
+    }
 
     TcParams prm{};
     // M runs over output pixels, or over the virtual grid up to the last output (grid modes).
@@ -616,6 +752,7 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     prm.b_res = b_res ? 1 : 0;
     prm.b_res_off = stages * stage_bytes;
     prm.epi_off = prm.b_res_off + (b_res ? bres_bytes : 0);
+    prm.n_pt = n_pt;
     prm.y = y;
     if (grid_rows)
         prm.vec_store = ((d.Wo % 4) == 0 && (d.Wq % 4) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) ? 1 : 0;
@@ -623,15 +760,15 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
         prm.vec_store = ((prm.HoWo % 8) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) ? 1 : 0;
     // At least half the SM's shared memory, so that one CTA runs per SM (it
     // may take all of TMEM).
-    int smem = prm.epi_off + kEpiBytes + kBarBytes + 1024;
+    int smem = prm.epi_off + epi_region + kBarBytes + 1024;
     if (smem > kSmemLimit) return CONV2D_ERR_UNSUPPORTED;
     if (smem < kSmemLimit / 2 + 4096) smem = kSmemLimit / 2 + 4096;
     int grid = n_sm;
     if (grid > prm.n_groups) grid = prm.n_groups;
 
     const bool bf = d.dtype == CONV2D_BF16;
-    cudaError_t e = bf ? launch_tc_mode<true>(d.BN, amode, amap, bmap, prm, grid, smem, st)
-                       : launch_tc_mode<false>(d.BN, amode, amap, bmap, prm, grid, smem, st);
+    cudaError_t e = bf ? launch_tc_mode<true>(d.BN, amode, amap, bmap, ymap, prm, grid, smem, st)
+                       : launch_tc_mode<false>(d.BN, amode, amap, bmap, ymap, prm, grid, smem, st);
     return e == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
 }
 

@@ -27,6 +27,8 @@ struct conv2d_desc {
     int taps;             // filter taps per K-chunk group: Kw (im2win) or Kh*Kw (implicit)
     int CP;               // channel extent per tap, padded to the 64-element K chunk
     int BN;               // output channels per MMA tile (64, 128 or 256)
+    bool gemm1x1;         // implicit path on a 1x1, stride-1, unpadded NCHW layer with Ci and H*W multiples
+                          // of 8: one GEMM per image straight on the caller's X and filter (no copies)
     int Hp, Wq;           // virtual pixel grid [N][Hp][Wq] of the grid-row tensor-core paths.  Padded:
                           // H+2p rows of pitch W+2p (rounded up to 4 when Wo % 4 == 0).  im2win: Ho rows
                           // of Wq output slots (window tensor rows hold Wq*s columns)

@@ -67,7 +67,13 @@ typedef enum { CONV2D_F32 = 0, CONV2D_F16 = 1, CONV2D_BF16 = 2 } conv2d_dtype;
  *                   (the implicit expansion of "im2col Expansion, FFT
  *                   Convolution, and Winograd Transforms", im2col section).
  *                   Workspace: the repacked filter, plus a channels-last copy
- *                   of X when the input layout is NCHW.
+ *                   of X when the input layout is NCHW.  A 1x1, stride-1,
+ *                   unpadded layer on NCHW input with Cin and H*W multiples
+ *                   of 8 is one GEMM per image, Y[co][p] = sum_ci W[co][ci]
+ *                   X[ci][p] (the convolution sum with Kh = Kw = 1, s = 1,
+ *                   p = 0, where the expansion is the identity): it reads x
+ *                   and w in place, needs no workspace (size 0) and makes
+ *                   one launch.
  *  IMPLICIT_FP32_CC fp32 on CUDA cores, staging X's rows directly (no input
  *                   expansion); workspace: the repacked filter only.
  *  PADDED_TC        fp16/bf16 on tcgen05 tensor cores, stride 1 and NCHW input
@@ -155,7 +161,8 @@ conv2d_status conv2d_fwd_profiled(conv2d_desc_t d, const void *x, const void *w,
                                   void *ev_start, void *ev_end);
 
 /* Number of kernel launches one conv2d_fwd call makes for this descriptor
- * (filter repack, input transform if any, contraction). */
+ * (filter repack, input transform if any, contraction; the contraction alone
+ * for the in-place 1x1 GEMM). */
 conv2d_status conv2d_launches_per_call(conv2d_desc_t d, int *launches);
 
 /* Size of the library's built-in workspace used by

@@ -265,3 +265,38 @@ def test_padded_single_channel_tile(shape, dtype):
     y, used, _ = run_gpu(X, Wt, s, p, dtype, "padded_tc")
     err, bad0 = parity(y, Y, S)
     assert bad0 == 0 and err <= TOL[dtype], (shape, dtype, err)
+
+
+# 1x1 layers run as one GEMM per image on the NCHW tensors (no workspace):
+# channel counts off the 64-wide K chunk, pixel counts off the 128-pixel tile
+# (a tail shorter than one 64-pixel box, tails that end mid-vector), output
+# channels off the 128-channel tile and several channel tiles.
+GEMM1X1_SHAPES = [
+    # N, Ci, H, W, Co
+    (2, 128, 16, 16, 128),
+    (3, 72, 10, 12, 17),
+    (1, 8, 2, 4, 130),
+    (2, 200, 7, 8, 300),
+    (4, 64, 56, 56, 64),
+    (1, 16, 5, 40, 256),
+]
+
+
+@pytest.mark.parametrize("shape", GEMM1X1_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_gemm_1x1(shape, dtype):
+    from dense_convolution_gb300 import capi
+    N, Ci, H, W, Co = shape
+    seed = sum(shape) * 17 + len(dtype)
+    X, X64 = synth.round_to(synth.normal(seed, 0, (N, Ci, H, W)), dtype)
+    Wt, W64 = synth.round_to(synth.normal(seed, 1, (Co, Ci, 1, 1)), dtype)
+    Y, S = oracle_full(X64, W64, 1, 0)
+    y, used, ws = run_gpu(X, Wt, 1, 0, dtype, "implicit_tc")
+    assert used == "implicit_tc" and ws == 0
+    err, bad0 = parity(y, Y, S)
+    assert bad0 == 0 and err <= TOL[dtype], (shape, dtype, err)
+    d = capi.conv2d_desc_create(N, Ci, H, W, Co, 1, 1, 1, 0, dtype, "implicit_tc")
+    try:
+        assert capi.conv2d_launches_per_call(d) == 1
+    finally:
+        capi.conv2d_desc_destroy(d)
