@@ -40,13 +40,17 @@ import synth  # noqa: E402
 METRIC = "conv fwd TFLOP/s (2*N*Cout*Ho*Wo*Cin*Kh*Kw/t), % of roofline, workspace MB"
 L2_FLUSH_BYTES = 512 << 20
 L2_BYTES = 129 << 20
-# DRAM bytes (read + write) per launch of the contraction kernel, from the ncu
-# captures summarised under profiles/ (launch lists where there is one, else
-# the full capture); null for workloads without a capture of the current kernel.
+# DRAM bytes (read + write) per launch of the contraction kernel, from ncu
+# captures of the current kernels (launch lists where there is one, else the
+# full capture; writes that stay in L2 during a replay read as 0); null for
+# workloads without such a capture.
 NCU_TRAFFIC_BYTES = {
-    ("resnet_stage1", "f16", "padded_tc"): 14.37e6,      # profiles/launches_resnet_stage1_f16.md
-    ("vgg", "f16", "implicit_tc"): 61.83e6,              # profiles/launches_vgg_f16.md
-    ("resnet_stage1", "f32", "im2win_fp32_cc"): 84.13e6,  # profiles/conv_fp32_resnet_stage1_f32.md
+    ("resnet_stage1", "f16", "padded_tc"): 14.37e6,
+    ("vgg", "f16", "implicit_tc"): 62.24e6,
+    ("sweep_k1", "f16", "implicit_tc"): 16.84e6,
+    ("sweep_k3", "f16", "padded_tc"): 18.73e6,
+    ("stem", "f16", "im2win_tc"): 40.34e6,
+    ("resnet_stage1", "f32", "im2win_fp32_cc"): 84.13e6,
 }
 ROTATION_BYTES = 3 * L2_BYTES         # rotating sets: together at least three L2s
 
