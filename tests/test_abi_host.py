@@ -168,3 +168,29 @@ def test_padded_algo_limits(capi):
 
 def test_destroy_null_is_ok(capi):
     capi.conv2d_desc_destroy(0)
+
+
+@pytest.mark.parametrize("shape,dtype,gemm", [
+    ((16, 128, 64, 64, 128, 1, 1, 1, 0), "f16", True),     # the 1x1 sweep layer
+    ((2, 72, 10, 12, 17, 1, 1, 1, 0), "bf16", True),      # Ci, H*W multiples of 8, any Co
+    ((2, 12, 10, 12, 17, 1, 1, 1, 0), "f16", False),      # Ci % 8 != 0: the TMA row pitch
+    ((2, 64, 5, 5, 64, 1, 1, 1, 0), "f16", False),        # H*W % 8 != 0
+    ((2, 64, 8, 8, 64, 1, 1, 2, 0), "f16", False),        # stride 2
+    ((2, 64, 8, 8, 64, 1, 1, 1, 1), "f16", False),        # padded 1x1
+])
+def test_one_by_one_gemm_selection(capi, shape, dtype, gemm):
+    d = capi.conv2d_desc_create(*shape, dtype, "implicit_tc")
+    try:
+        ws = capi.conv2d_workspace_size(d)
+        n = capi.conv2d_launches_per_call(d)
+        if gemm:
+            assert ws == 0 and n == 1
+        else:
+            assert ws > 0 and n == 3
+        # An NHWC input (Ci % 8 == 0 only) never takes the in-place GEMM, which
+        # reads X as [ci][pixels]: filter repack + implicit contraction.
+        if shape[1] % 8 == 0:
+            capi.conv2d_desc_set_input_layout(d, "nhwc")
+            assert capi.conv2d_launches_per_call(d) == 2
+    finally:
+        capi.conv2d_desc_destroy(d)
