@@ -22,7 +22,7 @@ ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 LAYOUTS = {"nchw": 0, "nhwc": 1}
 
 EXPORTED = ("conv2d_desc_create", "conv2d_desc_set_input_layout", "conv2d_desc_destroy", "conv2d_out_dims",
-            "conv2d_workspace_size", "conv2d_get_algo", "conv2d_fwd", "conv2d_fwd_profiled",
+            "conv2d_workspace_size", "conv2d_get_algo", "conv2d_fwd", "conv2d_fwd_profiled", "conv2d_fwd_host",
             "conv2d_launches_per_call", "conv2d_fwd_static_workspace", "conv2d_device_status",
             "conv2d_status_string")
 STATIC_WORKSPACE_BYTES = 64 << 20
@@ -54,6 +54,7 @@ def load(path: str = LIB_PATH):
     L.conv2d_get_algo.argtypes = [vp, ctypes.POINTER(c_int)]
     L.conv2d_fwd.argtypes = [vp, vp, vp, vp, vp, c_size, vp]
     L.conv2d_fwd_profiled.argtypes = [vp, vp, vp, vp, vp, c_size, vp, vp, vp]
+    L.conv2d_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, c_size, vp]
     L.conv2d_launches_per_call.argtypes = [vp, ctypes.POINTER(c_int)]
     L.conv2d_fwd_static_workspace.argtypes = [vp, vp, vp, vp, vp]
     L.conv2d_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
@@ -118,6 +119,13 @@ def conv2d_fwd_profiled(desc: int, x: int, w: int, y: int, workspace: int, works
                         ev_start: int, ev_end: int):
     _check(load().conv2d_fwd_profiled(desc, x, w, y, workspace or None, workspace_bytes, stream or None,
                                       ev_start or None, ev_end or None), "conv2d_fwd_profiled")
+
+
+def conv2d_fwd_host(desc: int, x_host: int, w_host: int, y_host: int, x_dev: int, w_dev: int, y_dev: int,
+                    workspace: int, workspace_bytes: int, stream: int = 0):
+    """conv2d_fwd on host operands: copy in, call, copy out, all on `stream`."""
+    _check(load().conv2d_fwd_host(desc, x_host, w_host, y_host, x_dev, w_dev, y_dev, workspace or None,
+                                  workspace_bytes, stream or None), "conv2d_fwd_host")
 
 
 def conv2d_launches_per_call(desc: int) -> int:

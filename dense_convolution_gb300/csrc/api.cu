@@ -316,6 +316,29 @@ CONV2D_API conv2d_status conv2d_fwd_profiled(conv2d_desc_t d, const void* x, con
     return fwd_impl(d, x, w, y, workspace, workspace_bytes, stream, ev_start, ev_end);
 }
 
+CONV2D_API conv2d_status conv2d_fwd_host(conv2d_desc_t dp, const void* x_host, const void* w_host, void* y_host,
+                                         void* x_dev, void* w_dev, void* y_dev, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+    if (!dp || !x_host || !w_host || !y_host || !x_dev || !w_dev || !y_dev) return CONV2D_ERR_NULL_PTR;
+    const conv2d_desc& d = *dp;
+    // The device-side checks of conv2d_fwd, before any copy is issued.
+    if (d.ws_total > 0 && !workspace) return CONV2D_ERR_NULL_PTR;
+    if (!aligned16(x_dev) || !aligned16(w_dev) || !aligned16(y_dev) || (workspace && !aligned16(workspace)))
+        return CONV2D_ERR_MISALIGNED;
+    if (workspace_bytes < d.ws_total) return CONV2D_ERR_WORKSPACE_TOO_SMALL;
+    const size_t elem = d.dtype == CONV2D_F32 ? 4 : 2;
+    const size_t x_bytes = (size_t)d.N * d.Ci * d.H * d.W * elem;
+    const size_t w_bytes = (size_t)d.Co * d.Ci * d.Kh * d.Kw * elem;
+    const size_t y_bytes = (size_t)d.N * d.Co * d.Ho * d.Wo * elem;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return CONV2D_ERR_CUDA;
+    if (cudaMemcpyAsync(w_dev, w_host, w_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return CONV2D_ERR_CUDA;
+    const conv2d_status s = fwd_impl(dp, x_dev, w_dev, y_dev, workspace, workspace_bytes, stream, nullptr, nullptr);
+    if (s != CONV2D_OK) return s;
+    if (cudaMemcpyAsync(y_host, y_dev, y_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return CONV2D_ERR_CUDA;
+    return CONV2D_OK;
+}
+
 CONV2D_API conv2d_status conv2d_launches_per_call(conv2d_desc_t d, int* launches) {
     if (!d || !launches) return CONV2D_ERR_NULL_PTR;
     if (d->gemm1x1) {   // the contraction alone

@@ -160,6 +160,23 @@ conv2d_status conv2d_fwd_profiled(conv2d_desc_t d, const void *x, const void *w,
                                   void *workspace, size_t workspace_bytes, void *stream,
                                   void *ev_start, void *ev_end);
 
+/* conv2d_fwd for operands in host memory.  On `stream`, in order: copies
+ * x_host into x_dev and w_host into w_dev (one cudaMemcpyAsync each), runs
+ * conv2d_fwd(d, x_dev, w_dev, y_dev, workspace, ...), and copies y_dev back
+ * into y_host.  Sizes follow the descriptor: x holds N*Cin*H*W and w
+ * Cout*Cin*Kh*Kw elements of the input dtype (in the descriptor's input
+ * layout), y N*Cout*Ho*Wo elements of the output dtype.  The caller owns all
+ * buffers; the device ones obey conv2d_fwd's rules.  With page-locked host
+ * memory the call returns before the copies finish (synchronise the stream
+ * before reading y_host or reusing x_host); with pageable memory the CUDA
+ * runtime stages the copies.  Calls on different streams overlap, so a caller
+ * streaming batches can hide one call's copies behind another's compute.
+ * Errors: as conv2d_fwd (checked before any copy), NULL_PTR for a null host
+ * pointer, CUDA when a copy cannot be issued. */
+conv2d_status conv2d_fwd_host(conv2d_desc_t d, const void *x_host, const void *w_host, void *y_host,
+                              void *x_dev, void *w_dev, void *y_dev, void *workspace,
+                              size_t workspace_bytes, void *stream);
+
 /* Number of kernel launches one conv2d_fwd call makes for this descriptor
  * (filter repack, input transform if any, contraction; the contraction alone
  * for the in-place 1x1 GEMM). */

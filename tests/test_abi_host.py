@@ -194,3 +194,25 @@ def test_one_by_one_gemm_selection(capi, shape, dtype, gemm):
             assert capi.conv2d_launches_per_call(d) == 2
     finally:
         capi.conv2d_desc_destroy(d)
+
+
+def test_fwd_host_argument_checks_before_copy(capi):
+    # These return before any copy or launch, so fake addresses are safe here.
+    d = capi.conv2d_desc_create(1, 8, 16, 16, 8, 3, 3, 1, 1, "f16", "implicit_tc")
+    try:
+        ws = capi.conv2d_workspace_size(d)
+        A = 1 << 20
+        with pytest.raises(capi.Conv2dError) as e:
+            capi.conv2d_fwd_host(d, 0, A, A, A, A, A, A, ws)
+        assert e.value.status == capi.ERR_NULL_PTR
+        with pytest.raises(capi.Conv2dError) as e:
+            capi.conv2d_fwd_host(d, A, A, A, A, A, 0, A, ws)
+        assert e.value.status == capi.ERR_NULL_PTR
+        with pytest.raises(capi.Conv2dError) as e:
+            capi.conv2d_fwd_host(d, A, A, A, A + 8, A, A, A, ws)
+        assert e.value.status == capi.ERR_MISALIGNED
+        with pytest.raises(capi.Conv2dError) as e:
+            capi.conv2d_fwd_host(d, A, A, A, A, A, A, A, ws - 1)
+        assert e.value.status == capi.ERR_WORKSPACE_TOO_SMALL
+    finally:
+        capi.conv2d_desc_destroy(d)

@@ -300,3 +300,37 @@ def test_gemm_1x1(shape, dtype):
         assert capi.conv2d_launches_per_call(d) == 1
     finally:
         capi.conv2d_desc_destroy(d)
+
+
+@pytest.mark.parametrize("name,dtype,algo", [("resnet_stage1", "f16", "auto"), ("sweep_k1", "f16", "auto"),
+                                              ("tiny", "f32", "auto"), ("stem", "bf16", "im2win_tc")])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_fwd_host_matches_device_call(name, dtype, algo, pinned):
+    """conv2d_fwd_host (copy in, call, copy out on one stream) gives the same
+    bits as conv2d_fwd on device operands, from page-locked or pageable host
+    memory."""
+    import torch
+    from dense_convolution_gb300 import capi
+    from dense_convolution_gb300.conv import Conv2d
+    wl = synth.WORKLOADS[name]
+    n = REDUCED_N[name]
+    d = synth.make_inputs(wl, dtype, N=n)
+    op = Conv2d(n, wl.Ci, wl.H, wl.W, wl.Co, wl.Kh, wl.Kw, wl.stride, wl.pad, dtype, algo)
+    xh = (torch.from_numpy(d["X"]) if dtype != "bf16" else d["X"]).contiguous()
+    wh = (torch.from_numpy(d["W"]) if dtype != "bf16" else d["W"]).contiguous()
+    if pinned:
+        xh, wh = xh.pin_memory(), wh.pin_memory()
+    ref = op(xh.cuda(), wh.cuda()).cpu()
+    xd, wd = torch.empty_like(xh, device="cuda"), torch.empty_like(wh, device="cuda")
+    yd = op.alloc_output()
+    yh = torch.full(tuple(yd.shape), float("nan"), dtype=yd.dtype)
+    if pinned:
+        yh = yh.pin_memory()
+    ws = op.alloc_workspace()
+    st = torch.cuda.current_stream()
+    capi.conv2d_fwd_host(op.desc, xh.data_ptr(), wh.data_ptr(), yh.data_ptr(), xd.data_ptr(), wd.data_ptr(),
+                         yd.data_ptr(), ws.data_ptr(), op.workspace_bytes, st.cuda_stream)
+    st.synchronize()
+    assert capi.conv2d_device_status(0) == 0
+    assert torch.equal(yh.view(torch.int16) if yh.element_size() == 2 else yh.view(torch.int32),
+                       ref.view(torch.int16) if ref.element_size() == 2 else ref.view(torch.int32))
