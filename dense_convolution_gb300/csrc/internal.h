@@ -46,8 +46,9 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Launch that may overlap the previous kernel of the stream (programmatic
 // dependent launch): the kernel can start while its predecessor finishes, and
 // must execute griddepcontrol.wait (pdl_wait) before touching that
-// predecessor's results.  Used for every kernel after the first one of a
-// conv2d_fwd call.
+// predecessor's results.  Used for every kernel of a conv2d_fwd call; the
+// first one waits before touching any memory (its predecessor may be any
+// kernel of the caller's) and signals its dependents only after that wait.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                                 Args... args) {

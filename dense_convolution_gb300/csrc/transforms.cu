@@ -402,6 +402,10 @@ __global__ void __launch_bounds__(256) pack_filter_tc_kernel(const uint16_t* __r
                                                              uint16_t* __restrict__ wq, int Ci, int Kh, int Kw,
                                                              int cdiv, int ck, int taps, int CP, int im2win) {
     __shared__ __align__(16) uint16_t fw[kPackSmemElems];
+    // First kernel of a call, launched as a programmatic dependent of whatever
+    // ran before on the stream: wait for it before touching memory, and only
+    // then let the transform behind this kernel start (it reads X at once).
+    pdl_wait();
     pdl_launch_dependents();
     const int co = blockIdx.x;
     const int KK = Kh * Kw, n = Ci * KK;
@@ -440,9 +444,8 @@ __global__ void __launch_bounds__(256) pack_filter_tc_kernel(const uint16_t* __r
 cudaError_t launch_pack_filter_tc(const void* w, void* wq, const conv2d_desc& d, bool im2win, cudaStream_t st) {
     if ((long long)d.Ci * d.Kh * d.Kw > kPackSmemElems) return cudaErrorInvalidValue;
     const int cdiv = d.Ci8 <= 16 ? d.Ci : d.Ci8;
-    pack_filter_tc_kernel<<<d.Co, 256, 0, st>>>(static_cast<const uint16_t*>(w), static_cast<uint16_t*>(wq), d.Ci,
-                                                d.Kh, d.Kw, cdiv, d.Ck, d.taps, d.CP, im2win ? 1 : 0);
-    return cudaGetLastError();
+    return launch_after(pack_filter_tc_kernel, dim3(d.Co), dim3(256), 0, st, static_cast<const uint16_t*>(w),
+                        static_cast<uint16_t*>(wq), d.Ci, d.Kh, d.Kw, cdiv, d.Ck, d.taps, d.CP, im2win ? 1 : 0);
 }
 
 // CUDA-core filter: wq[cb][ci][k][j] = w[cb*BCO + j][ci][k] (k = kh*Kw + kw),
@@ -451,6 +454,7 @@ cudaError_t launch_pack_filter_tc(const void* w, void* wq, const conv2d_desc& d,
 // (cb, ci): reads BCO runs of Kh*Kw floats, writes Kh*Kw*BCO floats in order.
 __global__ void __launch_bounds__(256) pack_filter_f32_kernel(const float* __restrict__ w, float* __restrict__ wq,
                                                               int Co, int Ci, int KK, int BCO) {
+    pdl_wait();                 // first kernel of a call: see pack_filter_tc_kernel
     pdl_launch_dependents();
     const int ci = blockIdx.x, cb = blockIdx.y;
     float* dst = wq + ((long long)cb * Ci + ci) * KK * BCO;
@@ -466,8 +470,8 @@ cudaError_t launch_pack_filter_f32(const float* w, float* wq, const conv2d_desc&
     const int BCO = 32 * d.cc_warps;
     const int ncb = (d.Co + BCO - 1) / BCO;
     if (ncb > 65535) return cudaErrorInvalidConfiguration;
-    pack_filter_f32_kernel<<<dim3(d.Ci, ncb), 256, 0, st>>>(w, wq, d.Co, d.Ci, d.Kh * d.Kw, BCO);
-    return cudaGetLastError();
+    return launch_after(pack_filter_f32_kernel, dim3(d.Ci, ncb), dim3(256), 0, st, w, wq, d.Co, d.Ci, d.Kh * d.Kw,
+                        BCO);
 }
 
 }  // namespace conv2d_gb300
