@@ -292,6 +292,10 @@ def run_gpu(args, rank, world):
         # its launches back to back on this stream, so its event pair gives the
         # kernel's average duration without the per-launch events' own cost.
         kms = ms
+    # A kernel cannot take longer than the whole call it is part of: a higher
+    # per-launch reading is the events' own cost or a clock drop between the
+    # two passes (seen under the power cap on the longest layers).
+    kms = min(kms, ms)
     ms = max_over_ranks(ms, world, dev)
 
     # End to end through the C ABI on host buffers (conv2d_fwd_host): pinned
