@@ -144,6 +144,20 @@ for _k in (1, 3, 5, 7, 9, 11):
     WORKLOADS[f"sweep_k{_k}"] = _sweep(_k)
 WORKLOADS["sweep_k3_s2"] = _sweep(3, 2)
 
+# The twelve layers of "Enabling Memory-efficient Im2win Convolution ...",
+# Table I (input Ci x Hi x Wi, filter Co x Hf x Wf with stride, no padding:
+# the table's output sizes are those of p = 0), at the batch of its Sec. IV-C
+# (Ni = 256).  The paper gives no value distributions: N(0, 1) inputs and
+# Kaiming-normal filters, as for the other layers.
+_CV = [  # Ci, H, W, Co, K, s
+    (3, 227, 227, 96, 11, 4), (3, 231, 231, 96, 11, 4), (3, 227, 227, 64, 7, 2), (64, 224, 224, 64, 7, 2),
+    (96, 24, 24, 256, 5, 1), (256, 12, 12, 512, 3, 1), (3, 224, 224, 64, 3, 1), (64, 112, 112, 128, 3, 1),
+    (64, 56, 56, 64, 3, 1), (128, 28, 28, 128, 3, 1), (256, 14, 14, 256, 3, 1), (512, 7, 7, 512, 3, 1),
+]
+for _i, (_ci, _h, _w, _co, _k, _s) in enumerate(_CV, start=1):
+    WORKLOADS[f"cv{_i}"] = Workload(f"cv{_i}", 256, _ci, _h, _w, _co, _k, _k, _s, 0, ("f32", "f16"), "n", "kaiming",
+                                    1100 + _i)
+
 
 def make_inputs(wl: Workload, dtype: str, N: int | None = None):
     """Draw X and W for a workload.  ``N`` may shrink the batch (the first N

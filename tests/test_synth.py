@@ -50,6 +50,11 @@ def test_workloads_table():
     assert w["vgg"].flops() == 2 * 64 * 512 * 28 * 28 * 512 * 9
     assert w["sweep_k3_s2"].out_hw() == (32, 32)
     assert w["sweep_k11"].pad == 5
+    # Table I of the im2win paper: output sizes of the twelve layers (p = 0).
+    outs = {1: 55, 2: 56, 3: 111, 4: 109, 5: 20, 6: 10, 7: 222, 8: 110, 9: 54, 10: 26, 11: 12, 12: 5}
+    for i, o in outs.items():
+        assert w[f"cv{i}"].out_hw() == (o, o), i
+        assert w[f"cv{i}"].N == 256
     d = synth.make_inputs(w["tiny"], "f32")
     assert d["X"].shape == (1, 16, 32, 32) and d["X"].dtype == np.float32
     small = synth.make_inputs(w["resnet_stage1"], "f16", N=2)
