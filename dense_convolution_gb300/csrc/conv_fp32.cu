@@ -3,7 +3,10 @@
 // Work split: a block computes one output row (n, ho), 64 consecutive output
 // columns and 32*warps output channels.  A lane owns an 8 x 8 register tile:
 // 8 consecutive output columns (lane % 8 picks which 8) x 8 output channels
-// (lane / 8 and the warp pick which 8).  Per (input channel, filter row,
+// (lane / 8 and the warp pick which 8).  Narrow maps (im2win mode, Wo <= 32)
+// give a block `rows` output rows instead: the 8 column groups of a lane row
+// split into rows x G, G = ceil(Wo / 8) groups per output row, so that up to
+// 8 rows of a 5-wide map share a block rather than 3 of its 64 columns.  Per (input channel, filter row,
 // filter column) a lane does 64 FMAs for two 16-byte filter loads, which the
 // 8 lanes of a channel group share as a broadcast.
 //
@@ -35,6 +38,9 @@ struct Fp32Params {
     int N, Ci, H, W, Co, Kh, Kw, s, p, Ho, Wo, Lp;
     int BCO, n_cb, n_wb, chunk, n_chunks;
     int pitch;          // floats per channel of staged input (im2win), or Kh*boxw (direct)
+    int rows, G;        // output rows per block; column groups (of 8) per row: 1 and 8 unless im2win and Wo <= 32
+    int rpitch;         // im2win: staged floats per output row (pitch = rows * rpitch)
+    int n_hb;           // row blocks per image (ceil(Ho / rows))
     int boxw;           // direct mode: staged row width (multiple of 4)
     int xs_floats;      // staged-input floats per stage (including read slack)
     int ws_floats;      // filter floats per stage
@@ -42,7 +48,7 @@ struct Fp32Params {
 
 constexpr int kCcCols = 64;    // output columns per block (8 lanes x 8)
 
-template <int KW, int S, bool IM2WIN>
+template <int KW, int S, bool IM2WIN, bool ROWS>
 __global__ void __launch_bounds__(128) conv_fp32_kernel(const Fp32Params prm,
                                                         const __grid_constant__ CUtensorMap xmap) {
     extern __shared__ uint8_t smem_raw[];
@@ -55,8 +61,9 @@ __global__ void __launch_bounds__(128) conv_fp32_kernel(const Fp32Params prm,
     long long b = blockIdx.x;
     const int cb = (int)(b % prm.n_cb); b /= prm.n_cb;
     const int wb = (int)(b % prm.n_wb); b /= prm.n_wb;
-    const int ho = (int)(b % prm.Ho);
-    const int n = (int)(b / prm.Ho);
+    const int ho0 = (int)(b % prm.n_hb) * (ROWS ? prm.rows : 1);   // first output row of the block
+    const int n = (int)(b / prm.n_hb);
+    const int rows_v = ROWS ? min(prm.rows, prm.Ho - ho0) : 1;     // rows of the block that exist
     const int Kh = prm.Kh;
     const int kw_n = KW > 0 ? KW : prm.Kw;
     const int sd = S > 0 ? S : prm.s;
@@ -96,20 +103,27 @@ __global__ void __launch_bounds__(128) conv_fp32_kernel(const Fp32Params prm,
         const uint32_t wbytes = (uint32_t)(nci * KK * prm.BCO * 4);
         if (IM2WIN) {
             const uint32_t xbytes = (uint32_t)((e1 - e0) * 4);
-            mbar_arrive_expect_tx(bar, wbytes + xbytes * nci);
-            for (int c = 0; c < nci; ++c) {
-                const float* src = prm.src + (((long long)n * prm.Ci + ci0 + c) * prm.Ho + ho) * prm.Lp + e0;
-                bulk_load(smem_addr(xs + c * prm.pitch), src, xbytes, bar);
-            }
+            mbar_arrive_expect_tx(bar, wbytes + xbytes * nci * rows_v);
+            for (int c = 0; c < nci; ++c)
+                for (int r = 0; r < rows_v; ++r) {
+                    const float* src =
+                        prm.src + (((long long)n * prm.Ci + ci0 + c) * prm.Ho + ho0 + r) * prm.Lp + e0;
+                    bulk_load(smem_addr(xs + c * prm.pitch + r * prm.rpitch), src, xbytes, bar);
+                }
         } else {
             const uint32_t xbytes = (uint32_t)(prm.boxw * Kh * prm.chunk * 4);
             mbar_arrive_expect_tx(bar, wbytes + xbytes);
-            tma_load_3d(smem_addr(xs), &xmap, bar, xbase, ho * sd - prm.p, n * prm.Ci + ci0);
+            tma_load_3d(smem_addr(xs), &xmap, bar, xbase, ho0 * sd - prm.p, n * prm.Ci + ci0);
         }
         bulk_load(smem_addr(ws), prm.wq + ((long long)cb * prm.Ci + ci0) * KK * prm.BCO, wbytes, bar);
     };
 
     const int lw = lane & 7, lc = lane >> 3;
+    // This lane's output row within the block (spare lanes, when rows * G < 8,
+    // work on the last row and store nothing) and column group within it.
+    const int G = ROWS ? prm.G : 8;
+    const int lrow = ROWS ? lw / G : 0, lg = lw - lrow * G;
+    const int lr = lrow < prm.rows ? lrow : prm.rows - 1;
     float acc[8][8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -117,7 +131,7 @@ __global__ void __launch_bounds__(128) conv_fp32_kernel(const Fp32Params prm,
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
     // Padded column of this lane's first window.
-    const int cl = (wo0 + 8 * lw) * sd;
+    const int cl = (wo0 + 8 * lg) * sd;
     constexpr int C = 8 * (S > 0 ? S : 1);
     constexpr int WIN = KW > 0 ? 7 * S + KW : 1;
 
@@ -142,7 +156,7 @@ __global__ void __launch_bounds__(128) conv_fp32_kernel(const Fp32Params prm,
                 // row[col * xstr] = padded input value at column col of this filter row.
                 const float* row;
                 int xstr;
-                if (IM2WIN) { row = xs + c * prm.pitch + kh - e0; xstr = Kh; }
+                if (IM2WIN) { row = xs + c * prm.pitch + (ROWS ? lr * prm.rpitch : 0) + kh - e0; xstr = Kh; }
                 else        { row = xs + (c * Kh + kh) * prm.boxw - prm.p - xbase; xstr = 1; }
                 const float* wr = ws + ((c * Kh + kh) * kw_n) * prm.BCO + warp * 32 + lc * 8;
                 if constexpr (KW > 0) {
@@ -152,7 +166,7 @@ __global__ void __launch_bounds__(128) conv_fp32_kernel(const Fp32Params prm,
 #pragma unroll
                     for (int j = C; j < WIN; ++j) {
                         float t = __shfl_down_sync(0xffffffffu, v[j % C], j / C);
-                        if (lw + j / C >= 8) t = row[(cl + j) * xstr];
+                        if (lg + j / C >= G) t = row[(cl + j) * xstr];   // the neighbour is in another row
                         v[j] = t;
                     }
 #pragma unroll
@@ -189,7 +203,9 @@ __global__ void __launch_bounds__(128) conv_fp32_kernel(const Fp32Params prm,
     // Store: each channel row gets 8 consecutive columns (two 16-byte stores
     // when the row is 16-byte aligned and all 8 columns are outputs).
     const int co_base = cb * prm.BCO + warp * 32 + lc * 8;
-    const int wt = wo0 + 8 * lw;
+    if (ROWS && lrow >= rows_v) return;                       // a spare lane or a row past Ho
+    const int ho = ho0 + lrow;
+    const int wt = wo0 + 8 * lg;
     const bool vec = (prm.Wo % 4) == 0 && wt + 8 <= prm.Wo;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -215,10 +231,10 @@ typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_
                                     CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 void* driver_entry(const char* name);   // conv_tc.cu
 
-template <int KW, int S, bool IM2WIN>
+template <int KW, int S, bool IM2WIN, bool ROWS = false>
 static cudaError_t launch_fp32_inst(const Fp32Params& prm, const CUtensorMap& map, int threads, size_t smem,
                                     long long blocks, cudaStream_t st) {
-    auto kern = conv_fp32_kernel<KW, S, IM2WIN>;
+    auto kern = conv_fp32_kernel<KW, S, IM2WIN, ROWS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_after(kern, dim3((unsigned)blocks), dim3(threads), smem, st, prm, map);
@@ -227,6 +243,14 @@ static cudaError_t launch_fp32_inst(const Fp32Params& prm, const CUtensorMap& ma
 template <bool IM2WIN>
 static cudaError_t launch_fp32_shape(const conv2d_desc& d, const Fp32Params& prm, const CUtensorMap& map,
                                      int threads, size_t smem, long long blocks, cudaStream_t st) {
+    if constexpr (IM2WIN) {
+        if (prm.rows > 1) {   // narrow maps: several output rows per block
+            if (d.Kw == 3 && d.s == 1) return launch_fp32_inst<3, 1, true, true>(prm, map, threads, smem, blocks, st);
+            if (d.Kw == 5 && d.s == 1) return launch_fp32_inst<5, 1, true, true>(prm, map, threads, smem, blocks, st);
+            if (d.Kw == 3 && d.s == 2) return launch_fp32_inst<3, 2, true, true>(prm, map, threads, smem, blocks, st);
+            return launch_fp32_inst<0, 0, true, true>(prm, map, threads, smem, blocks, st);
+        }
+    }
 #define CONV2D_FP32_CASE(KW_, S_) \
     if (d.Kw == KW_ && d.s == S_) return launch_fp32_inst<KW_, S_, IM2WIN>(prm, map, threads, smem, blocks, st);
     CONV2D_FP32_CASE(1, 1)
@@ -250,6 +274,13 @@ conv2d_status launch_conv_fp32(const conv2d_desc& d, const float* src, const flo
     prm.BCO = 32 * d.cc_warps;
     prm.n_cb = (d.Co + prm.BCO - 1) / prm.BCO;
     prm.n_wb = (d.Wo + kCcCols - 1) / kCcCols;
+    prm.rows = 1;
+    prm.G = 8;
+    if (im2win && d.Wo <= 32) {
+        prm.G = (d.Wo + 7) / 8;
+        prm.rows = 8 / prm.G;
+    }
+    prm.n_hb = (d.Ho + prm.rows - 1) / prm.rows;
     // Staged input per channel, with slack so that lanes past Wo read inside the buffer.
     const int span = (kCcCols - 1) * d.s + d.Kw;          // padded columns 64 windows touch
     const int slack = kCcCols * d.s + d.Kw + 8;
@@ -257,6 +288,12 @@ conv2d_status launch_conv_fp32(const conv2d_desc& d, const float* src, const flo
     if (im2win) {
         // Staged range [e0, e1) is rounded out to 16 bytes on both ends (+6 at most).
         prm.pitch = ((span * d.Kh + 8) + 3) & ~3;
+        prm.rpitch = prm.pitch;
+        if (prm.rows > 1) {
+            // A lane group reads at most ((8G-1)*s + Kw)*Kh floats from its row's start.
+            prm.rpitch = ((((8 * prm.G - 1) * d.s + d.Kw) * d.Kh + 8) + 3) & ~3;
+            prm.pitch = prm.rows * prm.rpitch;
+        }
         per_ci_x = prm.pitch;
         prm.boxw = 0;
     } else {
@@ -295,7 +332,7 @@ conv2d_status launch_conv_fp32(const conv2d_desc& d, const float* src, const flo
                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
     }
-    const long long blocks = (long long)d.N * d.Ho * prm.n_wb * prm.n_cb;
+    const long long blocks = (long long)d.N * prm.n_hb * prm.n_wb * prm.n_cb;
     if (blocks > 0x7fffffffLL) return CONV2D_ERR_UNSUPPORTED;
     const int threads = 32 * d.cc_warps;
     cudaError_t e = im2win ? launch_fp32_shape<true>(d, prm, map, threads, smem, blocks, st)
