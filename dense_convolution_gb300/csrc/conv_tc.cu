@@ -34,16 +34,18 @@
 // from the caller's filter) and N = 128 pixels (X, read as [ci][p] rows:
 // the "MN-major" operand layout, two 64-pixel boxes per chunk), so each
 // accumulator lane is one output channel and its columns are consecutive
-// pixels: the epilogue stores them straight from registers.
+// pixels: the epilogue rounds them into a swizzled shared-memory box that one
+// TMA store writes to Y.
 //
-// Warp roles (192 threads; one CTA per SM, two for tiles up to 128 channels wide; persistent over tiles):
-//   warp 0     TMA producer (one elected lane), STAGES-deep shared-memory ring
-//   warp 1     TMEM allocation + MMA issue (one lane): 4 x (128xBNx16) per stage
-//   warps 2-5  epilogue: tcgen05.ld of their 32-lane TMEM quarter, round to the
-//              output type, transpose through shared memory, store NCHW
-// Two TMEM accumulators let the epilogue of tile i overlap the MMAs of i+1
-// (with 256-wide tiles and two CTAs per SM, one each: the other CTA's MMAs
-// fill the gap).
+// Warp roles (352 threads; one persistent CTA per SM):
+//   warp 0      TMA producer (one lane), STAGES-deep shared-memory ring
+//   warps 1-2   MMA issue (one lane each; warp 1 also allocates TMEM): tile i
+//               of a pair of tiles into its own TMEM accumulators
+//   warps 3-10  two epilogue groups of four warps, group e draining issuer e:
+//               tcgen05.ld of their 32-lane TMEM quarter, round to the output
+//               type, transpose through shared memory, store NCHW
+// Two TMEM accumulators per issuer (when TMEM holds them) let the epilogue of
+// one tile overlap the MMAs of the next.
 // Every wait is bounded (ptx.cuh); on a timeout the CTA drains what it issued,
 // frees its TMEM and exits with the device status word set.
 #include <cuda.h>
