@@ -64,9 +64,9 @@ struct TcParams {
     int n_groups;       // tile groups
     int n_m_tiles;      // 128-pixel tiles (groups past the end are padded with empty tiles)
     int n_cchunks, CP, Kw, s, p;
-    int amode;          // A source: 0 implicit, 1 im2win, 2 padded (1 and 2 run kernel MODE 1)
+    int amode;          // A source: 0 implicit, 1 im2win, 2 padded (1 and 2 run kernel MODE 1), 3 1x1 GEMM
     int N, Wq, HpWq;    // grid modes: batch, row pitch and image pitch of the virtual pixel grid
-    int vec_store;      // MODE 0: Ho*Wo % 8 == 0 (16-byte stores); MODE 1: Wo % 4 == 0 (8-byte stores)
+    int vec_store;      // MODE 0: Ho*Wo % 8 == 0 (16-byte stores); MODE 1: Wo % 4 == 0 (8-byte stores); MODE 3 unused
     int kpb;            // taps per pipeline stage (halo mode), else 1
     int stages;         // depth of the shared-memory ring (<= kMaxStages)
     int stage_bytes;    // `group` A regions (+ the stage's B chunks unless B is resident)
