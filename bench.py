@@ -8,9 +8,9 @@ per the chosen algorithm), the contraction kernel and its epilogue.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--dtype DT]
                   [--algo A] [--impl reference]
 
-Prints ONE JSON line (rank 0).  Default workload: the ResNet stage-1 layer
-(N=32, Cin=64, 56x56, Cout=64, 3x3, stride 1, pad 1) in fp16 with fp32
-accumulation.  Timing: CUDA events on the launching stream around the whole
+Prints ONE JSON line (rank 0).  Default workload: the VGG-style layer
+(N=64, Cin=512, 28x28, Cout=512, 3x3, stride 1, pad 1; the largest of the
+workloads and a compute-bound 3x3 layer) in fp16 with fp32 accumulation.  Timing: CUDA events on the launching stream around the whole
 run of K back-to-back steps (per-step event pairs are snapped to a ~2 us
 completion tick on this platform and would bias short steps), each step on
 the next of several rotating input/filter/output/workspace sets whose total
@@ -173,7 +173,8 @@ def job_tflops(flops_per_rank: float, world: int, ms: float) -> float:
 
 def _workload(args):
     wl = synth.WORKLOADS[args.workload]
-    dtype = args.dtype or wl.dtypes[0]
+    # fp16 where the workload has it (the dtype of the tensor-peak target), else its first dtype.
+    dtype = args.dtype or ("f16" if "f16" in wl.dtypes else wl.dtypes[0])
     return wl, dtype
 
 
@@ -410,7 +411,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="resnet_stage1", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="vgg", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--dtype", default=None, choices=list(synth.DTYPES))
     ap.add_argument("--algo", default="auto")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
@@ -421,6 +422,10 @@ def main():
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.gpus != world:
+        # One process per GPU: N GPUs need N ranks from the launcher.
+        sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; launch N ranks with "
+                 f"python -m torch.distributed.run --nproc-per-node {args.gpus} bench.py --gpus {args.gpus}")
     if args.impl != "reference":
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))

@@ -23,9 +23,8 @@ LAYOUTS = {"nchw": 0, "nhwc": 1}
 
 EXPORTED = ("conv2d_desc_create", "conv2d_desc_set_input_layout", "conv2d_desc_destroy", "conv2d_out_dims",
             "conv2d_workspace_size", "conv2d_get_algo", "conv2d_fwd", "conv2d_fwd_profiled", "conv2d_fwd_host",
-            "conv2d_launches_per_call", "conv2d_fwd_static_workspace", "conv2d_device_status",
-            "conv2d_status_string")
-STATIC_WORKSPACE_BYTES = 64 << 20
+            "conv2d_launches_per_call", "conv2d_fwd_static_workspace", "conv2d_static_workspace_bytes",
+            "conv2d_device_status", "conv2d_status_string")
 
 
 class Conv2dError(RuntimeError):
@@ -57,6 +56,7 @@ def load(path: str = LIB_PATH):
     L.conv2d_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, c_size, vp]
     L.conv2d_launches_per_call.argtypes = [vp, ctypes.POINTER(c_int)]
     L.conv2d_fwd_static_workspace.argtypes = [vp, vp, vp, vp, vp]
+    L.conv2d_static_workspace_bytes.argtypes = [ctypes.POINTER(c_size)]
     L.conv2d_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     L.conv2d_status_string.argtypes = [c_int]
     L.conv2d_status_string.restype = ctypes.c_char_p
@@ -137,8 +137,22 @@ def conv2d_launches_per_call(desc: int) -> int:
 def conv2d_fwd_static_workspace(desc: int, x: int, w: int, y: int, stream: int = 0):
     """conv2d_fwd without a workspace argument, for callers that cannot
     allocate device memory: scratch comes from the library's built-in
-    64 MiB device array (shared by all calls; overlapping calls race)."""
+    device array of conv2d_static_workspace_bytes() bytes (shared by all
+    calls; overlapping calls race)."""
     _check(load().conv2d_fwd_static_workspace(desc, x, w, y, stream or None), "conv2d_fwd_static_workspace")
+
+
+def conv2d_static_workspace_bytes() -> int:
+    b = ctypes.c_size_t()
+    _check(load().conv2d_static_workspace_bytes(ctypes.byref(b)), "conv2d_static_workspace_bytes")
+    return b.value
+
+
+def __getattr__(name):
+    # STATIC_WORKSPACE_BYTES is read from the library, so it cannot drift from the C side.
+    if name == "STATIC_WORKSPACE_BYTES":
+        return conv2d_static_workspace_bytes()
+    raise AttributeError(name)
 
 
 def conv2d_device_status(stream: int = 0) -> int:

@@ -13,7 +13,8 @@
 // it until the process exits.  Host code cannot use the array's name as a
 // device address (on the host it names a stand-in object), so the device
 // address is looked up once per device with cudaGetSymbolAddress, on the
-// first call made while that device is current, and cached.
+// first call made while that device is current, and cached for the life of
+// the process (valid while the device's primary context is not reset).
 #include <mutex>
 
 #include "internal.h"
@@ -62,4 +63,10 @@ CONV2D_API conv2d_status conv2d_fwd_static_workspace(conv2d_desc_t d, const void
     // Every byte the kernels read from the workspace is written earlier in the
     // same call, so leftovers from a previous call need no clearing.
     return conv2d_fwd(d, x, w, y, ws, need > 0 ? kStaticWorkspaceBytes : 0, stream);
+}
+
+CONV2D_API conv2d_status conv2d_static_workspace_bytes(size_t* bytes) {
+    if (!bytes) return CONV2D_ERR_NULL_PTR;
+    *bytes = kStaticWorkspaceBytes;
+    return CONV2D_OK;
 }

@@ -197,6 +197,9 @@ conv2d_status conv2d_launches_per_call(conv2d_desc_t d, int *launches);
  *   held until the process exits.  The call allocates nothing.
  *   The first call on each device (with that device current) looks up the
  *   array's device address; make that first call before any stream capture.
+ *   The address is then kept for the life of the process, which assumes the
+ *   device's primary context is never destroyed (no cudaDeviceReset between
+ *   calls): a reset context may load the array at another address.
  *   Every call uses the same array and it keeps the previous call's contents
  *   (nothing in it needs to start at zero).  Calls whose kernels overlap on
  *   the GPU (other streams, other host threads) race on it: serialise them.
@@ -205,6 +208,11 @@ conv2d_status conv2d_launches_per_call(conv2d_desc_t d, int *launches);
  * when the address lookup fails. */
 conv2d_status conv2d_fwd_static_workspace(conv2d_desc_t d, const void *x, const void *w, void *y,
                                           void *stream);
+
+/* Size in bytes of the array conv2d_fwd_static_workspace uses
+ * (CONV2D_STATIC_WORKSPACE_BYTES of the library as built), for bindings that
+ * cannot read the macro.  Errors: NULL_PTR. */
+conv2d_status conv2d_static_workspace_bytes(size_t *bytes);
 
 /* Read and clear the library's device status word on the current device
  * (synchronises `stream`).  Returns CONV2D_OK when every kernel since the

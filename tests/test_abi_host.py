@@ -216,3 +216,9 @@ def test_fwd_host_argument_checks_before_copy(capi):
         assert e.value.status == capi.ERR_WORKSPACE_TOO_SMALL
     finally:
         capi.conv2d_desc_destroy(d)
+
+
+def test_static_workspace_size_getter(capi):
+    # The binding reads the size from the library, which reports the header's value.
+    assert capi.conv2d_static_workspace_bytes() == 64 << 20
+    assert capi.STATIC_WORKSPACE_BYTES == 64 << 20
