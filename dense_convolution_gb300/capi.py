@@ -24,7 +24,7 @@ LAYOUTS = {"nchw": 0, "nhwc": 1}
 EXPORTED = ("conv2d_desc_create", "conv2d_desc_set_input_layout", "conv2d_desc_destroy", "conv2d_out_dims",
             "conv2d_workspace_size", "conv2d_get_algo", "conv2d_fwd", "conv2d_fwd_profiled", "conv2d_fwd_host",
             "conv2d_launches_per_call", "conv2d_fwd_static_workspace", "conv2d_static_workspace_bytes",
-            "conv2d_device_status", "conv2d_status_string")
+            "conv2d_set_wait_limit", "conv2d_device_status", "conv2d_status_string")
 
 
 class Conv2dError(RuntimeError):
@@ -57,6 +57,7 @@ def load(path: str = LIB_PATH):
     L.conv2d_launches_per_call.argtypes = [vp, ctypes.POINTER(c_int)]
     L.conv2d_fwd_static_workspace.argtypes = [vp, vp, vp, vp, vp]
     L.conv2d_static_workspace_bytes.argtypes = [ctypes.POINTER(c_size)]
+    L.conv2d_set_wait_limit.argtypes = [ctypes.c_uint64, vp]
     L.conv2d_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     L.conv2d_status_string.argtypes = [c_int]
     L.conv2d_status_string.restype = ctypes.c_char_p
@@ -153,6 +154,11 @@ def __getattr__(name):
     if name == "STATIC_WORKSPACE_BYTES":
         return conv2d_static_workspace_bytes()
     raise AttributeError(name)
+
+
+def conv2d_set_wait_limit(ns: int, stream: int = 0):
+    """Limit of each kernel pipeline wait in ns (0 = the default 2 s); tests only."""
+    _check(load().conv2d_set_wait_limit(int(ns), stream or None), "conv2d_set_wait_limit")
 
 
 def conv2d_device_status(stream: int = 0) -> int:

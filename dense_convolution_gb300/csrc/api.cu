@@ -362,6 +362,13 @@ CONV2D_API conv2d_status conv2d_device_status(void* stream, uint32_t* code_out) 
     return (a | b) ? CONV2D_ERR_DEVICE_TIMEOUT : CONV2D_OK;
 }
 
+CONV2D_API conv2d_status conv2d_set_wait_limit(uint64_t ns, void* stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (wait_limit_set_tc(st, ns) != cudaSuccess || wait_limit_set_fp32(st, ns) != cudaSuccess)
+        return CONV2D_ERR_CUDA;
+    return CONV2D_OK;
+}
+
 CONV2D_API const char* conv2d_status_string(conv2d_status s) {
     switch (s) {
         case CONV2D_OK: return "ok";

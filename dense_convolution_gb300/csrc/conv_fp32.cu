@@ -139,15 +139,11 @@ __global__ void __launch_bounds__(128) conv_fp32_kernel(const Fp32Params prm,
     bool ok = true;
     for (int k = 0; k < prm.n_chunks; ++k) {
         if (tid == 0 && k + 1 < prm.n_chunks) issue(k + 1);
-        if (!mbar_wait(smem_addr(&bars[k & 1]), (k >> 1) & 1, &abort_flag)) {
-            // Let a copy issued for the next chunk land before the CTA exits.
-            if (tid == 0 && k + 1 < prm.n_chunks) {
-                int dummy = 0;
-                mbar_wait(smem_addr(&bars[(k + 1) & 1]), ((k + 1) >> 1) & 1, &dummy);
-            }
-            ok = false;
-            break;
-        }
+        // A thread whose wait gives up (or sees another's abort) skips the
+        // chunk but still meets the barrier at the end of the iteration; the
+        // abort flag, set before that barrier, is then read by all threads
+        // alike, so the block leaves the loop together.
+        if (mbar_wait(smem_addr(&bars[k & 1]), (k >> 1) & 1, &abort_flag)) {
         const float* xs = smem + (k & 1) * stage_floats;
         const float* ws = xs + prm.xs_floats;
         const int nci = min(prm.chunk, prm.Ci - k * prm.chunk);
@@ -196,7 +192,18 @@ __global__ void __launch_bounds__(128) conv_fp32_kernel(const Fp32Params prm,
                 }
             }
         }
+        }   // chunk k staged
         __syncthreads();
+        if (*reinterpret_cast<volatile int*>(&abort_flag)) {
+            // Let the copies of this chunk and of the next one (issued before
+            // this chunk's wait) land before the CTA exits.
+            if (tid == 0) {
+                mbar_drain_wait(smem_addr(&bars[k & 1]), (k >> 1) & 1);
+                if (k + 1 < prm.n_chunks) mbar_drain_wait(smem_addr(&bars[(k + 1) & 1]), ((k + 1) >> 1) & 1);
+            }
+            ok = false;
+            break;
+        }
     }
     if (!ok) return;
 
@@ -225,6 +232,7 @@ __global__ void __launch_bounds__(128) conv_fp32_kernel(const Fp32Params prm,
 
 // ---------------------------------------------------------------- host side
 cudaError_t status_read_clear_fp32(cudaStream_t st, uint32_t* out) { return status_read_clear(st, out); }
+cudaError_t wait_limit_set_fp32(cudaStream_t st, uint64_t ns) { return wait_limit_set(st, ns); }
 
 typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                     const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,

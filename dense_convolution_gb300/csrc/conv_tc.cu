@@ -265,18 +265,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
             }
             if (!ok) {
                 // Let every copy already issued land before the CTA can exit.
-                int dummy = 0;
                 int st = stage;
                 uint32_t ph = phase;
                 for (int i = 0; i < S && i < issued; ++i) {
                     if (--st < 0) { st = S - 1; ph ^= 1; }
-                    mbar_wait(full_bar(st), ph, &dummy);
+                    mbar_drain_wait(full_bar(st), ph);
                 }
             }
-            if (prm.b_res) {
-                int dummy = 0;
-                mbar_wait(bres_bar, 0, &dummy);
-            }
+            if (prm.b_res) mbar_drain_wait(bres_bar, 0);
         }
     } else if (warp <= kIssuers) {
         // ------------------------------------------------------------ MMA issuers
@@ -337,9 +333,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
                 if (++acc == nacc) { acc = 0; acc_phase ^= 1; }
             }
             if (!ok && issued_any) {
-                int dummy = 0;
                 umma_commit(drain_bar(is));
-                mbar_wait(drain_bar(is), 0, &dummy);
+                mbar_drain_wait(drain_bar(is), 0);
             }
         }
     } else {
@@ -524,6 +519,7 @@ void* driver_entry(const char* name) {
 }
 
 cudaError_t status_read_clear_tc(cudaStream_t st, uint32_t* out) { return status_read_clear(st, out); }
+cudaError_t wait_limit_set_tc(cudaStream_t st, uint64_t ns) { return wait_limit_set(st, ns); }
 
 int device_sm_count() {
     static int cached[64] = {0};

@@ -85,5 +85,7 @@ int device_sm_count();
 void* driver_entry(const char* name);
 cudaError_t status_read_clear_tc(cudaStream_t st, uint32_t* out);
 cudaError_t status_read_clear_fp32(cudaStream_t st, uint32_t* out);
+cudaError_t wait_limit_set_tc(cudaStream_t st, uint64_t ns);
+cudaError_t wait_limit_set_fp32(cudaStream_t st, uint64_t ns);
 
 }  // namespace conv2d_gb300

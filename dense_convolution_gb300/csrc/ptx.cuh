@@ -20,6 +20,22 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait, then give up
 // device code is needed); each unit exports a host reader.
 static __device__ uint32_t g_device_status = 0;
 
+// Limit of the pipeline waits (mbar_wait), default kWaitLimitNs.  The host can
+// lower it (wait_limit_set) so that a test sees waits give up; the waits that
+// let in-flight copies and MMAs finish before a CTA exits (mbar_drain_wait)
+// always use kWaitLimitNs.
+static __constant__ uint64_t g_wait_limit_ns = kWaitLimitNs;
+
+// Set this translation unit's pipeline-wait limit for kernels launched on
+// `st` after this call (0 restores the default).
+static inline cudaError_t wait_limit_set(cudaStream_t st, uint64_t ns) {
+    static uint64_t v;   // the copy reads the source when the stream reaches it
+    v = ns ? ns : kWaitLimitNs;
+    cudaError_t e = cudaMemcpyToSymbolAsync(g_wait_limit_ns, &v, sizeof(v), 0, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    return e;
+}
+
 // Read and clear this translation unit's status word (synchronises `st`).
 static inline cudaError_t status_read_clear(cudaStream_t st, uint32_t* out) {
     uint32_t v = 0, z = 0;
@@ -101,15 +117,31 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
+    const uint64_t limit = g_wait_limit_ns;
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 0) {
             if (*abort) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit) {
                 atomicOr(&g_device_status, kStatusTimeout);
                 *abort = 1;
                 return false;
             }
+        }
+    }
+}
+
+// Wait used after an abort, for copies or MMAs this CTA already issued to
+// complete before it exits: no abort test, fixed limit kWaitLimitNs (then the
+// status word is set and the wait gives up).
+__device__ __forceinline__ bool mbar_drain_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(&g_device_status, kStatusTimeout);
+            return false;
         }
     }
 }

@@ -221,6 +221,17 @@ conv2d_status conv2d_static_workspace_bytes(size_t *bytes);
  * readback failed.  `*code_out` (may be NULL) receives the raw status bits. */
 conv2d_status conv2d_device_status(void *stream, uint32_t *code_out);
 
+/* Limit, in nanoseconds, of each pipeline wait of the library's kernels on
+ * the current device (default 2 s; ns = 0 restores the default), for
+ * kernels launched on `stream` after this call returns (the call
+ * synchronises `stream`).  A wait that runs past the limit gives up: the
+ * kernel lets the copies and MMAs it already issued finish, exits, and sets
+ * the bit conv2d_device_status reports as CONV2D_ERR_DEVICE_TIMEOUT (that
+ * call's output is invalid).  A tiny limit makes ordinary waits give up, so
+ * a test can check this path without any wait that never ends.  Not for
+ * production use.  The paper has no counterpart.  Errors: CUDA. */
+conv2d_status conv2d_set_wait_limit(uint64_t ns, void *stream);
+
 /* Static string for a status code (never NULL). */
 const char *conv2d_status_string(conv2d_status s);
 

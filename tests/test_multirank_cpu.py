@@ -57,7 +57,7 @@ def test_reference_arm_prints_on_rank0_only():
     port = _free_port()
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
-           "--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "3"]
+           "--gpus", "2", "--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "3"]
     out = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT,
                          env={**os.environ, "OMP_NUM_THREADS": "1"})
     assert out.returncode == 0, out.stderr[-2000:]
@@ -65,3 +65,13 @@ def test_reference_arm_prints_on_rank0_only():
     assert len(lines) == 1
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["value"] > 0
+
+
+def test_gpus_flag_must_match_world_size():
+    """--gpus N without N ranks is refused (exit code non-zero) instead of
+    silently measuring one GPU."""
+    env = {**os.environ, "WORLD_SIZE": "1", "RANK": "0"}
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--impl", "reference",
+                          "--workload", "tiny", "--steps", "1"], capture_output=True, text=True, timeout=300,
+                         cwd=ROOT, env=env)
+    assert out.returncode != 0 and "WORLD_SIZE" in out.stderr
