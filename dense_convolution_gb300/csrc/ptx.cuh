@@ -115,9 +115,22 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // *abort so that the other warps of the CTA stop too.  Returns false when the
 // wait did not complete.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     const uint64_t limit = g_wait_limit_ns;
+    if (limit < kWaitLimitNs) {
+        // A lowered limit: poll without suspending and test the clock every
+        // time, so that even a wait of a few microseconds can expire.
+        for (;;) {
+            if (mbar_test_wait(bar, parity)) return true;
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > limit) {
+                atomicOr(&g_device_status, kStatusTimeout);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 0) {

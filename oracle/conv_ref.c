@@ -25,7 +25,9 @@
  *     H_out = (H + 2p - K_H) // s + 1 (floor) and symmetric zero padding.
  *
  * Alongside Y every direct routine returns S[n,co,ho,wo] = sum |x*w| over the
- * same terms; parity is measured as |y_gpu - Y| / S.
+ * same terms; parity is measured as |y_gpu - Y| / S.  An optional bias
+ * (oracle_add_bias, the `Y_col += bias` of "Unifying Convolutions and GEMM",
+ * Sec. 6) adds b[co] to Y and |b[co]| to S.
  *
  * Parity pins (tests/test_oracle_pins.py) tie each routine to something other
  * than itself: brute force in Python, scipy's 2-D correlation, float64
@@ -243,5 +245,29 @@ int oracle_im2win_conv(const double *Xw, const double *Wt, double *Y,
                     }
                     Y[((n * Co + co) * Ho + m) * Wo + q] = acc;
                 }
+    return 0;
+}
+
+/* Bias of the PyTorch listing of "Unifying Convolutions and GEMM", Sec. 6
+ * (manual_im2col_conv(x, weights, bias, ...), `Y_col += bias`): one value per
+ * output channel, added to every output of that channel after the sum:
+ *
+ *   Y[n,co,ho,wo] += b[co],   S[n,co,ho,wo] += |b[co]|
+ *
+ * so that the parity measure |y - Y| / S also covers the bias term.  Y and S
+ * are whole NCHW outputs of N x Co x Ho x Wo; S may be NULL. */
+int oracle_add_bias(double *Y, double *S, const double *b, int N, int Co, int Ho, int Wo)
+{
+    if (N < 0 || Co < 1 || Ho < 1 || Wo < 1) return -1;
+    const int64_t plane = (int64_t)Ho * Wo;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t co = 0; co < Co; ++co) {
+            double *y = Y + (n * Co + co) * plane;
+            double *sa = S ? S + (n * Co + co) * plane : NULL;
+            for (int64_t i = 0; i < plane; ++i) {
+                y[i] += b[co];
+                if (sa) sa[i] += fabs(b[co]);
+            }
+        }
     return 0;
 }

@@ -60,9 +60,10 @@ def lib():
             L.oracle_conv2d_im2col.argtypes = [dp, dp, dp, dp] + [ci] * 9
             L.oracle_im2win_transform.argtypes = [dp, dp] + [ci] * 8
             L.oracle_im2win_conv.argtypes = [dp, dp, dp] + [ci] * 9
+            L.oracle_add_bias.argtypes = [dp, dp, dp] + [ci] * 4
             for f in ("oracle_out_dims", "oracle_conv2d_direct_slice", "oracle_conv2d_direct",
                       "oracle_conv2d_points", "oracle_im2col", "oracle_conv2d_im2col",
-                      "oracle_im2win_transform", "oracle_im2win_conv"):
+                      "oracle_im2win_transform", "oracle_im2win_conv", "oracle_add_bias"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -177,6 +178,19 @@ def im2win_conv(Xw, Wt, H, W, stride=1, pad=0):
     assert lib().oracle_im2win_conv(_p(Xw), _p(Wt), _p(Y),
                                     N, Ci, H, W, Co, Kh, Kw, stride, pad) == 0
     return Y
+
+
+def add_bias(Y, S, b):
+    """In place: Y[n, co] += b[co] and S[n, co] += |b[co]| ("Unifying
+    Convolutions and GEMM", Sec. 6 listing, `Y_col += bias`).  Y and S are
+    C-contiguous float64 NCHW arrays (S may be None)."""
+    b = _f64(b).ravel()
+    N, Co, Ho, Wo = Y.shape
+    assert b.shape[0] == Co and Y.flags.c_contiguous and Y.dtype == np.float64
+    if S is not None:
+        assert S.shape == Y.shape and S.flags.c_contiguous and S.dtype == np.float64
+    assert lib().oracle_add_bias(_p(Y), _p(S) if S is not None else None, _p(b), N, Co, Ho, Wo) == 0
+    return Y, S
 
 
 def parity_error(y_test, y_ref, s_ref):

@@ -434,3 +434,84 @@ def test_pins_catch_planted_mistakes(tmp_path, oracle):
         so = tmp_path / f"m{i}.so"
         subprocess.run(["gcc", "-O1", "-fPIC", "-shared", str(mut), "-o", str(so), "-lm"], check=True)
         assert not _pins_pass(str(so)), f"mutation {i} not caught: {b}"
+
+
+# --------------------------------------------------------------- bias ("Unifying Convolutions and GEMM", Sec. 6)
+
+def _bias_closed_form_ok(add_bias):
+    """All-ones X and W plus a bias: Y = Ci * r(ho) * c(wo) + b[co] and
+    S = Ci * r(ho) * c(wo) + |b[co]| (r, c = filter rows / columns inside the
+    image), with distinct signed biases per channel and two images."""
+    import ctypes  # noqa: F401
+    N, C, H, W, Co, Kh, Kw, s, p = 2, 3, 6, 7, 4, 3, 3, 1, 1
+    from oracle import ref
+    Y, S = ref.conv2d(np.ones((N, C, H, W)), np.ones((Co, C, Kh, Kw)), s, p)
+    b = np.array([0.5, -2.25, 3.0, -0.125])
+    add_bias(Y, S, b)
+    Ho, Wo = Y.shape[2:]
+    for n in range(N):
+        for co in range(Co):
+            for ho in range(Ho):
+                r = len([kh for kh in range(Kh) if 0 <= ho * s + kh - p < H])
+                for wo in range(Wo):
+                    c = len([kw for kw in range(Kw) if 0 <= wo * s + kw - p < W])
+                    if Y[n, co, ho, wo] != C * r * c + b[co] or S[n, co, ho, wo] != C * r * c + abs(b[co]):
+                        return False
+    return True
+
+
+def test_bias_all_ones_closed_form(oracle):
+    assert _bias_closed_form_ok(oracle.add_bias)
+
+
+def test_bias_zero_filter_gives_bias(oracle):
+    b = np.array([1.5, -4.0, 0.0])
+    Y, S = oracle.conv2d(np.ones((2, 2, 5, 5)), np.zeros((3, 2, 3, 3)), 1, 1)
+    oracle.add_bias(Y, S, b)
+    assert np.array_equal(Y, np.broadcast_to(b[None, :, None, None], Y.shape))
+    assert np.array_equal(S, np.abs(Y))
+
+
+def test_bias_vs_torch(oracle):
+    import torch
+    import torch.nn.functional as F
+    r = np.random.default_rng(31)
+    X = r.normal(size=(3, 5, 9, 8))
+    Wt = r.normal(size=(6, 5, 3, 2))
+    b = r.normal(size=6)
+    Y, S = oracle.conv2d(X, Wt, 2, 1)
+    oracle.add_bias(Y, S, b)
+    ref = F.conv2d(torch.from_numpy(X), torch.from_numpy(Wt), torch.from_numpy(b), stride=2, padding=1).numpy()
+    assert np.max(np.abs(Y - ref)) < 1e-12
+
+
+_BIAS_MUTATIONS = [
+    ("y[i] += b[co];", "y[i] += b[n];"),                       # bias indexed by image
+    ("y[i] += b[co];", "y[i] -= b[co];"),                      # wrong sign
+    ("if (sa) sa[i] += fabs(b[co]);", "if (sa) sa[i] += b[co];"),   # signed |b| in S
+    ("for (int64_t co = 0; co < Co; ++co) {\n            double *y",
+     "for (int64_t co = 0; co + 1 < Co; ++co) {\n            double *y"),   # last channel skipped
+]
+
+
+def test_bias_pins_catch_planted_mistakes(tmp_path, oracle):
+    import ctypes
+    import subprocess
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "conv_ref.c")).read()
+    dp = ctypes.POINTER(ctypes.c_double)
+    for i, (a, b) in enumerate(_BIAS_MUTATIONS):
+        assert a in src, a
+        mut = tmp_path / f"b{i}.c"
+        mut.write_text(src.replace(a, b, 1))
+        so = tmp_path / f"b{i}.so"
+        subprocess.run(["gcc", "-O1", "-fPIC", "-shared", str(mut), "-o", str(so), "-lm"], check=True)
+        L = ctypes.CDLL(str(so))
+        L.oracle_add_bias.argtypes = [dp, dp, dp] + [ctypes.c_int] * 4
+        L.oracle_add_bias.restype = ctypes.c_int
+
+        def add_bias(Y, S, bias, L=L):
+            bias = np.ascontiguousarray(bias, dtype=np.float64)
+            N, Co, Ho, Wo = Y.shape
+            L.oracle_add_bias(Y.ctypes.data_as(dp), S.ctypes.data_as(dp), bias.ctypes.data_as(dp), N, Co, Ho, Wo)
+
+        assert not _bias_closed_form_ok(add_bias), f"bias mutation {i} not caught: {b}"
