@@ -21,7 +21,8 @@ ALGOS = {"auto": 0, "im2win_fp32_cc": 1, "im2win_tc": 2, "implicit_tc": 3, "impl
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 LAYOUTS = {"nchw": 0, "nhwc": 1}
 
-EXPORTED = ("conv2d_desc_create", "conv2d_desc_set_input_layout", "conv2d_desc_destroy", "conv2d_out_dims",
+EXPORTED = ("conv2d_desc_create", "conv2d_desc_set_input_layout", "conv2d_desc_set_output_dtype",
+            "conv2d_desc_set_bias", "conv2d_desc_destroy", "conv2d_out_dims",
             "conv2d_workspace_size", "conv2d_get_algo", "conv2d_fwd", "conv2d_fwd_profiled", "conv2d_fwd_host",
             "conv2d_launches_per_call", "conv2d_fwd_static_workspace", "conv2d_static_workspace_bytes",
             "conv2d_set_wait_limit", "conv2d_device_status", "conv2d_status_string")
@@ -47,6 +48,8 @@ def load(path: str = LIB_PATH):
     c_int, c_size, vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
     L.conv2d_desc_create.argtypes = [ctypes.POINTER(vp)] + [c_int] * 11
     L.conv2d_desc_set_input_layout.argtypes = [vp, c_int]
+    L.conv2d_desc_set_output_dtype.argtypes = [vp, c_int]
+    L.conv2d_desc_set_bias.argtypes = [vp, vp]
     L.conv2d_desc_destroy.argtypes = [vp]
     L.conv2d_out_dims.argtypes = [vp, ctypes.POINTER(c_int), ctypes.POINTER(c_int)]
     L.conv2d_workspace_size.argtypes = [vp, ctypes.POINTER(c_size)]
@@ -88,6 +91,16 @@ def conv2d_desc_create(N, Cin, H, W, Cout, Kh, Kw, stride, pad, dtype="f32", alg
 def conv2d_desc_set_input_layout(desc: int, layout="nchw"):
     lo = LAYOUTS[layout] if isinstance(layout, str) else int(layout)
     _check(load().conv2d_desc_set_input_layout(desc, lo), "conv2d_desc_set_input_layout")
+
+
+def conv2d_desc_set_output_dtype(desc: int, out="f32"):
+    dt = DTYPES[out] if isinstance(out, str) else int(out)
+    _check(load().conv2d_desc_set_output_dtype(desc, dt), "conv2d_desc_set_output_dtype")
+
+
+def conv2d_desc_set_bias(desc: int, bias: int):
+    """Device address of Cout bias values of the input dtype (0 = no bias)."""
+    _check(load().conv2d_desc_set_bias(desc, bias or None), "conv2d_desc_set_bias")
 
 
 def conv2d_desc_destroy(desc: int):

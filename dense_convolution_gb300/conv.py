@@ -18,13 +18,17 @@ _NAME = {v: k for k, v in _TORCH_DTYPE.items()}
 class Conv2d:
     """One problem shape: descriptor, output shape and workspace size."""
 
-    def __init__(self, N, Cin, H, W, Cout, Kh, Kw, stride=1, pad=0, dtype="f32", algo="auto", layout="nchw"):
+    def __init__(self, N, Cin, H, W, Cout, Kh, Kw, stride=1, pad=0, dtype="f32", algo="auto", layout="nchw",
+                 out_dtype=None):
         self.shape = (N, Cin, H, W, Cout, Kh, Kw, stride, pad)
         self.dtype = dtype
+        self.out_dtype = out_dtype or dtype
         self.layout = layout
         self.desc = capi.conv2d_desc_create(N, Cin, H, W, Cout, Kh, Kw, stride, pad, dtype, algo)
         if layout != "nchw":
             capi.conv2d_desc_set_input_layout(self.desc, layout)
+        if self.out_dtype != dtype:
+            capi.conv2d_desc_set_output_dtype(self.desc, self.out_dtype)
         self.Ho, self.Wo = capi.conv2d_out_dims(self.desc)
         self.workspace_bytes = capi.conv2d_workspace_size(self.desc)
         self.algo = capi.conv2d_get_algo(self.desc)
@@ -48,16 +52,20 @@ class Conv2d:
         return torch.empty(n, dtype=torch.uint8, device=device)
 
     def alloc_output(self, device="cuda"):
-        return torch.empty(self.out_shape, dtype=_TORCH_DTYPE[self.dtype], device=device)
+        return torch.empty(self.out_shape, dtype=_TORCH_DTYPE[self.out_dtype], device=device)
 
     def __call__(self, x: torch.Tensor, w: torch.Tensor, y: torch.Tensor | None = None,
-                 workspace: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+                 workspace: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None,
+                 bias: torch.Tensor | None = None) -> torch.Tensor:
         N, Ci, H, W, Co, Kh, Kw = self.shape[:7]
         want_x = (N, Ci, H, W) if self.layout == "nchw" else (N, H, W, Ci)
         if tuple(x.shape) != want_x or not x.is_contiguous() or x.dtype != _TORCH_DTYPE[self.dtype]:
             raise ValueError(f"x must be a contiguous {self.dtype} tensor of shape {want_x}")
         if tuple(w.shape) != (Co, Ci, Kh, Kw) or not w.is_contiguous() or w.dtype != x.dtype:
             raise ValueError(f"w must be a contiguous {self.dtype} tensor of shape {(Co, Ci, Kh, Kw)}")
+        if bias is not None and (tuple(bias.shape) != (Co,) or not bias.is_contiguous() or bias.dtype != x.dtype):
+            raise ValueError(f"bias must be a contiguous {self.dtype} tensor of shape {(Co,)}")
+        capi.conv2d_desc_set_bias(self.desc, bias.data_ptr() if bias is not None else 0)
         if y is None:
             y = self.alloc_output(x.device)
         if workspace is None and self.workspace_bytes:

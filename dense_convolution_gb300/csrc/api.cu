@@ -184,6 +184,8 @@ CONV2D_API conv2d_status conv2d_desc_create(conv2d_desc_t* out, int N, int Cin, 
     d.dtype = dtype;
     d.requested = algo;
     d.layout = CONV2D_LAYOUT_NCHW;
+    d.out_dtype = dtype;
+    d.bias = nullptr;
     d.Ho = (int)Ho; d.Wo = (int)Wo; d.Wp = (int)Wp;
     conv2d_status st = finalize(d);
     if (st != CONV2D_OK) return st;
@@ -201,6 +203,21 @@ CONV2D_API conv2d_status conv2d_desc_set_input_layout(conv2d_desc_t d, conv2d_la
     conv2d_status st = finalize(t);
     if (st != CONV2D_OK) return st;
     *d = t;
+    return CONV2D_OK;
+}
+
+CONV2D_API conv2d_status conv2d_desc_set_output_dtype(conv2d_desc_t d, conv2d_dtype out) {
+    if (!d) return CONV2D_ERR_NULL_PTR;
+    if (out != d->dtype && !(out == CONV2D_F32 && d->dtype != CONV2D_F32)) return CONV2D_ERR_BAD_PARAM;
+    d->out_dtype = out;
+    return CONV2D_OK;
+}
+
+CONV2D_API conv2d_status conv2d_desc_set_bias(conv2d_desc_t d, const void* bias) {
+    if (!d) return CONV2D_ERR_NULL_PTR;
+    const size_t align = d->dtype == CONV2D_F32 ? 4 : 2;
+    if (reinterpret_cast<uintptr_t>(bias) % align) return CONV2D_ERR_MISALIGNED;
+    d->bias = bias;
     return CONV2D_OK;
 }
 
@@ -329,7 +346,7 @@ CONV2D_API conv2d_status conv2d_fwd_host(conv2d_desc_t dp, const void* x_host, c
     const size_t elem = d.dtype == CONV2D_F32 ? 4 : 2;
     const size_t x_bytes = (size_t)d.N * d.Ci * d.H * d.W * elem;
     const size_t w_bytes = (size_t)d.Co * d.Ci * d.Kh * d.Kw * elem;
-    const size_t y_bytes = (size_t)d.N * d.Co * d.Ho * d.Wo * elem;
+    const size_t y_bytes = (size_t)d.N * d.Co * d.Ho * d.Wo * (d.out_dtype == CONV2D_F32 ? 4 : 2);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return CONV2D_ERR_CUDA;
     if (cudaMemcpyAsync(w_dev, w_host, w_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return CONV2D_ERR_CUDA;

@@ -44,6 +44,7 @@ struct Fp32Params {
     int boxw;           // direct mode: staged row width (multiple of 4)
     int xs_floats;      // staged-input floats per stage (including read slack)
     int ws_floats;      // filter floats per stage
+    const float* bias;  // Co bias values, or null
 };
 
 constexpr int kCcCols = 64;    // output columns per block (8 lanes x 8)
@@ -218,6 +219,11 @@ __global__ void __launch_bounds__(128) conv_fp32_kernel(const Fp32Params prm,
     for (int j = 0; j < 8; ++j) {
         const int co = co_base + j;
         if (co >= prm.Co) continue;
+        if (prm.bias) {
+            const float bj = __ldg(prm.bias + co);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i][j] += bj;
+        }
         float* out = prm.y + (((long long)n * prm.Co + co) * prm.Ho + ho) * prm.Wo + wt;
         if (vec) {
             reinterpret_cast<float4*>(out)[0] = make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
@@ -276,7 +282,7 @@ static cudaError_t launch_fp32_shape(const conv2d_desc& d, const Fp32Params& prm
 conv2d_status launch_conv_fp32(const conv2d_desc& d, const float* src, const float* wq, float* y, bool im2win,
                                cudaStream_t st) {
     Fp32Params prm{};
-    prm.src = src; prm.wq = wq; prm.y = y;
+    prm.src = src; prm.wq = wq; prm.y = y; prm.bias = static_cast<const float*>(d.bias);
     prm.N = d.N; prm.Ci = d.Ci; prm.H = d.H; prm.W = d.W; prm.Co = d.Co; prm.Kh = d.Kh; prm.Kw = d.Kw;
     prm.s = d.s; prm.p = d.p; prm.Ho = d.Ho; prm.Wo = d.Wo; prm.Lp = d.Lp;
     prm.BCO = 32 * d.cc_warps;

@@ -79,7 +79,17 @@ struct TcParams {
     int epi_off;
     int n_pt;           // MODE 3: 128-pixel tiles per image
     void* y;
+    const void* bias;   // Co bias values of the input type, or null
+    int out32;          // 1: Y is fp32 (no rounding to the input type)
 };
+
+// Bias of output channel co, widened to fp32.
+template <bool BF16>
+__device__ __forceinline__ float load_bias(const void* bias, int co) {
+    const unsigned short u = __ldg(static_cast<const unsigned short*>(bias) + co);
+    if (BF16) return __bfloat162float(__ushort_as_bfloat16(u));
+    return __half2float(__ushort_as_half(u));
+}
 
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448;                               // 227 KB per block
@@ -353,7 +363,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
         const int eg = ew >> 2;                         // epilogue group = issuer
         const int quarter = warp & 3;                   // TMEM lane quarter this warp may access
         uint16_t* wst = reinterpret_cast<uint16_t*>(smem + prm.epi_off + ew * kEpiWarpBytes);
-        uint16_t* const yout = static_cast<uint16_t*>(prm.y);
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int g = blockIdx.x; g < prm.n_groups && eg < prm.group; g += gridDim.x) {
@@ -376,6 +385,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
                 const int co0 = n0 + quarter * 32;
                 const bool live = img < prm.N && co0 < prm.Co;
                 const uint32_t wbuf = smem_addr(smem + prm.epi_off + ew * kEpi1x1WarpBytes);
+                const float bl = (prm.bias && co0 + lane < prm.Co) ? load_bias<BF16>(prm.bias, co0 + lane) : 0.f;
 #pragma unroll 1
                 for (int h = 0; h < BN / 64; ++h) {
                     uint32_t v0[32], v1[32];
@@ -383,9 +393,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
                     tmem_ld_32x32b_x32(t_row + h * 64 + 32, v1);
                     tmem_ld_wait();
                     if (!live || p0 + h * 64 >= prm.HoWo) continue;   // warp-uniform
+                    if (prm.bias) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            v0[j] = __float_as_uint(__uint_as_float(v0[j]) + bl);
+                            v1[j] = __float_as_uint(__uint_as_float(v1[j]) + bl);
+                        }
+                    }
+                    const uint32_t row = wbuf + (uint32_t)lane * 128u;
+                    if (prm.out32) {
+                        // fp32 output: two stores of 32 channels x 32 pixels (128-byte rows).
+#pragma unroll
+                        for (int sub = 0; sub < 2; ++sub) {
+                            const uint32_t(&v)[32] = sub == 0 ? v0 : v1;
+                            if (p0 + h * 64 + sub * 32 >= prm.HoWo) break;   // warp-uniform
+                            if (lane == 0) bulk_wait_read_all();
+                            __syncwarp();
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                st_shared_v4(row + (uint32_t)((c ^ (lane & 7)) * 16), v[4 * c], v[4 * c + 1],
+                                             v[4 * c + 2], v[4 * c + 3]);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_3d(&ymap, wbuf, p0 + h * 64 + sub * 32, co0, img);
+                                bulk_commit_group();
+                            }
+                        }
+                        continue;
+                    }
                     if (lane == 0) bulk_wait_read_all();              // the box is free again
                     __syncwarp();
-                    const uint32_t row = wbuf + (uint32_t)lane * 128u;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         const uint32_t(&v)[32] = c < 4 ? v0 : v1;
@@ -414,9 +452,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
             } else {
             const int mw = m0 + quarter * 32;
             // Store geometry: this lane's piece of the warp's 32 pixels (vector
-            // paths) or its own pixel (scalar path).
+            // paths) or its own pixel (scalar path), as element offsets into Y.
             bool v_ok, p_ok;
-            uint16_t *vbase, *pbase;
+            long long voff, poff;
             int vpc, vrow0;
             if constexpr (MODE == 1) {
                 vpc = lane & 7; vrow0 = lane >> 3;
@@ -424,42 +462,92 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
                 const int ng = qg / prm.HpWq, rg = qg - ng * prm.HpWq;
                 const int yg = rg / prm.Wq, xg = rg - yg * prm.Wq;
                 v_ok = ng < prm.N && yg < prm.Ho && xg < prm.Wo;
-                vbase = yout + (long long)ng * prm.Co * prm.HoWo + yg * prm.Wo + xg;
+                voff = (long long)ng * prm.Co * prm.HoWo + yg * prm.Wo + xg;
                 const int qp = mw + lane;
                 const int np = qp / prm.HpWq, rp = qp - np * prm.HpWq;
                 const int yp = rp / prm.Wq, xp = rp - yp * prm.Wq;
                 p_ok = np < prm.N && yp < prm.Ho && xp < prm.Wo;
-                pbase = yout + (long long)np * prm.Co * prm.HoWo + yp * prm.Wo + xp;
+                poff = (long long)np * prm.Co * prm.HoWo + yp * prm.Wo + xp;
             } else {
                 vpc = lane & 3; vrow0 = lane >> 2;
                 const int mg = mw + 8 * vpc;
                 v_ok = mg < prm.M;
                 const int img = v_ok ? mg / prm.HoWo : 0;
                 const int r = v_ok ? mg - img * prm.HoWo : 0;
-                vbase = yout + ((long long)img * prm.Co) * prm.HoWo + r;
+                voff = ((long long)img * prm.Co) * prm.HoWo + r;
                 const int m = mw + lane;
                 p_ok = m < prm.M;
                 const int imgp = p_ok ? m / prm.HoWo : 0;
                 const int rp = p_ok ? m - imgp * prm.HoWo : 0;
-                pbase = yout + ((long long)imgp * prm.Co) * prm.HoWo + rp;
+                poff = ((long long)imgp * prm.Co) * prm.HoWo + rp;
             }
-            auto cvt = [](uint32_t u) -> uint16_t {
-                const float f = __uint_as_float(u);
+            auto cvt = [](float f) -> uint16_t {
                 if (BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(f));
                 return __half_as_ushort(__float2half_rn(f));
             };
+            // Register j of a chunk is channel cob + j of this lane's pixel; the
+            // bias of channel cob + lane is loaded by lane `lane` and broadcast.
             auto emit = [&](const uint32_t (&v)[32], int cc) {
                 const int cob = n0 + cc * 32;
+                float f[32];
+                float bl = 0.f;
+                if (prm.bias && cob + lane < prm.Co) bl = load_bias<BF16>(prm.bias, cob + lane);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    f[j] = __uint_as_float(v[j]);
+                    if (prm.bias) f[j] += __shfl_sync(0xffffffffu, bl, j);
+                }
+                if (prm.out32) {
+                    // fp32 output: 16 channels x 32 pixels (2 KB) per pass.
+                    float* const y32 = static_cast<float*>(prm.y);
+                    float* const wf = reinterpret_cast<float*>(wst);
+#pragma unroll
+                    for (int hlf = 0; hlf < 2; ++hlf) {
+                        const int c16 = cob + hlf * 16;
+                        if (prm.vec_store) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) wf[j * 32 + lane] = f[hlf * 16 + j];
+                            __syncwarp();
+                            if constexpr (MODE == 1) {
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const int row = vrow0 + 4 * i;
+                                    if (v_ok && c16 + row < prm.Co)
+                                        *reinterpret_cast<float4*>(y32 + voff + (long long)(c16 + row) * prm.HoWo) =
+                                            *reinterpret_cast<const float4*>(wf + row * 32 + 4 * vpc);
+                                }
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 2; ++i) {
+                                    const int row = vrow0 + 8 * i;
+                                    if (v_ok && c16 + row < prm.Co) {
+                                        float4* dst = reinterpret_cast<float4*>(y32 + voff + (long long)(c16 + row) * prm.HoWo);
+                                        const float4* src = reinterpret_cast<const float4*>(wf + row * 32 + 8 * vpc);
+                                        dst[0] = src[0];
+                                        dst[1] = src[1];
+                                    }
+                                }
+                            }
+                            __syncwarp();
+                        } else if (p_ok) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                if (c16 + j < prm.Co) y32[poff + (long long)(c16 + j) * prm.HoWo] = f[hlf * 16 + j];
+                        }
+                    }
+                    return;
+                }
+                uint16_t* const yout = static_cast<uint16_t*>(prm.y);
                 if (prm.vec_store) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) wst[j * 32 + lane] = cvt(v[j]);
+                    for (int j = 0; j < 32; ++j) wst[j * 32 + lane] = cvt(f[j]);
                     __syncwarp();
                     if constexpr (MODE == 1) {
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const int row = vrow0 + 4 * i;
                             if (v_ok && cob + row < prm.Co)
-                                *reinterpret_cast<uint2*>(vbase + (long long)(cob + row) * prm.HoWo) =
+                                *reinterpret_cast<uint2*>(yout + voff + (long long)(cob + row) * prm.HoWo) =
                                     *reinterpret_cast<const uint2*>(wst + row * 32 + 4 * vpc);
                         }
                     } else {
@@ -467,7 +555,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
                         for (int i = 0; i < 4; ++i) {
                             const int row = vrow0 + 8 * i;
                             if (v_ok && cob + row < prm.Co)
-                                *reinterpret_cast<uint4*>(vbase + (long long)(cob + row) * prm.HoWo) =
+                                *reinterpret_cast<uint4*>(yout + voff + (long long)(cob + row) * prm.HoWo) =
                                     *reinterpret_cast<const uint4*>(wst + row * 32 + 8 * vpc);
                         }
                     }
@@ -475,7 +563,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
                 } else if (p_ok) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (cob + j < prm.Co) pbase[(long long)(cob + j) * prm.HoWo] = cvt(v[j]);
+                        if (cob + j < prm.Co) yout[poff + (long long)(cob + j) * prm.HoWo] = cvt(f[j]);
                 }
             };
 #pragma unroll 1
@@ -715,11 +803,15 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     if (gemm1x1) {
         // Y as [N][Co][P]: store boxes of 64 pixels x 32 channels (one epilogue warp's lanes).
         const cuuint64_t P = (cuuint64_t)d.H * d.W;
+        // fp32 Y: boxes of 32 pixels x 32 channels (128-byte rows as well).
+        const bool o32 = d.out_dtype == CONV2D_F32;
+        const cuuint64_t ye = o32 ? 4 : 2;
         cuuint64_t ydims[3] = {P, (cuuint64_t)d.Co, (cuuint64_t)d.N};
-        cuuint64_t ystr[2] = {P * 2, P * 2 * (cuuint64_t)d.Co};
-        cuuint32_t ybox[3] = {64, 32, 1};
+        cuuint64_t ystr[2] = {P * ye, P * ye * (cuuint64_t)d.Co};
+        cuuint32_t ybox[3] = {o32 ? 32u : 64u, 32, 1};
         cuuint32_t yestr[3] = {1, 1, 1};
-        r = enc_tiled(&ymap, dt, 3, y, ydims, ystr, ybox, yestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+        r = enc_tiled(&ymap, o32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : dt, 3, y, ydims, ystr, ybox, yestr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
     } else {
@@ -752,6 +844,8 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     prm.epi_off = prm.b_res_off + (b_res ? bres_bytes : 0);
     prm.n_pt = n_pt;
     prm.y = y;
+    prm.bias = d.bias;
+    prm.out32 = d.out_dtype == CONV2D_F32 ? 1 : 0;
     if (grid_rows)
         prm.vec_store = ((d.Wo % 4) == 0 && (d.Wq % 4) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) ? 1 : 0;
     else

@@ -13,6 +13,8 @@ struct conv2d_desc {
     conv2d_dtype dtype;
     conv2d_algo requested;
     conv2d_layout layout;
+    conv2d_dtype out_dtype;   // element type of Y: dtype, or F32 for 16-bit inputs
+    const void* bias;         // Co bias values of the input type (device), or null
     // Derived geometry.
     int Ho, Wo, Wp;       // output size; padded input width W + 2p
     conv2d_algo algo;     // resolved (never AUTO)

@@ -121,6 +121,27 @@ conv2d_status conv2d_desc_create(conv2d_desc_t *out, int N, int Cin, int H, int 
  * unknown layout; UNSUPPORTED for NHWC with an fp32 algorithm. */
 conv2d_status conv2d_desc_set_input_layout(conv2d_desc_t d, conv2d_layout layout);
 
+/* Element type of Y.  Default: the input dtype (fp16/bf16 outputs rounded to
+ * nearest even once, from the fp32 accumulator).  For CONV2D_F16 /
+ * CONV2D_BF16 inputs, CONV2D_F32 keeps the fp32 accumulator unrounded (Y is
+ * then [N][Cout][Ho][Wo] floats).  The pages fix no output type for 16-bit
+ * inputs ("Enabling Memory-efficient Im2win Convolution ...", Sec. III-F
+ * says only that the tensor cores take fp16); this option serves callers
+ * that want the fp32 sum.  BAD_PARAM for any other type. */
+conv2d_status conv2d_desc_set_output_dtype(conv2d_desc_t d, conv2d_dtype out);
+
+/* Per-output-channel bias, the `Y_col += bias` of the PyTorch listing in
+ * "Unifying Convolutions and GEMM", Sec. 6:
+ *   Y[n,co,ho,wo] = b[co] + sum_{ci,kh,kw} X[...] * W[...]
+ * added to the fp32 accumulator before the one rounding to Y's type.
+ *   bias  device pointer to Cout elements of the INPUT dtype (fp32 for
+ *         CONV2D_F32, else fp16/bf16 like W), or NULL for no bias (default).
+ * The descriptor keeps the pointer (it does not copy the values): every
+ * conv2d_fwd* call made with this descriptor reads b from it on the GPU, so
+ * the buffer must stay valid while such calls can run.  Errors: NULL_PTR (d),
+ * MISALIGNED (bias not aligned to its element size). */
+conv2d_status conv2d_desc_set_bias(conv2d_desc_t d, const void *bias);
+
 /* Release a descriptor (NULL is accepted and ignored). */
 conv2d_status conv2d_desc_destroy(conv2d_desc_t d);
 
@@ -137,7 +158,9 @@ conv2d_status conv2d_get_algo(conv2d_desc_t d, conv2d_algo *chosen);
 /* Forward convolution on `stream`.
  *   x  device, layout per conv2d_desc_set_input_layout, dtype of the desc
  *   w  device, [Cout][Cin][Kh][Kw] contiguous, dtype of the desc
- *   y  device, [N][Cout][Ho][Wo] contiguous; fp32 for CONV2D_F32, else dtype
+ *   y  device, [N][Cout][Ho][Wo] contiguous, of the output dtype (the input
+ *      dtype unless conv2d_desc_set_output_dtype chose fp32); plus b[co]
+ *      when conv2d_desc_set_bias gave a bias
  *   workspace, workspace_bytes: device scratch of at least
  *      conv2d_workspace_size bytes (NULL/0 allowed when that size is 0);
  *      its contents on entry do not matter and are garbage on exit.

@@ -222,3 +222,27 @@ def test_static_workspace_size_getter(capi):
     # The binding reads the size from the library, which reports the header's value.
     assert capi.conv2d_static_workspace_bytes() == 64 << 20
     assert capi.STATIC_WORKSPACE_BYTES == 64 << 20
+
+
+def test_output_dtype_and_bias_setters(capi):
+    d16 = capi.conv2d_desc_create(1, 8, 8, 8, 8, 3, 3, 1, 1, "f16", "auto")
+    d32 = capi.conv2d_desc_create(1, 8, 8, 8, 8, 3, 3, 1, 1, "f32", "auto")
+    try:
+        capi.conv2d_desc_set_output_dtype(d16, "f32")      # fp32 sum of 16-bit inputs
+        capi.conv2d_desc_set_output_dtype(d16, "f16")      # back to the input type
+        for desc, bad in ((d16, "bf16"), (d32, "f16"), (d32, "bf16")):
+            with pytest.raises(capi.Conv2dError) as e:
+                capi.conv2d_desc_set_output_dtype(desc, bad)
+            assert e.value.status == capi.ERR_BAD_PARAM
+        capi.conv2d_desc_set_bias(d16, 0)                  # no bias
+        capi.conv2d_desc_set_bias(d16, 0x10002)            # 2-byte aligned is enough for 16-bit values
+        with pytest.raises(capi.Conv2dError) as e:
+            capi.conv2d_desc_set_bias(d16, 0x10001)
+        assert e.value.status == capi.ERR_MISALIGNED
+        with pytest.raises(capi.Conv2dError) as e:
+            capi.conv2d_desc_set_bias(d32, 0x10002)
+        assert e.value.status == capi.ERR_MISALIGNED
+        capi.conv2d_desc_set_bias(d16, 0)
+    finally:
+        capi.conv2d_desc_destroy(d16)
+        capi.conv2d_desc_destroy(d32)
