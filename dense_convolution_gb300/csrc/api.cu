@@ -130,6 +130,26 @@ conv2d_status finalize(conv2d_desc& d) {
         d.gemm1x1 = d.algo == CONV2D_ALGO_IMPLICIT_TC && d.layout == CONV2D_LAYOUT_NCHW && d.Kh == 1 &&
                     d.Kw == 1 && d.s == 1 && d.p == 0 && d.Ci % 8 == 0 && ((long long)d.H * d.W) % 8 == 0;
         if (d.gemm1x1) d.BN = 128;   // 128 output channels x 128 pixels per MMA tile
+        // Implicit GEMM on NCHW input at stride 1: operand tiles are built from X
+        // inside the contraction kernel (zero-padded halo over a virtual grid of
+        // pitch Wq), so no copy of X is made.  Vector width: the widest that
+        // divides W; the pitch is W + 2p rounded up to it (and to 4 when Wo % 4
+        // == 0 for the 8-byte stores); the narrowest pitch wins.
+        d.nchw_halo = false;
+        if (d.algo == CONV2D_ALGO_IMPLICIT_TC && d.layout == CONV2D_LAYOUT_NCHW && !d.gemm1x1 && d.s == 1) {
+            int best_v = 0, best_wq = 0;
+            for (int v = 8; v >= 1; v /= 2) {
+                if (d.W % v) continue;
+                const int a = v > (d.Wo % 4 == 0 ? 4 : 1) ? v : (d.Wo % 4 == 0 ? 4 : 1);
+                const int wq = (d.Wp + a - 1) / a * a;
+                if (!best_v || wq < best_wq) { best_v = v; best_wq = wq; }
+            }
+            d.halo_v = best_v;
+            d.Wq = best_wq;
+            d.Hp = d.H + 2 * d.p;
+            const long long rows = (long long)d.N * d.Hp * d.Wq;
+            d.nchw_halo = rows + (long long)d.Kh * d.Wq + d.Kw + kTcBlockM <= kMaxElems && halo_plan_fits(d);
+        }
         if ((long long)d.Ci * d.Kh * d.Kw > 16384) return CONV2D_ERR_UNSUPPORTED;   // per-channel filter staging
         if (d.N > 65535) return CONV2D_ERR_UNSUPPORTED;
         const long long wq = (long long)d.Co * d.taps * d.CP;
@@ -152,7 +172,7 @@ conv2d_status finalize(conv2d_desc& d) {
             const long long win = rows * d.s * d.Ck;
             if (win > kMaxElems * 4) return CONV2D_ERR_UNSUPPORTED;
             d.ws_input = (size_t)win * 2;
-        } else if (d.layout == CONV2D_LAYOUT_NCHW) {
+        } else if (d.layout == CONV2D_LAYOUT_NCHW && !d.nchw_halo) {
             d.ws_input = (size_t)((long long)d.N * d.H * d.W * d.Ci8) * 2;
         }
     }
@@ -297,6 +317,11 @@ conv2d_status fwd_impl(conv2d_desc_t dp, const void* x, const void* w, void* y, 
                 break;
             }
             e = launch_pack_filter_tc(w, wq, d, false, st);
+            if (d.nchw_halo) {   // the kernel reads NCHW X itself
+                if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
+                if (e == cudaSuccess) s = launch_conv_tc(d, x, wq, y, 4, st);
+                break;
+            }
             const void* src = x;
             if (e == cudaSuccess && d.layout == CONV2D_LAYOUT_NCHW) {
                 e = launch_nchw_to_nhwc16(x, win, d.N, d.Ci, d.H, d.W, d.Ci8, st);
@@ -364,7 +389,7 @@ CONV2D_API conv2d_status conv2d_launches_per_call(conv2d_desc_t d, int* launches
     }
     int n = 2;   // filter repack + contraction
     if (d->algo == CONV2D_ALGO_IM2WIN_FP32_CC || d->algo == CONV2D_ALGO_IM2WIN_TC || d->algo == CONV2D_ALGO_PADDED_TC ||
-        (d->algo == CONV2D_ALGO_IMPLICIT_TC && d->layout == CONV2D_LAYOUT_NCHW))
+        (d->algo == CONV2D_ALGO_IMPLICIT_TC && d->layout == CONV2D_LAYOUT_NCHW && !d->nchw_halo))
         ++n;
     *launches = n;
     return CONV2D_OK;

@@ -81,6 +81,16 @@ struct TcParams {
     void* y;
     const void* bias;   // Co bias values of the input type, or null
     int out32;          // 1: Y is fp32 (no rounding to the input type)
+    // MODE 4 (halo tiles built from NCHW X in shared memory): the A ring
+    // holds a_stages stages of `group` halo regions of halo_rows rows each,
+    // one stage per (channel chunk, group of khg filter rows); B streams
+    // through the ring above (stages, stage_bytes) unless resident.
+    const void* x;      // NCHW input
+    int Ci, H, W;
+    int khg, n_khg;     // filter rows per A stage; A stages per channel chunk
+    int halo_rows;      // rows (pixels) of one halo region, a multiple of 8
+    int a_stages, a_stage_bytes, a_ring_off;
+    int vecw;           // pixels per vector load (W % vecw == 0, Wq % vecw == 0)
 };
 
 // Bias of output channel co, widened to fp32.
@@ -102,6 +112,10 @@ template <int MODE>
 __host__ __device__ constexpr int epi_bytes() { return MODE == 3 ? kEpi1x1Bytes : kEpiBytes; }
 constexpr int kBarBytes = 512;
 constexpr int kTcThreads = 32 * (1 + kIssuers + 8);              // producer, issuers, 8 epilogue warps
+constexpr int kTransposerWarps = 4;                              // MODE 4: halo builders
+constexpr int kMaxAStages = 4;
+template <int MODE>
+__host__ __device__ constexpr int tc_threads() { return kTcThreads + (MODE == 4 ? 32 * kTransposerWarps : 0); }
 
 template <int BN>
 struct TcConfig {
@@ -111,6 +125,90 @@ struct TcConfig {
 // filter][epilogue staging][barriers].  A stage is [A region of issuer 0]
 // [A region of issuer 1][kpb B chunks, unless the filter is resident]; every
 // region is a multiple of 1024 bytes (128-byte swizzle atoms).
+
+// ---------------------------------------------------------------- MODE 4 halo builders
+// V consecutive pixels of one channel from global memory (16-bit elements;
+// the address is aligned to 2*V bytes), as V halves in d[0..].
+template <int V>
+__device__ __forceinline__ void load_pixels(const uint16_t* src, uint32_t (&d)[4]) {
+    if constexpr (V == 8) {
+        const uint4 t = __ldg(reinterpret_cast<const uint4*>(src));
+        d[0] = t.x; d[1] = t.y; d[2] = t.z; d[3] = t.w;
+    } else if constexpr (V == 4) {
+        const uint2 t = __ldg(reinterpret_cast<const uint2*>(src));
+        d[0] = t.x; d[1] = t.y;
+    } else if constexpr (V == 2) {
+        d[0] = __ldg(reinterpret_cast<const unsigned int*>(src));
+    } else {
+        d[0] = __ldg(src);
+    }
+}
+
+constexpr int kBuildBatch = 8;   // vector groups whose loads a builder lane keeps in flight
+
+// Build this warp's share of one A stage: for each valid tile i of the group,
+// halo_rows rows of 64 channels (chunk cb) in the 128-byte-swizzled K-major
+// layout, row r = padded pixel P = (mt0 + i)*128 + kg*khg*Wq + r of the
+// virtual grid [N][H+2p][Wq]:  X[n][c][yy-p][xx-p], zero outside the image,
+// past Ci, in the pitch's junk columns and past the last image.  Rows are
+// taken in groups of V pixels that start at padded column = p (mod V), so a
+// group lies in one image row and is either all inside the image (one V-wide
+// load per channel) or all padding.  Lane l carries channels 2l and 2l+1 and
+// writes them as one 32-bit word, so a warp store fills one 128-byte row.
+template <int V>
+__device__ __forceinline__ void build_halo_stage(const TcParams& prm, int tw, int lane, uint32_t stage_base,
+                                                 int mt0, int n_val, int cb, int kg) {
+    const uint16_t* __restrict__ xg = static_cast<const uint16_t*>(prm.x);
+    const long long plane = (long long)prm.H * prm.W;
+    const int R = prm.halo_rows;
+    const int g0 = prm.p % V ? prm.p % V - V : 0;           // first group's first row (<= 0)
+    const int n_vg = (R - g0 + V - 1) / V;                   // groups per halo region
+    const int ch = cb * kTcBlockK + 2 * lane;                // this lane's channel pair
+    const int total = n_val * n_vg;
+    for (int j0 = tw; j0 < total; j0 += kTransposerWarps * kBuildBatch) {
+        uint32_t d0[kBuildBatch][4], d1[kBuildBatch][4];
+        int ti[kBuildBatch], tr[kBuildBatch];               // tile (-1: no group) and first row
+#pragma unroll
+        for (int u = 0; u < kBuildBatch; ++u) {
+            const int j = j0 + u * kTransposerWarps;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d0[u][e] = d1[u][e] = 0u;
+            ti[u] = -1;
+            tr[u] = 0;
+            if (j >= total) continue;
+            const int i = j / n_vg, jg = j - i * n_vg;
+            const int r0 = g0 + jg * V;
+            ti[u] = i;
+            tr[u] = r0;
+            const int P = (mt0 + i) * kTcBlockM + kg * prm.khg * prm.Wq + r0;
+            if (P < 0) continue;
+            const int n = P / prm.HpWq;
+            const int rem = P - n * prm.HpWq;
+            const int yy = rem / prm.Wq, xx = rem - yy * prm.Wq;
+            const int iy = yy - prm.p, ix = xx - prm.p;
+            if (n >= prm.N || iy < 0 || iy >= prm.H || ix < 0 || ix >= prm.W) continue;
+            const uint16_t* src = xg + ((long long)n * prm.Ci + ch) * plane + (long long)iy * prm.W + ix;
+            if (ch < prm.Ci) load_pixels<V>(src, d0[u]);
+            if (ch + 1 < prm.Ci) load_pixels<V>(src + plane, d1[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < kBuildBatch; ++u) {
+            if (ti[u] < 0) continue;                          // warp-uniform
+            const int r0 = tr[u];
+            const uint32_t tile = stage_base + (uint32_t)(ti[u] * prm.a_bytes);
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                const int r = r0 + e;
+                if (r < 0 || r >= R) continue;
+                const uint32_t lo = (d0[u][e >> 1] >> (16 * (e & 1))) & 0xffffu;
+                const uint32_t hi = (d1[u][e >> 1] >> (16 * (e & 1))) & 0xffffu;
+                const uint32_t addr =
+                    tile + (uint32_t)r * 128u + ((((uint32_t)(lane >> 2) ^ (uint32_t)(r & 7)) << 4) | ((lane & 3) << 2));
+                st_shared_b32(addr, lo | (hi << 16));
+            }
+        }
+    }
+}
 
 // MODE is the A addressing (0 im2col walk, 1 virtual-grid rows, 3 1x1 GEMM
 // on NCHW); each compiles to its own kernel so the producer and MMA loops
@@ -125,7 +223,7 @@ struct TcConfig {
 // whole filter slice fits (one channel tile), it is loaded once per CTA and
 // stays resident, and stages carry A only.
 template <int BN, bool BF16, int MODE>
-__global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_constant__ CUtensorMap amap,
+__global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __grid_constant__ CUtensorMap amap,
                                                                 const __grid_constant__ CUtensorMap bmap,
                                                                 const __grid_constant__ CUtensorMap ymap,
                                                                 const TcParams prm) {
@@ -139,7 +237,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
     // bars: [0, S) full, [S, 2S) empty, then per issuer i: accf[i][0..n_acc),
     // acce[i][0..n_acc), then the resident-filter barrier and kIssuers drain barriers.
     const int nacc = prm.n_acc;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4 * kIssuers + 1 + kIssuers);
+    // MODE 4 A ring: afull[0..kMaxAStages), aempty[0..kMaxAStages) after the drain barriers.
+    uint64_t* abars = bars + 2 * S + 2 * kIssuers * nacc + 1 + kIssuers;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(abars + 2 * kMaxAStages);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -157,6 +257,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
             for (int a = 0; a < nacc; ++a) { mbar_init(accf_bar(is, a), 1); mbar_init(acce_bar(is, a), 4); }
         mbar_init(bres_bar, 1);
         for (int is = 0; is < kIssuers; ++is) mbar_init(drain_bar(is), 1);
+        if constexpr (MODE == 4) {
+            for (int i = 0; i < prm.a_stages; ++i) {
+                mbar_init(smem_addr(&abars[i]), kTransposerWarps);          // one arrive per builder warp
+                mbar_init(smem_addr(&abars[kMaxAStages + i]), prm.group);    // one commit per issuer
+            }
+        }
         *abort_flag = 0;
         mbar_fence_init();
         tma_prefetch_desc(&amap);
@@ -200,6 +306,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
             long long issued = 0;
             bool free_now = false;
             for (int g = blockIdx.x; g < prm.n_groups && ok; g += gridDim.x) {
+                if constexpr (MODE == 4) {
+                    // A is built by the halo builders; only filter chunks stream
+                    // here, one per (channel chunk, tap), in the issuers' order.
+                    if (prm.b_res) break;
+                    const int nb0 = (g % prm.n_n_tiles) * BN;
+                    const int Kh = prm.taps / prm.Kw;
+                    for (int cb = 0; cb < prm.n_cchunks && ok; ++cb)
+                        for (int kg = 0; kg < prm.n_khg && ok; ++kg) {
+                            const int kh1 = min(Kh, (kg + 1) * prm.khg);
+                            for (int kh = kg * prm.khg; kh < kh1 && ok; ++kh)
+                                for (int kw = 0; kw < prm.Kw; ++kw) {
+                                    if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag)) { ok = false; break; }
+                                    mbar_arrive_expect_tx(full_bar(stage), (uint32_t)Cfg::kBBytes);
+                                    tma_load_2d(smem_addr(smem + stage * prm.stage_bytes), &bmap, full_bar(stage),
+                                                (kh * prm.Kw + kw) * prm.CP + cb * kTcBlockK, nb0);
+                                    ++issued;
+                                    if (++stage == S) { stage = 0; phase ^= 1; }
+                                }
+                        }
+                    continue;
+                }
                 const int n0 = (g % prm.n_n_tiles) * BN;
                 const int mt0 = (g / prm.n_n_tiles) * prm.group;
                 int m0[kIssuers], img[kIssuers], ho[kIssuers], wo[kIssuers];
@@ -290,8 +417,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
         if (lane == 0 && is < prm.group) {
             // MODE 3: the pixel operand is MN-major (instruction descriptor bit 16).
             constexpr uint32_t idesc = umma_idesc_f16(BF16, kTcBlockM, BN) | (MODE == 3 ? (1u << 16) : 0u);
-            int stage = 0, acc = 0;
-            uint32_t phase = 0, acc_phase = 0;
+            int stage = 0, acc = 0, a_stage = 0;
+            uint32_t phase = 0, acc_phase = 0, a_phase = 0;
             bool ok = true, issued_any = false, ready_now = false;
             if (prm.b_res && !mbar_wait(bres_bar, 0, abort_flag)) ok = false;
             const uint32_t bres_base = smem_addr(smem + prm.b_res_off);
@@ -299,6 +426,53 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
                 if (!mbar_wait(acce_bar(is, acc), acc_phase ^ 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)((is * nacc + acc) * BN);
+                if constexpr (MODE == 4) {
+                    // One A stage = this tile's halo for (channel chunk cb, filter rows
+                    // kg*khg ..): tap (kh, kw) reads it from row (kh - kg*khg)*Wq + kw
+                    // (128 bytes per row; descriptor addresses in 16-byte units).
+                    const int Kh = prm.taps / prm.Kw;
+                    bool first = true;
+                    for (int cb = 0; cb < prm.n_cchunks && ok; ++cb)
+                        for (int kg = 0; kg < prm.n_khg && ok; ++kg) {
+                            const uint32_t afull = smem_addr(&abars[a_stage]);
+                            if (!mbar_wait(afull, a_phase, abort_flag)) { ok = false; break; }
+                            tc_fence_after();
+                            const uint64_t a_desc = sw128_kmajor_desc(smem_addr(
+                                smem + prm.a_ring_off + a_stage * prm.a_stage_bytes + is * prm.a_bytes));
+                            const int kh1 = min(Kh, (kg + 1) * prm.khg);
+                            for (int kh = kg * prm.khg; kh < kh1 && ok; ++kh)
+                                for (int kw = 0; kw < prm.Kw; ++kw) {
+                                    const int t = kh * prm.Kw + kw;
+                                    uint32_t b_addr;
+                                    if (prm.b_res) {
+                                        b_addr = bres_base + (uint32_t)((cb * prm.taps + t) * Cfg::kBBytes);
+                                    } else {
+                                        if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
+                                        tc_fence_after();
+                                        b_addr = smem_addr(smem + stage * prm.stage_bytes);
+                                    }
+                                    const uint64_t b_desc = sw128_kmajor_desc(b_addr);
+                                    const uint64_t a_off = (uint64_t)(((kh - kg * prm.khg) * prm.Wq + kw) * 8);
+#pragma unroll
+                                    for (int k = 0; k < kTcBlockK / 16; ++k)
+                                        umma_f16(d_tmem, a_desc + a_off + (uint64_t)(2 * k), b_desc + (uint64_t)(2 * k),
+                                                 idesc, (!first || k > 0) ? 1u : 0u);
+                                    first = false;
+                                    issued_any = true;
+                                    if (!prm.b_res) {
+                                        umma_commit(empty_bar(stage));
+                                        if (++stage == S) { stage = 0; phase ^= 1; }
+                                    }
+                                }
+                            if (!ok) break;
+                            umma_commit(smem_addr(&abars[kMaxAStages + a_stage]));
+                            if (++a_stage == prm.a_stages) { a_stage = 0; a_phase ^= 1; }
+                        }
+                    if (!ok) break;
+                    umma_commit(accf_bar(is, acc));
+                    if (++acc == nacc) { acc = 0; acc_phase ^= 1; }
+                    continue;
+                }
                 int cb = 0, t = 0;
                 for (int sp = 0; sp < prm.n_sp; ++sp) {
                     if (!ready_now && !mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
@@ -347,7 +521,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
                 mbar_drain_wait(drain_bar(is), 0);
             }
         }
-    } else {
+    } else if (warp < kTcThreads / 32) {
         // ------------------------------------------------------------ epilogue
         // Two groups of four warps; group e drains the accumulators of issuer
         // e.  Warp q of a group owns TMEM lanes 32q..32q+31, i.e. pixels
@@ -456,7 +630,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
             bool v_ok, p_ok;
             long long voff, poff;
             int vpc, vrow0;
-            if constexpr (MODE == 1) {
+            if constexpr (MODE == 1 || MODE == 4) {
                 vpc = lane & 7; vrow0 = lane >> 3;
                 const int qg = mw + 4 * vpc;
                 const int ng = qg / prm.HpWq, rg = qg - ng * prm.HpWq;
@@ -508,7 +682,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
 #pragma unroll
                             for (int j = 0; j < 16; ++j) wf[j * 32 + lane] = f[hlf * 16 + j];
                             __syncwarp();
-                            if constexpr (MODE == 1) {
+                            if constexpr (MODE == 1 || MODE == 4) {
 #pragma unroll
                                 for (int i = 0; i < 4; ++i) {
                                     const int row = vrow0 + 4 * i;
@@ -542,7 +716,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
 #pragma unroll
                     for (int j = 0; j < 32; ++j) wst[j * 32 + lane] = cvt(f[j]);
                     __syncwarp();
-                    if constexpr (MODE == 1) {
+                    if constexpr (MODE == 1 || MODE == 4) {
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const int row = vrow0 + 4 * i;
@@ -585,6 +759,40 @@ __global__ void __launch_bounds__(kTcThreads, 1) conv_tc_kernel(const __grid_con
         if constexpr (MODE == 3) {
             if (lane == 0) bulk_wait_all();
         }
+    } else {
+        // ------------------------------------------------------------ halo builders (MODE 4)
+        // Each A stage: wait until both issuers have released the slot, build
+        // this warp's share of the group's halo regions, make the generic-proxy
+        // stores visible to the tensor core (async proxy), arrive.
+        if constexpr (MODE == 4) {
+            const int tw = warp - kTcThreads / 32;
+            int a_stage = 0;
+            uint32_t a_phase = 0;
+            bool ok = true;
+            for (int g = blockIdx.x; g < prm.n_groups && ok; g += gridDim.x) {
+                const int mt0 = (g / prm.n_n_tiles) * prm.group;
+                int n_val = 0;
+                for (int i = 0; i < prm.group; ++i) n_val += (mt0 + i < prm.n_m_tiles) ? 1 : 0;
+                for (int cb = 0; cb < prm.n_cchunks && ok; ++cb)
+                    for (int kg = 0; kg < prm.n_khg; ++kg) {
+                        if (!mbar_wait(smem_addr(&abars[kMaxAStages + a_stage]), a_phase ^ 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t base = smem_addr(smem + prm.a_ring_off + a_stage * prm.a_stage_bytes);
+                        switch (prm.vecw) {
+                            case 8: build_halo_stage<8>(prm, tw, lane, base, mt0, n_val, cb, kg); break;
+                            case 4: build_halo_stage<4>(prm, tw, lane, base, mt0, n_val, cb, kg); break;
+                            case 2: build_halo_stage<2>(prm, tw, lane, base, mt0, n_val, cb, kg); break;
+                            default: build_halo_stage<1>(prm, tw, lane, base, mt0, n_val, cb, kg); break;
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_addr(&abars[a_stage]));
+                        if (++a_stage == prm.a_stages) { a_stage = 0; a_phase ^= 1; }
+                    }
+            }
+        }
     }
 
     tc_fence_before();
@@ -608,6 +816,15 @@ void* driver_entry(const char* name) {
 
 cudaError_t status_read_clear_tc(cudaStream_t st, uint32_t* out) { return status_read_clear(st, out); }
 cudaError_t wait_limit_set_tc(cudaStream_t st, uint64_t ns) { return wait_limit_set(st, ns); }
+
+// Whether the MODE 4 rings fit for this shape with tile pairs (the larger
+// case): two A stages of the smallest halo (one filter row) and three
+// streamed filter chunks.
+bool halo_plan_fits(const conv2d_desc& d) {
+    const int rows = (kTcBlockM + d.Kw - 1 + 7) / 8 * 8;
+    const int budget = kSmemLimit - 1024 - kEpiBytes - kBarBytes;
+    return 2 * (kIssuers * rows * 128) + 3 * d.BN * kTcBlockK * 2 <= budget;
+}
 
 int device_sm_count() {
     static int cached[64] = {0};
@@ -635,7 +852,7 @@ static cudaError_t launch_tc_inst(const CUtensorMap& a, const CUtensorMap& b, co
     auto kern = conv_tc_kernel<BN, BF16, MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_after(kern, dim3(grid), dim3(kTcThreads), smem, st, a, b, y, prm);
+    return launch_after(kern, dim3(grid), dim3(tc_threads<MODE>()), smem, st, a, b, y, prm);
 }
 
 template <bool BF16, int MODE>
@@ -658,6 +875,7 @@ static cudaError_t launch_tc_mode(int BN, int amode, const CUtensorMap& a, const
     switch (amode) {
         case 0:  return launch_tc_bn<BF16, 0>(BN, a, b, y, prm, grid, smem, st);
         case 3:  return launch_tc_bn<BF16, 3>(BN, a, b, y, prm, grid, smem, st);
+        case 4:  return launch_tc_bn<BF16, 4>(BN, a, b, y, prm, grid, smem, st);
         default: return launch_tc_bn<BF16, 1>(BN, a, b, y, prm, grid, smem, st);
     }
 }
@@ -681,7 +899,8 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     const int n_cchunks = d.CP / kTcBlockK;
     const int b_chunk = d.BN * kTcBlockK * 2;
     const bool halo = amode == 2;
-    const bool grid_rows = amode == 1 || amode == 2;
+    const bool halo4 = amode == 4;                 // halo tiles built from NCHW X in the kernel
+    const bool grid_rows = amode == 1 || amode == 2 || halo4;
     const bool gemm1x1 = amode == 3;
     const int n_pt = (d.H * d.W + kTcBlockM - 1) / kTcBlockM;   // 1x1 GEMM: pixel tiles per image
     const int n_n_tiles = (d.Co + d.BN - 1) / d.BN;
@@ -722,12 +941,39 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
         b_res = stages >= 3;
     }
     if (!b_res) plan(budget, false, kpb, a_rows, stages);
-    if (stages < 2) return CONV2D_ERR_UNSUPPORTED;
-    const int stage_bytes = group * a_rows * 128 + (b_res ? 0 : kpb * b_chunk);
+    int stage_bytes = group * a_rows * 128 + (b_res ? 0 : kpb * b_chunk);
+    // MODE 4: A ring of halo regions (two stages), B streamed (>= 3 stages)
+    // or resident; the largest filter-row group whose halo fits.
+    int khg = 0, halo_rows = 0, a_stage_bytes = 0;
+    const int a_stages4 = 2;
+    if (halo4) {
+        b_res = false;
+        stages = 0;
+        for (int g = d.Kh; g >= 1 && !khg; --g) {
+            const int rows = (kTcBlockM + (g - 1) * d.Wq + d.Kw - 1 + 7) / 8 * 8;
+            const int ast = group * rows * 128;
+            if (n_n_tiles == 1 && a_stages4 * ast + bres_bytes <= budget) {
+                b_res = true;
+                stages = 1;
+            } else if (a_stages4 * ast + 3 * b_chunk <= budget) {
+                stages = (budget - a_stages4 * ast) / b_chunk;
+                if (stages > kMaxStages) stages = kMaxStages;
+            } else {
+                continue;
+            }
+            khg = g; halo_rows = rows; a_stage_bytes = ast;
+        }
+        if (!khg) return CONV2D_ERR_UNSUPPORTED;
+        stage_bytes = b_chunk;
+        kpb = 1;
+    }
+    if (stages < (halo4 ? 1 : 2)) return CONV2D_ERR_UNSUPPORTED;
     const int n_acc = 2 * kIssuers * d.BN <= 512 ? 2 : 1;
 
     CUresult r;
-    if (im2win) {
+    if (halo4) {
+        r = CUDA_SUCCESS;            // A is built in the kernel; amap is set to bmap below (unused)
+    } else if (im2win) {
         // Window tensor rows of Ck elements, Wq*s per image row: virtual row q
         // starts s*Ck elements after row q-1 and spans Kw*Ck elements.  Rows
         // at or past m_end read as zero, so no copy runs off the tensor's end.
@@ -782,7 +1028,7 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
         r = enc_tiled(&bmap, dt, 2, const_cast<void*>(wq), bdims, bstr, bbox, bestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    } else if (grid_rows) {
+    } else if (grid_rows && !halo4) {
         cuuint64_t bdims[3] = {(cuuint64_t)d.CP, (cuuint64_t)d.Co, (cuuint64_t)d.taps};
         cuuint64_t bstr[2] = {(cuuint64_t)d.taps * d.CP * 2, (cuuint64_t)d.CP * 2};
         cuuint32_t bbox[3] = {(cuuint32_t)kTcBlockK, (cuuint32_t)d.BN, (cuuint32_t)kpb};
@@ -815,6 +1061,7 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
     } else {
+        if (halo4) amap = bmap;
         ymap = amap;   // unused by the other modes
     }
 
@@ -841,6 +1088,20 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     prm.taps = d.taps;
     prm.b_res = b_res ? 1 : 0;
     prm.b_res_off = stages * stage_bytes;
+    if (halo4) {
+        // [B ring][A ring][resident filter][epilogue][barriers]
+        prm.a_ring_off = (int)align_up((size_t)(b_res ? 0 : stages * stage_bytes), 1024);
+        prm.a_stages = a_stages4;
+        prm.a_stage_bytes = a_stage_bytes;
+        prm.a_bytes = halo_rows * 128;
+        prm.halo_rows = halo_rows;
+        prm.khg = khg;
+        prm.n_khg = (d.Kh + khg - 1) / khg;
+        prm.b_res_off = prm.a_ring_off + a_stages4 * a_stage_bytes;
+        prm.x = src;
+        prm.Ci = d.Ci; prm.H = d.H; prm.W = d.W;
+        prm.vecw = d.halo_v;
+    }
     prm.epi_off = prm.b_res_off + (b_res ? bres_bytes : 0);
     prm.n_pt = n_pt;
     prm.y = y;

@@ -31,6 +31,9 @@ struct conv2d_desc {
     int BN;               // output channels per MMA tile (64, 128 or 256)
     bool gemm1x1;         // implicit path on a 1x1, stride-1, unpadded NCHW layer with Ci and H*W multiples
                           // of 8: one GEMM per image straight on the caller's X and filter (no copies)
+    bool nchw_halo;       // implicit path on NCHW input, stride 1: the contraction kernel builds its operand
+                          // tiles from X itself (no input copy; workspace = the repacked filter)
+    int halo_v;           // pixels per vector load of X in that kernel (W % halo_v == 0, Wq % halo_v == 0)
     int Hp, Wq;           // virtual pixel grid [N][Hp][Wq] of the grid-row tensor-core paths.  Padded:
                           // H+2p rows of pitch W+2p (rounded up to 4 when Wo % 4 == 0).  im2win: Ho rows
                           // of Wq output slots (window tensor rows hold Wq*s columns)
@@ -84,6 +87,7 @@ conv2d_status launch_conv_fp32(const conv2d_desc& d, const float* src, const flo
 conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* wq, void* y, int amode,
                              cudaStream_t st);
 int device_sm_count();
+bool halo_plan_fits(const conv2d_desc& d);
 void* driver_entry(const char* name);
 cudaError_t status_read_clear_tc(cudaStream_t st, uint32_t* out);
 cudaError_t status_read_clear_fp32(cudaStream_t st, uint32_t* out);
