@@ -16,7 +16,8 @@ namespace {
 constexpr long long kMaxElems = 0x7fffffffLL;   // kernels index tensors with 32-bit element counts
 
 bool is_tc(conv2d_algo a) {
-    return a == CONV2D_ALGO_IM2WIN_TC || a == CONV2D_ALGO_IMPLICIT_TC || a == CONV2D_ALGO_PADDED_TC;
+    return a == CONV2D_ALGO_IM2WIN_TC || a == CONV2D_ALGO_IMPLICIT_TC || a == CONV2D_ALGO_PADDED_TC ||
+           a == CONV2D_ALGO_IMPLICIT_NCHW_TC;
 }
 
 // Padded algorithm geometry: row pitch W+2p, rounded up to 4 when Wo % 4 == 0
@@ -113,6 +114,8 @@ conv2d_status finalize(conv2d_desc& d) {
     } else {
         const bool im2win = d.algo == CONV2D_ALGO_IM2WIN_TC;
         const bool padded = d.algo == CONV2D_ALGO_PADDED_TC;
+        if (d.algo == CONV2D_ALGO_IMPLICIT_NCHW_TC && (d.s != 1 || d.layout != CONV2D_LAYOUT_NCHW))
+            return CONV2D_ERR_UNSUPPORTED;
         if (padded) {
             if (d.s != 1 || d.layout != CONV2D_LAYOUT_NCHW) return CONV2D_ERR_UNSUPPORTED;
         } else if (!tc_shape_ok(d, im2win)) {
@@ -136,7 +139,7 @@ conv2d_status finalize(conv2d_desc& d) {
         // divides W; the pitch is W + 2p rounded up to it (and to 4 when Wo % 4
         // == 0 for the 8-byte stores); the narrowest pitch wins.
         d.nchw_halo = false;
-        if (d.algo == CONV2D_ALGO_IMPLICIT_TC && d.layout == CONV2D_LAYOUT_NCHW && !d.gemm1x1 && d.s == 1) {
+        if (d.algo == CONV2D_ALGO_IMPLICIT_NCHW_TC) {
             int best_v = 0, best_wq = 0;
             for (int v = 8; v >= 1; v /= 2) {
                 if (d.W % v) continue;
@@ -149,6 +152,7 @@ conv2d_status finalize(conv2d_desc& d) {
             d.Hp = d.H + 2 * d.p;
             const long long rows = (long long)d.N * d.Hp * d.Wq;
             d.nchw_halo = rows + (long long)d.Kh * d.Wq + d.Kw + kTcBlockM <= kMaxElems && halo_plan_fits(d);
+            if (!d.nchw_halo) return CONV2D_ERR_UNSUPPORTED;
         }
         if ((long long)d.Ci * d.Kh * d.Kw > 16384) return CONV2D_ERR_UNSUPPORTED;   // per-channel filter staging
         if (d.N > 65535) return CONV2D_ERR_UNSUPPORTED;
@@ -192,7 +196,7 @@ CONV2D_API conv2d_status conv2d_desc_create(conv2d_desc_t* out, int N, int Cin, 
     if (N < 1 || Cin < 1 || H < 1 || W < 1 || Cout < 1 || Kh < 1 || Kw < 1 || stride < 1 || pad < 0)
         return CONV2D_ERR_BAD_PARAM;
     if (dtype != CONV2D_F32 && dtype != CONV2D_F16 && dtype != CONV2D_BF16) return CONV2D_ERR_BAD_PARAM;
-    if (algo < CONV2D_ALGO_AUTO || algo > CONV2D_ALGO_PADDED_TC) return CONV2D_ERR_BAD_PARAM;
+    if (algo < CONV2D_ALGO_AUTO || algo > CONV2D_ALGO_IMPLICIT_NCHW_TC) return CONV2D_ERR_BAD_PARAM;
     const long long Hp = (long long)H + 2LL * pad, Wp = (long long)W + 2LL * pad;
     if (Hp < Kh || Wp < Kw || Wp > 0x7fffffffLL) return CONV2D_ERR_BAD_PARAM;
     const long long Ho = (Hp - Kh) / stride + 1, Wo = (Wp - Kw) / stride + 1;
@@ -317,11 +321,6 @@ conv2d_status fwd_impl(conv2d_desc_t dp, const void* x, const void* w, void* y, 
                 break;
             }
             e = launch_pack_filter_tc(w, wq, d, false, st);
-            if (d.nchw_halo) {   // the kernel reads NCHW X itself
-                if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
-                if (e == cudaSuccess) s = launch_conv_tc(d, x, wq, y, 4, st);
-                break;
-            }
             const void* src = x;
             if (e == cudaSuccess && d.layout == CONV2D_LAYOUT_NCHW) {
                 e = launch_nchw_to_nhwc16(x, win, d.N, d.Ci, d.H, d.W, d.Ci8, st);
@@ -331,6 +330,11 @@ conv2d_status fwd_impl(conv2d_desc_t dp, const void* x, const void* w, void* y, 
             if (e == cudaSuccess) s = launch_conv_tc(d, src, wq, y, 0, st);
             break;
         }
+        case CONV2D_ALGO_IMPLICIT_NCHW_TC:   // the contraction kernel reads NCHW X itself
+            e = launch_pack_filter_tc(w, wq, d, false, st);
+            if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
+            if (e == cudaSuccess) s = launch_conv_tc(d, x, wq, y, 4, st);
+            break;
         case CONV2D_ALGO_PADDED_TC:
             e = launch_pack_filter_tc(w, wq, d, false, st);
             if (e == cudaSuccess) e = launch_nchw_to_padded_nhwc16(x, win, d, st);

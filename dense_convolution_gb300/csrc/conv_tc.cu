@@ -91,6 +91,10 @@ struct TcParams {
     int halo_rows;      // rows (pixels) of one halo region, a multiple of 8
     int a_stages, a_stage_bytes, a_ring_off;
     int vecw;           // pixels per vector load (W % vecw == 0, Wq % vecw == 0)
+    int staged;         // 1: X arrives by TMA boxes of kSeg pixels x 64 channels into per-warp
+                        //    staging slots (H*W % 8 == 0); 0: builder lanes load X themselves
+    int n_slots;        // staging slots per builder warp
+    int stg_off;        // staging region (slots, then a 128-byte discard row per warp)
 };
 
 // Bias of output channel co, widened to fp32.
@@ -145,6 +149,124 @@ __device__ __forceinline__ void load_pixels(const uint16_t* src, uint32_t (&d)[4
 }
 
 constexpr int kBuildBatch = 8;   // vector groups whose loads a builder lane keeps in flight
+constexpr int kSeg = 56;         // staged pixels per TMA box (112-byte rows: conflict-free ldmatrix rows)
+constexpr int kSegBytes = kSeg * kTcBlockK * 2;
+constexpr int kMaxSlots = 2;
+
+// Build this warp's share of one A stage from TMA-staged X (H*W % 8 == 0).
+// The stage needs the padded pixels [Pa, Pb) of the virtual grid; their image
+// rows are read as runs of whole input rows, flat along the image (n, ci, HW),
+// in boxes of kSeg pixels x 64 channels (copy-engine zero fill past HW and Ci).
+// Segment k of the stage goes to builder warp k % 4, through this warp's
+// staging slots (copies of later segments in flight while one is transposed).
+// A box is transposed 8 pixels x 32 channels at a time (ldmatrix .trans) and
+// stored as 16-byte channel chunks of the halo rows of every tile that holds
+// the pixel (stmatrix; a lane whose pixel no tile needs writes a discard row).
+// Rows of padding, pitch junk and images past N are written as zeros.
+__device__ __forceinline__ void build_halo_stage_staged(const TcParams& prm, const CUtensorMap* xmap, int tw,
+                                                        int lane, uint32_t stage_base, uint32_t slot_base,
+                                                        uint32_t slot_bar0, uint32_t& slot_phases, uint32_t discard,
+                                                        int mt0, int n_val, int cb, int kg) {
+    const int R = prm.halo_rows, Wq = prm.Wq, Hp = prm.HpWq / prm.Wq, HW = prm.H * prm.W;
+    const int off = kg * prm.khg * Wq;
+    const int Pa = mt0 * kTcBlockM + off, Pb = (mt0 + n_val - 1) * kTcBlockM + off + R;
+    const int Y_lo = Pa / Wq, Y_hi = (Pb - 1) / Wq;         // padded rows n*Hp + yy of the stage
+    const int n_lo = Y_lo / Hp, n_hi = min(Y_hi / Hp, prm.N - 1);
+    // Segments per image: input rows iy_lo..iy_hi, flat [iy_lo*W, (iy_hi+1)*W) from a multiple of 8.
+    auto image_rows = [&](int n, int& f0, int& f1) {
+        const int ylo = max(Y_lo - n * Hp, 0) - prm.p, yhi = min(Y_hi - n * Hp, Hp - 1) - prm.p;
+        const int ia = max(ylo, 0), ib = min(yhi, prm.H - 1);
+        if (ia > ib) { f0 = f1 = 0; return 0; }
+        f0 = (ia * prm.W) & ~7;
+        f1 = (ib + 1) * prm.W;
+        return (f1 - f0 + kSeg - 1) / kSeg;
+    };
+    int total = 0;
+    for (int n = n_lo; n <= n_hi; ++n) { int a, b; total += image_rows(n, a, b); }
+    auto seg_at = [&](int k, int& n_out, int& x_out) {
+        for (int n = n_lo; n <= n_hi; ++n) {
+            int f0, f1;
+            const int c = image_rows(n, f0, f1);
+            if (k < c) { n_out = n; x_out = f0 + k * kSeg; return; }
+            k -= c;
+        }
+        n_out = 0; x_out = 0;
+    };
+    const int n_slots = prm.n_slots;
+    auto issue = [&](int k, int slot) {
+        int n, x;
+        seg_at(k, n, x);
+        if (lane == 0) {
+            const uint32_t bar = slot_bar0 + 8u * (uint32_t)slot;
+            fence_proxy_async_smem();                    // earlier ldmatrix reads of the slot come first
+            mbar_arrive_expect_tx(bar, (uint32_t)kSegBytes);
+            tma_load_3d(slot_base + (uint32_t)(slot * kSegBytes), xmap, bar, x, cb * kTcBlockK, n);
+        }
+    };
+    int k_issue = tw;
+    for (int sl = 0; sl < n_slots && k_issue < total; ++sl, k_issue += kTransposerWarps) issue(k_issue, sl);
+
+    // Zero rows while the copies are in flight: padded rows Y_lo + tw, + 4, ...
+    for (int Y = Y_lo + tw; Y <= Y_hi; Y += kTransposerWarps) {
+        const int n = Y / Hp, yy = Y - n * Hp;
+        const bool blank = n >= prm.N || yy < prm.p || yy >= prm.p + prm.H;
+        for (int run = 0; run < 2; ++run) {
+            const int c0 = blank ? (run ? Wq : 0) : (run ? prm.p + prm.W : 0);
+            const int c1 = blank ? Wq : (run ? Wq : prm.p);
+            if (c0 >= c1) continue;
+            for (int i = 0; i < n_val; ++i) {
+                const int base = (mt0 + i) * kTcBlockM + off;
+                const int r0 = max(Y * Wq + c0 - base, 0), r1 = min(Y * Wq + c1 - base, R);
+                const uint32_t tile = stage_base + (uint32_t)(i * prm.a_bytes);
+                for (int t = lane; t < (r1 - r0) * 8; t += 32)
+                    st_shared_v4(tile + (uint32_t)(r0 + (t >> 3)) * 128u + (uint32_t)(t & 7) * 16u, 0u, 0u, 0u, 0u);
+            }
+        }
+    }
+
+    int slot = 0;
+    for (int k = tw; k < total; k += kTransposerWarps) {
+        int n, x;
+        seg_at(k, n, x);
+        const uint32_t bar = slot_bar0 + 8u * (uint32_t)slot;
+        mbar_drain_wait(bar, (slot_phases >> slot) & 1u);   // this warp's own copy: it always lands
+        slot_phases ^= 1u << slot;
+        const uint32_t sbase = slot_base + (uint32_t)(slot * kSegBytes);
+        const int j = lane & 7;
+        for (int b = 0; b < kSeg / 8; ++b) {
+            const int f = x + 8 * b + j;
+            int r[kIssuers];
+            bool any = false;
+            const int iy = f / prm.W, ix = f - iy * prm.W;
+            const int P = n * prm.HpWq + (iy + prm.p) * Wq + ix + prm.p;
+#pragma unroll
+            for (int i = 0; i < kIssuers; ++i) {
+                r[i] = P - ((mt0 + i) * kTcBlockM + off);
+                const bool in = i < n_val && f < HW && r[i] >= 0 && r[i] < R;
+                if (!in) r[i] = -1;
+                any |= in;
+            }
+            if (!__any_sync(0xffffffffu, any)) continue;
+            uint32_t q[2][4];
+            ldsm_x4_trans(sbase + (uint32_t)lane * (kSeg * 2) + 16u * b, q[0]);
+            ldsm_x4_trans(sbase + (uint32_t)(lane + 32) * (kSeg * 2) + 16u * b, q[1]);
+            const uint32_t mm = (uint32_t)(lane >> 3);
+#pragma unroll
+            for (int i = 0; i < kIssuers; ++i) {
+                if (i >= n_val) break;
+                const uint32_t tile = stage_base + (uint32_t)(i * prm.a_bytes);
+                const uint32_t row = tile + (uint32_t)r[i] * 128u;
+                const uint32_t ph = (uint32_t)(r[i] & 7);
+                stsm_x4(r[i] >= 0 ? row + ((mm ^ ph) << 4) : discard, q[0]);
+                stsm_x4(r[i] >= 0 ? row + (((mm + 4u) ^ ph) << 4) : discard, q[1]);
+            }
+        }
+        __syncwarp();
+        if (k_issue < total) { issue(k_issue, slot); k_issue += kTransposerWarps; }
+        if (++slot == n_slots) slot = 0;
+    }
+}
+
 
 // Build this warp's share of one A stage: for each valid tile i of the group,
 // halo_rows rows of 64 channels (chunk cb) in the 128-byte-swizzled K-major
@@ -239,7 +361,9 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
     const int nacc = prm.n_acc;
     // MODE 4 A ring: afull[0..kMaxAStages), aempty[0..kMaxAStages) after the drain barriers.
     uint64_t* abars = bars + 2 * S + 2 * kIssuers * nacc + 1 + kIssuers;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(abars + 2 * kMaxAStages);
+    // MODE 4 staging: one barrier per (builder warp, slot) after those.
+    uint64_t* sbars = abars + 2 * kMaxAStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbars + kTransposerWarps * kMaxSlots);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -262,6 +386,7 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                 mbar_init(smem_addr(&abars[i]), kTransposerWarps);          // one arrive per builder warp
                 mbar_init(smem_addr(&abars[kMaxAStages + i]), prm.group);    // one commit per issuer
             }
+            for (int i = 0; i < kTransposerWarps * kMaxSlots; ++i) mbar_init(smem_addr(&sbars[i]), 1);
         }
         *abort_flag = 0;
         mbar_fence_init();
@@ -767,8 +892,12 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
         if constexpr (MODE == 4) {
             const int tw = warp - kTcThreads / 32;
             int a_stage = 0;
-            uint32_t a_phase = 0;
+            uint32_t a_phase = 0, slot_phases = 0;
             bool ok = true;
+            const uint32_t slot_base = smem_addr(smem + prm.stg_off + tw * prm.n_slots * kSegBytes);
+            const uint32_t discard =
+                smem_addr(smem + prm.stg_off + kTransposerWarps * prm.n_slots * kSegBytes + tw * 128);
+            const uint32_t slot_bar0 = smem_addr(&sbars[tw * kMaxSlots]);
             for (int g = blockIdx.x; g < prm.n_groups && ok; g += gridDim.x) {
                 const int mt0 = (g / prm.n_n_tiles) * prm.group;
                 int n_val = 0;
@@ -780,7 +909,10 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                             break;
                         }
                         const uint32_t base = smem_addr(smem + prm.a_ring_off + a_stage * prm.a_stage_bytes);
-                        switch (prm.vecw) {
+                        if (prm.staged) {
+                            build_halo_stage_staged(prm, &amap, tw, lane, base, slot_base, slot_bar0, slot_phases,
+                                                    discard, mt0, n_val, cb, kg);
+                        } else switch (prm.vecw) {
                             case 8: build_halo_stage<8>(prm, tw, lane, base, mt0, n_val, cb, kg); break;
                             case 4: build_halo_stage<4>(prm, tw, lane, base, mt0, n_val, cb, kg); break;
                             case 2: build_halo_stage<2>(prm, tw, lane, base, mt0, n_val, cb, kg); break;
@@ -823,7 +955,8 @@ cudaError_t wait_limit_set_tc(cudaStream_t st, uint64_t ns) { return wait_limit_
 bool halo_plan_fits(const conv2d_desc& d) {
     const int rows = (kTcBlockM + d.Kw - 1 + 7) / 8 * 8;
     const int budget = kSmemLimit - 1024 - kEpiBytes - kBarBytes;
-    return 2 * (kIssuers * rows * 128) + 3 * d.BN * kTcBlockK * 2 <= budget;
+    const int stg = ((long long)d.H * d.W) % 8 == 0 ? kTransposerWarps * (kSegBytes + 128) : 0;
+    return 2 * (kIssuers * rows * 128) + 3 * d.BN * kTcBlockK * 2 + stg <= budget;
 }
 
 int device_sm_count() {
@@ -944,24 +1077,30 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     int stage_bytes = group * a_rows * 128 + (b_res ? 0 : kpb * b_chunk);
     // MODE 4: A ring of halo regions (two stages), B streamed (>= 3 stages)
     // or resident; the largest filter-row group whose halo fits.
-    int khg = 0, halo_rows = 0, a_stage_bytes = 0;
+    int khg = 0, halo_rows = 0, a_stage_bytes = 0, n_slots = 0, stg_bytes = 0;
     const int a_stages4 = 2;
+    const bool staged = halo4 && ((long long)d.H * d.W) % 8 == 0;   // flat TMA boxes need a 16-byte plane pitch
     if (halo4) {
         b_res = false;
         stages = 0;
+        // Largest filter-row group first; two staging slots per builder warp
+        // before one; a resident filter before a streamed one.
         for (int g = d.Kh; g >= 1 && !khg; --g) {
             const int rows = (kTcBlockM + (g - 1) * d.Wq + d.Kw - 1 + 7) / 8 * 8;
             const int ast = group * rows * 128;
-            if (n_n_tiles == 1 && a_stages4 * ast + bres_bytes <= budget) {
-                b_res = true;
-                stages = 1;
-            } else if (a_stages4 * ast + 3 * b_chunk <= budget) {
-                stages = (budget - a_stages4 * ast) / b_chunk;
-                if (stages > kMaxStages) stages = kMaxStages;
-            } else {
-                continue;
+            for (int ns = staged ? kMaxSlots : 0; ns >= (staged ? 1 : 0) && !khg; --ns) {
+                const int stg = staged ? (kTransposerWarps * (ns * kSegBytes + 128) + 1023) / 1024 * 1024 : 0;
+                if (n_n_tiles == 1 && a_stages4 * ast + bres_bytes + stg <= budget) {
+                    b_res = true;
+                    stages = 1;
+                } else if (a_stages4 * ast + 3 * b_chunk + stg <= budget) {
+                    stages = (budget - a_stages4 * ast - stg) / b_chunk;
+                    if (stages > kMaxStages) stages = kMaxStages;
+                } else {
+                    continue;
+                }
+                khg = g; halo_rows = rows; a_stage_bytes = ast; n_slots = ns; stg_bytes = stg;
             }
-            khg = g; halo_rows = rows; a_stage_bytes = ast;
         }
         if (!khg) return CONV2D_ERR_UNSUPPORTED;
         stage_bytes = b_chunk;
@@ -972,7 +1111,19 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
 
     CUresult r;
     if (halo4) {
-        r = CUDA_SUCCESS;            // A is built in the kernel; amap is set to bmap below (unused)
+        // A is built in the kernel.  Staged builders read X as [N][Ci][H*W] in
+        // boxes of kSeg pixels x 64 channels (zero past H*W and Ci, no swizzle).
+        r = CUDA_SUCCESS;
+        if (staged) {
+            const cuuint64_t P = (cuuint64_t)d.H * d.W;
+            cuuint64_t xdims[3] = {P, (cuuint64_t)d.Ci, (cuuint64_t)d.N};
+            cuuint64_t xstr[2] = {P * 2, P * 2 * (cuuint64_t)d.Ci};
+            cuuint32_t xbox[3] = {(cuuint32_t)kSeg, (cuuint32_t)kTcBlockK, 1};
+            cuuint32_t xestr[3] = {1, 1, 1};
+            r = enc_tiled(&amap, dt, 3, const_cast<void*>(src), xdims, xstr, xbox, xestr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        }
     } else if (im2win) {
         // Window tensor rows of Ck elements, Wq*s per image row: virtual row q
         // starts s*Ck elements after row q-1 and spans Kw*Ck elements.  Rows
@@ -1061,7 +1212,7 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
     } else {
-        if (halo4) amap = bmap;
+        if (halo4 && !staged) amap = bmap;   // unused
         ymap = amap;   // unused by the other modes
     }
 
@@ -1097,7 +1248,10 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
         prm.halo_rows = halo_rows;
         prm.khg = khg;
         prm.n_khg = (d.Kh + khg - 1) / khg;
-        prm.b_res_off = prm.a_ring_off + a_stages4 * a_stage_bytes;
+        prm.stg_off = prm.a_ring_off + a_stages4 * a_stage_bytes;
+        prm.staged = staged ? 1 : 0;
+        prm.n_slots = n_slots;
+        prm.b_res_off = prm.stg_off + stg_bytes;
         prm.x = src;
         prm.Ci = d.Ci; prm.H = d.H; prm.W = d.W;
         prm.vecw = d.halo_v;

@@ -82,6 +82,15 @@ typedef enum { CONV2D_F32 = 0, CONV2D_F16 = 1, CONV2D_BF16 = 2 } conv2d_dtype;
  *                   tap's operand tile is one tiled TMA box at a constant
  *                   shift (kh*pitch + kw) and the outputs at padded positions
  *                   are discarded.  Workspace: repacked filter + padded copy.
+ *  IMPLICIT_NCHW_TC fp16/bf16 on tcgen05 tensor cores, stride 1, NCHW input:
+ *                   the implicit expansion done inside the contraction kernel
+ *                   with no copy of X ("im2col Expansion, FFT Convolution, and
+ *                   Winograd Transforms", im2col section: the indexing lives
+ *                   in the GEMM's load path).  The kernel reads X in place and
+ *                   builds each zero-padded channels-last operand tile in
+ *                   shared memory; every tap of a filter-row group reads that
+ *                   tile at a row offset.  Workspace: the repacked filter
+ *                   only; two launches (repack, contraction).
  *  AUTO             resolved per shape when the descriptor is created
  *                   (conv2d_get_algo reports the choice). */
 typedef enum {
@@ -90,7 +99,8 @@ typedef enum {
     CONV2D_ALGO_IM2WIN_TC = 2,
     CONV2D_ALGO_IMPLICIT_TC = 3,
     CONV2D_ALGO_IMPLICIT_FP32_CC = 4,
-    CONV2D_ALGO_PADDED_TC = 5
+    CONV2D_ALGO_PADDED_TC = 5,
+    CONV2D_ALGO_IMPLICIT_NCHW_TC = 6
 } conv2d_algo;
 
 /* Memory layout of X.  Y is always NCHW.  W is always [Cout][Cin][Kh][Kw]. */

@@ -99,33 +99,17 @@ def test_auto_choices_and_workspace(capi):
                 assert ws >= N * (H + 2 * p) * wq * ci8 * 2    # zero-padded channels-last copy of X
             if algo == "implicit_tc":
                 ci8 = (Ci + 7) // 8 * 8
+                assert ws >= N * H * W * ci8 * 2          # channels-last copy of X
+                # The copy never exceeds the im2win tensor (equal for 1x1 layers);
+                # the repacked filter comes on top.
                 packed = Co * Kh * Kw * ((ci8 + 63) // 64 * 64) * 2
-                if s == 1:
-                    # Stride 1 on NCHW input: the kernel builds its operand tiles from X
-                    # itself; the workspace is the repacked filter alone, two launches.
-                    assert ws == packed, name
-                    assert capi.conv2d_launches_per_call(d) == 2
-                else:
-                    assert ws >= N * H * W * ci8 * 2          # channels-last copy of X
-                    # The copy never exceeds the im2win tensor (equal for 1x1 layers);
-                    # the repacked filter comes on top.
-                    assert ws <= im2win_tensor + packed + 1024
+                assert ws <= im2win_tensor + packed + 1024
         finally:
             capi.conv2d_desc_destroy(d)
 
 
 def test_nhwc_layout_drops_input_copy(capi):
-    # Stride 1: NCHW input is read in place too, both layouts need the packed filter only.
     d = capi.conv2d_desc_create(8, 64, 28, 28, 64, 3, 3, 1, 1, "f16", "implicit_tc")
-    try:
-        nchw = capi.conv2d_workspace_size(d)
-        capi.conv2d_desc_set_input_layout(d, "nhwc")
-        nhwc = capi.conv2d_workspace_size(d)
-        assert nhwc == nchw == 64 * 9 * 64 * 2
-    finally:
-        capi.conv2d_desc_destroy(d)
-    # Stride 2: NCHW input takes a channels-last copy, NHWC input none.
-    d = capi.conv2d_desc_create(8, 64, 28, 28, 64, 3, 3, 2, 1, "f16", "implicit_tc")
     try:
         nchw = capi.conv2d_workspace_size(d)
         capi.conv2d_desc_set_input_layout(d, "nhwc")
@@ -201,10 +185,6 @@ def test_one_by_one_gemm_selection(capi, shape, dtype, gemm):
         n = capi.conv2d_launches_per_call(d)
         if gemm:
             assert ws == 0 and n == 1
-        elif shape[7] == 1:
-            # Stride 1: the contraction builds its operand tiles from NCHW X itself
-            # (filter repack + contraction; workspace = the repacked filter).
-            assert ws > 0 and n == 2
         else:
             assert ws > 0 and n == 3
         # An NHWC input (Ci % 8 == 0 only) never takes the in-place GEMM, which
@@ -266,3 +246,27 @@ def test_output_dtype_and_bias_setters(capi):
     finally:
         capi.conv2d_desc_destroy(d16)
         capi.conv2d_desc_destroy(d32)
+
+
+@pytest.mark.parametrize("shape,dtype", [((32, 64, 56, 56, 64, 3, 3, 1, 1), "f16"),
+                                         ((64, 512, 28, 28, 512, 3, 3, 1, 1), "bf16"),
+                                         ((1, 13, 11, 13, 17, 3, 5, 1, 2), "f16"),
+                                         ((2, 64, 16, 16, 130, 1, 1, 1, 0), "f16")])
+def test_implicit_nchw_needs_only_the_packed_filter(capi, shape, dtype):
+    """The implicit GEMM that reads NCHW X in the contraction kernel: workspace =
+    the repacked filter, two launches; stride > 1, NHWC input and fp32 are refused."""
+    N, Ci, H, W, Co, Kh, Kw, s, p = shape
+    d = capi.conv2d_desc_create(*shape, dtype, "implicit_nchw_tc")
+    try:
+        ci8 = (Ci + 7) // 8 * 8
+        assert capi.conv2d_workspace_size(d) == Co * Kh * Kw * ((ci8 + 63) // 64 * 64) * 2
+        assert capi.conv2d_launches_per_call(d) == 2
+        assert capi.conv2d_get_algo(d) == "implicit_nchw_tc"
+        with pytest.raises(capi.Conv2dError) as e:
+            capi.conv2d_desc_set_input_layout(d, "nhwc")
+        assert e.value.status == capi.ERR_UNSUPPORTED
+    finally:
+        capi.conv2d_desc_destroy(d)
+    for bad, status in (((N, Ci, H, W, Co, Kh, Kw, 2, p), "f16"), (shape, "f32")):
+        with pytest.raises(capi.Conv2dError):
+            capi.conv2d_desc_create(*bad, status, "implicit_nchw_tc")

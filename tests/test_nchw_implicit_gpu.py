@@ -58,11 +58,11 @@ def test_nchw_implicit_whole_output(shape, dtype):
     X, X64 = synth.round_to(synth.normal(seed, 0, (N, Ci, H, W)), dtype)
     Wt, W64 = synth.round_to(synth.normal(seed, 1, (Co, Ci, Kh, Kw), (2.0 / (Ci * Kh * Kw)) ** 0.5), dtype)
     Y, S = oracle_full(X64, W64, 1, p)
-    y, used, ws = run_gpu(X, Wt, 1, p, dtype, "implicit_tc")
-    assert used == "implicit_tc" and ws == _packed_bytes(Ci, Co, Kh, Kw)
+    y, used, ws = run_gpu(X, Wt, 1, p, dtype, "implicit_nchw_tc")
+    assert used == "implicit_nchw_tc" and ws == _packed_bytes(Ci, Co, Kh, Kw)
     err, bad0 = parity(y, Y, S)
     assert bad0 == 0 and err <= TOL[dtype], (shape, dtype, err)
-    d = capi.conv2d_desc_create(N, Ci, H, W, Co, Kh, Kw, 1, p, dtype, "implicit_tc")
+    d = capi.conv2d_desc_create(N, Ci, H, W, Co, Kh, Kw, 1, p, dtype, "implicit_nchw_tc")
     try:
         assert capi.conv2d_launches_per_call(d) == 2
     finally:
@@ -82,6 +82,6 @@ def test_nchw_implicit_small_integers_bit_exact(shape, dtype):
     assert np.max(np.abs(Y)) < 2048
     t = torch.from_numpy(Y.astype(np.float32))
     expect = (t.half() if dtype == "f16" else t.bfloat16()).double().numpy()
-    y, _, _ = run_gpu(d["X"], d["W"], 1, p, dtype, "implicit_tc")
+    y, _, _ = run_gpu(d["X"], d["W"], 1, p, dtype, "implicit_nchw_tc")
     mism = np.argwhere(y != expect)
     assert mism.size == 0, mism[:5].tolist()

@@ -22,18 +22,19 @@ from tests.helpers import TOL, oracle_full, parity, run_gpu
 
 pytestmark = pytest.mark.gpu
 
-ALGOS = {"f32": ["im2win_fp32_cc", "implicit_fp32_cc"], "f16": ["im2win_tc", "implicit_tc", "padded_tc"],
-         "bf16": ["im2win_tc", "implicit_tc", "padded_tc"]}
+ALGOS = {"f32": ["im2win_fp32_cc", "implicit_fp32_cc"],
+         "f16": ["im2win_tc", "implicit_tc", "padded_tc", "implicit_nchw_tc"],
+         "bf16": ["im2win_tc", "implicit_tc", "padded_tc", "implicit_nchw_tc"]}
 REDUCED_N = {"tiny": 1, "resnet_stage1": 2, "stem": 1, "vgg": 1, "sweep_k1": 1, "sweep_k3": 1,
              "sweep_k5": 1, "sweep_k7": 1, "sweep_k9": 1, "sweep_k11": 1, "sweep_k3_s2": 2}
 REDUCED_N.update({f"cv{i}": 1 for i in range(1, 13)})
 
 
 def _supported(wl, algo):
-    """The documented shape limits: the padded path is stride 1 only; the direct
+    """The documented shape limits: the padded and in-kernel NCHW paths are stride 1 only; the direct
     fp32 path needs 16-byte input rows (W % 4 == 0) and its staged rows in one
     copy box (63*s + Kw + 6 <= 256)."""
-    if algo == "padded_tc" and wl.stride != 1:
+    if algo in ("padded_tc", "implicit_nchw_tc") and wl.stride != 1:
         return False
     if algo == "implicit_fp32_cc" and (wl.W % 4 != 0 or 63 * wl.stride + wl.Kw + 6 > 256):
         return False
