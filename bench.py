@@ -217,7 +217,11 @@ def run_gpu(args, rank, world):
     d = synth.make_inputs(wl, dtype)
     xh = (torch.from_numpy(d["X"]) if dtype != "bf16" else d["X"]).contiguous().pin_memory()
     wh = (torch.from_numpy(d["W"]) if dtype != "bf16" else d["W"]).contiguous().pin_memory()
-    op = Conv2d(wl.N, wl.Ci, wl.H, wl.W, wl.Co, wl.Kh, wl.Kw, wl.stride, wl.pad, dtype, args.algo)
+    tuning = {}
+    for kv in filter(None, args.tune.split(",")):
+        k, v = kv.split("=")
+        tuning[k.strip()] = int(v)
+    op = Conv2d(wl.N, wl.Ci, wl.H, wl.W, wl.Co, wl.Kh, wl.Kw, wl.stride, wl.pad, dtype, args.algo, tuning=tuning)
     # Rotating operand sets (X, W, Y, workspace), together >= 3 x L2.
     x0 = xh.to(dev)
     w0 = wh.to(dev)
@@ -384,6 +388,7 @@ def run_gpu(args, rank, world):
                    "l2": f"{n_sets} rotating X/W/Y/workspace sets, {n_sets * set_bytes / 2 ** 20:.0f} MB > 129 MB L2; "
                          "no flush inside the timed region",
                    "workspace_mb": op.workspace_bytes / 2 ** 20,
+                   "tuning": tuning or "automatic",
                    "im2win_tensor_mb": wl.N * wl.Ci * Ho * (wl.W + 2 * wl.pad) * wl.Kh * elem / 2 ** 20,
                    "parallelism": f"independent batch per GPU x{world}"},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
@@ -415,6 +420,8 @@ def main():
     ap.add_argument("--dtype", default=None, choices=list(synth.DTYPES))
     ap.add_argument("--algo", default="auto")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--tune", default="",
+                    help="pipeline knobs for ablations, e.g. stages=1,sync_copies=1,raster=2,no_resident=1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="profiling runs: no CPU baseline, 3 end-to-end steps, no clock-sustain loop")

@@ -21,9 +21,10 @@ ALGOS = {"auto": 0, "im2win_fp32_cc": 1, "im2win_tc": 2, "implicit_tc": 3, "impl
          "implicit_nchw_tc": 6}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 LAYOUTS = {"nchw": 0, "nhwc": 1}
+TUNING = {"stages": 0, "sync_copies": 1, "raster": 2, "no_resident": 3}
 
 EXPORTED = ("conv2d_desc_create", "conv2d_desc_set_input_layout", "conv2d_desc_set_output_dtype",
-            "conv2d_desc_set_bias", "conv2d_desc_destroy", "conv2d_out_dims",
+            "conv2d_desc_set_bias", "conv2d_desc_set_tuning", "conv2d_desc_destroy", "conv2d_out_dims",
             "conv2d_workspace_size", "conv2d_get_algo", "conv2d_fwd", "conv2d_fwd_profiled", "conv2d_fwd_host",
             "conv2d_launches_per_call", "conv2d_fwd_static_workspace", "conv2d_static_workspace_bytes",
             "conv2d_set_wait_limit", "conv2d_device_status", "conv2d_status_string")
@@ -51,6 +52,7 @@ def load(path: str = LIB_PATH):
     L.conv2d_desc_set_input_layout.argtypes = [vp, c_int]
     L.conv2d_desc_set_output_dtype.argtypes = [vp, c_int]
     L.conv2d_desc_set_bias.argtypes = [vp, vp]
+    L.conv2d_desc_set_tuning.argtypes = [vp, c_int, c_int]
     L.conv2d_desc_destroy.argtypes = [vp]
     L.conv2d_out_dims.argtypes = [vp, ctypes.POINTER(c_int), ctypes.POINTER(c_int)]
     L.conv2d_workspace_size.argtypes = [vp, ctypes.POINTER(c_size)]
@@ -102,6 +104,12 @@ def conv2d_desc_set_output_dtype(desc: int, out="f32"):
 def conv2d_desc_set_bias(desc: int, bias: int):
     """Device address of Cout bias values of the input dtype (0 = no bias)."""
     _check(load().conv2d_desc_set_bias(desc, bias or None), "conv2d_desc_set_bias")
+
+
+def conv2d_desc_set_tuning(desc: int, knob, value: int):
+    """Pipeline knob for ablations: "stages", "sync_copies", "raster", "no_resident"."""
+    k = TUNING[knob] if isinstance(knob, str) else int(knob)
+    _check(load().conv2d_desc_set_tuning(desc, k, int(value)), "conv2d_desc_set_tuning")
 
 
 def conv2d_desc_destroy(desc: int):

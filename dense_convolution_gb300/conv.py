@@ -19,7 +19,7 @@ class Conv2d:
     """One problem shape: descriptor, output shape and workspace size."""
 
     def __init__(self, N, Cin, H, W, Cout, Kh, Kw, stride=1, pad=0, dtype="f32", algo="auto", layout="nchw",
-                 out_dtype=None):
+                 out_dtype=None, tuning=None):
         self.shape = (N, Cin, H, W, Cout, Kh, Kw, stride, pad)
         self.dtype = dtype
         self.out_dtype = out_dtype or dtype
@@ -29,6 +29,8 @@ class Conv2d:
             capi.conv2d_desc_set_input_layout(self.desc, layout)
         if self.out_dtype != dtype:
             capi.conv2d_desc_set_output_dtype(self.desc, self.out_dtype)
+        for knob, value in (tuning or {}).items():
+            capi.conv2d_desc_set_tuning(self.desc, knob, value)
         self.Ho, self.Wo = capi.conv2d_out_dims(self.desc)
         self.workspace_bytes = capi.conv2d_workspace_size(self.desc)
         self.algo = capi.conv2d_get_algo(self.desc)

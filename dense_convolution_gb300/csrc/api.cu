@@ -245,6 +245,29 @@ CONV2D_API conv2d_status conv2d_desc_set_bias(conv2d_desc_t d, const void* bias)
     return CONV2D_OK;
 }
 
+CONV2D_API conv2d_status conv2d_desc_set_tuning(conv2d_desc_t d, conv2d_tuning knob, int value) {
+    if (!d) return CONV2D_ERR_NULL_PTR;
+    switch (knob) {
+        case CONV2D_TUNE_STAGES:
+            if (value < 0 || value > 8) return CONV2D_ERR_BAD_PARAM;
+            d->tune_stages = value;
+            return CONV2D_OK;
+        case CONV2D_TUNE_SYNC_COPIES:
+            if (value < 0 || value > 1) return CONV2D_ERR_BAD_PARAM;
+            d->tune_sync_copies = value;
+            return CONV2D_OK;
+        case CONV2D_TUNE_RASTER:
+            if (value < 0 || value > 2) return CONV2D_ERR_BAD_PARAM;
+            d->tune_raster = value;
+            return CONV2D_OK;
+        case CONV2D_TUNE_NO_RESIDENT:
+            if (value < 0 || value > 1) return CONV2D_ERR_BAD_PARAM;
+            d->tune_no_resident = value;
+            return CONV2D_OK;
+    }
+    return CONV2D_ERR_BAD_PARAM;
+}
+
 CONV2D_API conv2d_status conv2d_desc_destroy(conv2d_desc_t d) {
     delete d;
     return CONV2D_OK;

@@ -45,6 +45,7 @@ struct Fp32Params {
     int xs_floats;      // staged-input floats per stage (including read slack)
     int ws_floats;      // filter floats per stage
     const float* bias;  // Co bias values, or null
+    int nst;            // stages in the ring: 2 (copies of chunk k+1 overlap the FMAs of chunk k) or 1
 };
 
 constexpr int kCcCols = 64;    // output columns per block (8 lanes x 8)
@@ -94,8 +95,11 @@ __global__ void __launch_bounds__(128) conv_fp32_kernel(const Fp32Params prm,
     __syncthreads();
     pdl_wait();   // the repacked filter / strips come from the kernels launched just before
 
+    // Stage and barrier parity of chunk k.
+    auto stage_of = [&](int k) { return prm.nst == 2 ? (k & 1) : 0; };
+    auto parity_of = [&](int k) { return (uint32_t)(prm.nst == 2 ? (k >> 1) & 1 : k & 1); };
     auto issue = [&](int k) {
-        const int st = k & 1;
+        const int st = stage_of(k);
         float* xs = smem + st * stage_floats;
         float* ws = xs + prm.xs_floats;
         const uint32_t bar = smem_addr(&bars[st]);
@@ -139,13 +143,13 @@ __global__ void __launch_bounds__(128) conv_fp32_kernel(const Fp32Params prm,
     if (tid == 0) issue(0);
     bool ok = true;
     for (int k = 0; k < prm.n_chunks; ++k) {
-        if (tid == 0 && k + 1 < prm.n_chunks) issue(k + 1);
+        if (prm.nst == 2 && tid == 0 && k + 1 < prm.n_chunks) issue(k + 1);
         // A thread whose wait gives up (or sees another's abort) skips the
         // chunk but still meets the barrier at the end of the iteration; the
         // abort flag, set before that barrier, is then read by all threads
         // alike, so the block leaves the loop together.
-        if (mbar_wait(smem_addr(&bars[k & 1]), (k >> 1) & 1, &abort_flag)) {
-        const float* xs = smem + (k & 1) * stage_floats;
+        if (mbar_wait(smem_addr(&bars[stage_of(k)]), parity_of(k), &abort_flag)) {
+        const float* xs = smem + stage_of(k) * stage_floats;
         const float* ws = xs + prm.xs_floats;
         const int nci = min(prm.chunk, prm.Ci - k * prm.chunk);
         for (int c = 0; c < nci; ++c) {
@@ -199,12 +203,15 @@ __global__ void __launch_bounds__(128) conv_fp32_kernel(const Fp32Params prm,
             // Let the copies of this chunk and of the next one (issued before
             // this chunk's wait) land before the CTA exits.
             if (tid == 0) {
-                mbar_drain_wait(smem_addr(&bars[k & 1]), (k >> 1) & 1);
-                if (k + 1 < prm.n_chunks) mbar_drain_wait(smem_addr(&bars[(k + 1) & 1]), ((k + 1) >> 1) & 1);
+                mbar_drain_wait(smem_addr(&bars[stage_of(k)]), parity_of(k));
+                if (prm.nst == 2 && k + 1 < prm.n_chunks)
+                    mbar_drain_wait(smem_addr(&bars[stage_of(k + 1)]), parity_of(k + 1));
             }
             ok = false;
             break;
         }
+        // One stage: the next chunk's copies start once every warp is done with this one.
+        if (prm.nst == 1 && tid == 0 && k + 1 < prm.n_chunks) issue(k + 1);
     }
     if (!ok) return;
 
@@ -283,6 +290,7 @@ conv2d_status launch_conv_fp32(const conv2d_desc& d, const float* src, const flo
                                cudaStream_t st) {
     Fp32Params prm{};
     prm.src = src; prm.wq = wq; prm.y = y; prm.bias = static_cast<const float*>(d.bias);
+    prm.nst = d.tune_stages == 1 ? 1 : 2;
     prm.N = d.N; prm.Ci = d.Ci; prm.H = d.H; prm.W = d.W; prm.Co = d.Co; prm.Kh = d.Kh; prm.Kw = d.Kw;
     prm.s = d.s; prm.p = d.p; prm.Ho = d.Ho; prm.Wo = d.Wo; prm.Lp = d.Lp;
     prm.BCO = 32 * d.cc_warps;

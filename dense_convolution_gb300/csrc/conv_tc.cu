@@ -95,7 +95,25 @@ struct TcParams {
                         //    staging slots (H*W % 8 == 0); 0: builder lanes load X themselves
     int n_slots;        // staging slots per builder warp
     int stg_off;        // staging region (slots, then a 128-byte discard row per warp)
+    // Ablation knobs (conv2d_desc_set_tuning).
+    int raster;         // tile-group visit order: 0 channel tile fastest, 1 pixel group fastest,
+                        // 2 zig-zag (channel tiles in alternating direction on successive pixel groups)
+    int sync_copies;    // 1: the producer waits for each stage's copies before issuing the next stage
+    int n_mg;           // pixel groups (ceil(n_m_tiles / group))
 };
+
+// Tile group g -> (channel tile nt, pixel group mg) in the chosen raster order.
+// Every role walks g = blockIdx.x, +gridDim.x, ... and maps it the same way.
+__device__ __forceinline__ void tile_of(const TcParams& prm, int g, int& nt, int& mg) {
+    if (prm.raster == 1) {
+        nt = g / prm.n_mg;
+        mg = g - nt * prm.n_mg;
+    } else {
+        mg = g / prm.n_n_tiles;
+        nt = g - mg * prm.n_n_tiles;
+        if (prm.raster == 2 && (mg & 1)) nt = prm.n_n_tiles - 1 - nt;
+    }
+}
 
 // Bias of output channel co, widened to fp32.
 template <bool BF16>
@@ -435,7 +453,9 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                     // A is built by the halo builders; only filter chunks stream
                     // here, one per (channel chunk, tap), in the issuers' order.
                     if (prm.b_res) break;
-                    const int nb0 = (g % prm.n_n_tiles) * BN;
+                    int nt_, mg_;
+                    tile_of(prm, g, nt_, mg_);
+                    const int nb0 = nt_ * BN;
                     const int Kh = prm.taps / prm.Kw;
                     for (int cb = 0; cb < prm.n_cchunks && ok; ++cb)
                         for (int kg = 0; kg < prm.n_khg && ok; ++kg) {
@@ -446,14 +466,19 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                                     mbar_arrive_expect_tx(full_bar(stage), (uint32_t)Cfg::kBBytes);
                                     tma_load_2d(smem_addr(smem + stage * prm.stage_bytes), &bmap, full_bar(stage),
                                                 (kh * prm.Kw + kw) * prm.CP + cb * kTcBlockK, nb0);
+                                    const bool landed =
+                                        !prm.sync_copies || mbar_wait(full_bar(stage), phase, abort_flag);
                                     ++issued;
                                     if (++stage == S) { stage = 0; phase ^= 1; }
+                                    if (!landed) { ok = false; break; }
                                 }
                         }
                     continue;
                 }
-                const int n0 = (g % prm.n_n_tiles) * BN;
-                const int mt0 = (g / prm.n_n_tiles) * prm.group;
+                int nt_, mg_;
+                tile_of(prm, g, nt_, mg_);
+                const int n0 = nt_ * BN;
+                const int mt0 = mg_ * prm.group;
                 int m0[kIssuers], img[kIssuers], ho[kIssuers], wo[kIssuers];
                 bool val[kIssuers];
                 int n_val = 0;
@@ -517,8 +542,10 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                         if constexpr (MODE == 1) tma_load_3d(b_dst, &bmap, full_bar(stage), c0, n0, t);
                         else                     tma_load_2d(b_dst, &bmap, full_bar(stage), t * prm.CP + c0, n0);
                     }
+                    const bool landed = !prm.sync_copies || mbar_wait(full_bar(stage), phase, abort_flag);
                     ++issued;
                     stage = nstage; phase = nphase; free_now = free_next;
+                    if (!landed) { ok = false; break; }   // (the drain below waits for this stage too)
                     if (++cb == prm.n_cchunks) {
                         cb = 0; t += kpb; kw += kpb;
                         if (kw == prm.Kw) { kw = 0; ++kh; }
@@ -668,8 +695,10 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
             const bool got = mbar_wait(accf_bar(eg, acc), acc_phase, abort_flag);
             if (!named_bar_and(1 + eg, 128, got)) break;
             tc_fence_after();
-            const int n0 = (g % prm.n_n_tiles) * BN;
-            const int m0 = ((g / prm.n_n_tiles) * prm.group + eg) * kTcBlockM;
+            int nt_, mg_;
+            tile_of(prm, g, nt_, mg_);
+            const int n0 = nt_ * BN;
+            const int m0 = (mg_ * prm.group + eg) * kTcBlockM;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    (uint32_t)((eg * nacc + acc) * BN);
             if constexpr (MODE == 3) {
@@ -899,7 +928,9 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                 smem_addr(smem + prm.stg_off + kTransposerWarps * prm.n_slots * kSegBytes + tw * 128);
             const uint32_t slot_bar0 = smem_addr(&sbars[tw * kMaxSlots]);
             for (int g = blockIdx.x; g < prm.n_groups && ok; g += gridDim.x) {
-                const int mt0 = (g / prm.n_n_tiles) * prm.group;
+                int nt_, mg_;
+                tile_of(prm, g, nt_, mg_);
+                const int mt0 = mg_ * prm.group;
                 int n_val = 0;
                 for (int i = 0; i < prm.group; ++i) n_val += (mt0 + i < prm.n_m_tiles) ? 1 : 0;
                 for (int cb = 0; cb < prm.n_cchunks && ok; ++cb)
@@ -1069,7 +1100,7 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     const int bres_bytes = n_cchunks * d.taps * b_chunk;
     int kpb = 1, a_rows = kTcBlockM, stages = 0;
     bool b_res = false;
-    if (n_n_tiles == 1 && bres_bytes < budget) {
+    if (n_n_tiles == 1 && bres_bytes < budget && !d.tune_no_resident) {
         plan(budget - bres_bytes, true, kpb, a_rows, stages);
         b_res = stages >= 3;
     }
@@ -1078,7 +1109,7 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     // MODE 4: A ring of halo regions (two stages), B streamed (>= 3 stages)
     // or resident; the largest filter-row group whose halo fits.
     int khg = 0, halo_rows = 0, a_stage_bytes = 0, n_slots = 0, stg_bytes = 0;
-    const int a_stages4 = 2;
+    const int a_stages4 = d.tune_stages == 1 ? 1 : 2;
     const bool staged = halo4 && ((long long)d.H * d.W) % 8 == 0;   // flat TMA boxes need a 16-byte plane pitch
     if (halo4) {
         b_res = false;
@@ -1090,7 +1121,7 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
             const int ast = group * rows * 128;
             for (int ns = staged ? kMaxSlots : 0; ns >= (staged ? 1 : 0) && !khg; --ns) {
                 const int stg = staged ? (kTransposerWarps * (ns * kSegBytes + 128) + 1023) / 1024 * 1024 : 0;
-                if (n_n_tiles == 1 && a_stages4 * ast + bres_bytes + stg <= budget) {
+                if (n_n_tiles == 1 && !d.tune_no_resident && a_stages4 * ast + bres_bytes + stg <= budget) {
                     b_res = true;
                     stages = 1;
                 } else if (a_stages4 * ast + 3 * b_chunk + stg <= budget) {
@@ -1107,6 +1138,10 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
         kpb = 1;
     }
     if (stages < (halo4 ? 1 : 2)) return CONV2D_ERR_UNSUPPORTED;
+    if (d.tune_stages > 0 && stages > d.tune_stages) {   // ablation: a shallower ring
+        stages = d.tune_stages;
+        if (!halo4) stage_bytes = group * a_rows * 128 + (b_res ? 0 : kpb * b_chunk);
+    }
     const int n_acc = 2 * kIssuers * d.BN <= 512 ? 2 : 1;
 
     CUresult r;
@@ -1258,6 +1293,9 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     }
     prm.epi_off = prm.b_res_off + (b_res ? bres_bytes : 0);
     prm.n_pt = n_pt;
+    prm.raster = d.tune_raster;
+    prm.sync_copies = d.tune_sync_copies;
+    prm.n_mg = (n_m_tiles + group - 1) / group;
     prm.y = y;
     prm.bias = d.bias;
     prm.out32 = d.out_dtype == CONV2D_F32 ? 1 : 0;

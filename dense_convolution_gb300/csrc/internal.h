@@ -15,6 +15,11 @@ struct conv2d_desc {
     conv2d_layout layout;
     conv2d_dtype out_dtype;   // element type of Y: dtype, or F32 for 16-bit inputs
     const void* bias;         // Co bias values of the input type (device), or null
+    // Ablation knobs (conv2d_desc_set_tuning); 0 = automatic.
+    int tune_stages;          // cap on the shared-memory ring depth
+    int tune_sync_copies;     // 1: each stage's copies land before the next stage's are issued
+    int tune_raster;          // tile visit order (0 channel tile fastest, 1 pixel group fastest, 2 zig-zag)
+    int tune_no_resident;     // 1: never keep the whole filter slice resident in shared memory
     // Derived geometry.
     int Ho, Wo, Wp;       // output size; padded input width W + 2p
     conv2d_algo algo;     // resolved (never AUTO)

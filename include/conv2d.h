@@ -152,6 +152,37 @@ conv2d_status conv2d_desc_set_output_dtype(conv2d_desc_t d, conv2d_dtype out);
  * MISALIGNED (bias not aligned to its element size). */
 conv2d_status conv2d_desc_set_bias(conv2d_desc_t d, const void *bias);
 
+/* Knobs of the pipeline, for ablation studies in the manner of "Enabling
+ * Memory-efficient Im2win Convolution ...", Sec. IV-E (Fig. 4: the kernel
+ * without double buffering, without asynchronous copies, without the
+ * zig-zag block order).  Results do not depend on them (same sums; only the
+ * order in which tiles are visited and copies overlap changes).
+ *   CONV2D_TUNE_STAGES        cap on the depth of the shared-memory operand
+ *                             ring: 1 = no double buffering (every stage's
+ *                             copies wait for the previous stage's MMAs or
+ *                             FMAs), 2..8, 0 = automatic (default).  The
+ *                             CUDA-core kernel has two stages: 1 selects one.
+ *   The other knobs act on the tensor-core kernels only.
+ *   CONV2D_TUNE_SYNC_COPIES   1 = the copy-issuing thread waits for each
+ *                             stage's copies to land before it issues the
+ *                             next stage (copies no longer overlap each
+ *                             other); 0 = asynchronous (default).
+ *   CONV2D_TUNE_RASTER        visit order of the output tile groups (tensor
+ *                             cores): 0 = output-channel tile fastest
+ *                             (default), 1 = pixel group fastest, 2 = zig-zag
+ *                             (channel tiles in alternating direction on
+ *                             successive pixel groups).
+ *   CONV2D_TUNE_NO_RESIDENT   1 = never keep the filter slice resident in
+ *                             shared memory (tensor cores); 0 = automatic.
+ * Errors: NULL_PTR, BAD_PARAM (unknown knob or value out of range). */
+typedef enum {
+    CONV2D_TUNE_STAGES = 0,
+    CONV2D_TUNE_SYNC_COPIES = 1,
+    CONV2D_TUNE_RASTER = 2,
+    CONV2D_TUNE_NO_RESIDENT = 3
+} conv2d_tuning;
+conv2d_status conv2d_desc_set_tuning(conv2d_desc_t d, conv2d_tuning knob, int value);
+
 /* Release a descriptor (NULL is accepted and ignored). */
 conv2d_status conv2d_desc_destroy(conv2d_desc_t d);
 

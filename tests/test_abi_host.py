@@ -270,3 +270,21 @@ def test_implicit_nchw_needs_only_the_packed_filter(capi, shape, dtype):
     for bad, status in (((N, Ci, H, W, Co, Kh, Kw, 2, p), "f16"), (shape, "f32")):
         with pytest.raises(capi.Conv2dError):
             capi.conv2d_desc_create(*bad, status, "implicit_nchw_tc")
+
+
+def test_tuning_knobs_ranges(capi):
+    d = capi.conv2d_desc_create(1, 8, 8, 8, 8, 3, 3, 1, 1, "f16", "auto")
+    try:
+        for knob, good, bad in (("stages", (0, 1, 2, 8), (-1, 9)), ("sync_copies", (0, 1), (2, -1)),
+                                ("raster", (0, 1, 2), (3, -1)), ("no_resident", (0, 1), (2,))):
+            for v in good:
+                capi.conv2d_desc_set_tuning(d, knob, v)
+            for v in bad:
+                with pytest.raises(capi.Conv2dError) as e:
+                    capi.conv2d_desc_set_tuning(d, knob, v)
+                assert e.value.status == capi.ERR_BAD_PARAM
+        with pytest.raises(capi.Conv2dError) as e:
+            capi.conv2d_desc_set_tuning(d, 7, 0)
+        assert e.value.status == capi.ERR_BAD_PARAM
+    finally:
+        capi.conv2d_desc_destroy(d)
