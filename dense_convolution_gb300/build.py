@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libconv2d_gb300.so")
-SOURCES = ["api.cu", "transforms.cu", "conv_fp32.cu", "conv_tc.cu", "static_workspace.cu"]
+SOURCES = ["api.cu", "transforms.cu", "conv_fp32.cu", "conv_tc.cu", "winograd.cu", "static_workspace.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -18,7 +18,7 @@ OK, ERR_BAD_PARAM, ERR_UNSUPPORTED, ERR_NULL_PTR, ERR_MISALIGNED, ERR_WORKSPACE_
     ERR_DEVICE_TIMEOUT = range(8)
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
 ALGOS = {"auto": 0, "im2win_fp32_cc": 1, "im2win_tc": 2, "implicit_tc": 3, "implicit_fp32_cc": 4, "padded_tc": 5,
-         "implicit_nchw_tc": 6}
+         "implicit_nchw_tc": 6, "winograd_fp32_cc": 7}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 LAYOUTS = {"nchw": 0, "nhwc": 1}
 TUNING = {"stages": 0, "sync_copies": 1, "raster": 2, "no_resident": 3}

@@ -92,6 +92,13 @@ conv2d_status finalize(conv2d_desc& d) {
     if (d.layout == CONV2D_LAYOUT_NHWC && d.algo != CONV2D_ALGO_IMPLICIT_TC) return CONV2D_ERR_UNSUPPORTED;
     d.ws_weights = d.ws_input = d.ws_input_off = d.ws_total = 0;
     d.gemm1x1 = false;
+    if (d.algo == CONV2D_ALGO_WINOGRAD_FP32_CC) {
+        // F(2x2, 3x3): 3x3 filters, stride 1, NCHW input; workspace = the transformed filter.
+        if (d.Kh != 3 || d.Kw != 3 || d.s != 1) return CONV2D_ERR_UNSUPPORTED;
+        d.ws_weights = winograd_filter_bytes(d);
+        d.ws_total = d.ws_weights;
+        return CONV2D_OK;
+    }
     if (!tc) {
         d.Lp = (d.Wp * d.Kh + 3) & ~3;
         // 32 output channels per warp, 1, 2 or 4 warps; fewer warps when one
@@ -196,7 +203,7 @@ CONV2D_API conv2d_status conv2d_desc_create(conv2d_desc_t* out, int N, int Cin, 
     if (N < 1 || Cin < 1 || H < 1 || W < 1 || Cout < 1 || Kh < 1 || Kw < 1 || stride < 1 || pad < 0)
         return CONV2D_ERR_BAD_PARAM;
     if (dtype != CONV2D_F32 && dtype != CONV2D_F16 && dtype != CONV2D_BF16) return CONV2D_ERR_BAD_PARAM;
-    if (algo < CONV2D_ALGO_AUTO || algo > CONV2D_ALGO_IMPLICIT_NCHW_TC) return CONV2D_ERR_BAD_PARAM;
+    if (algo < CONV2D_ALGO_AUTO || algo > CONV2D_ALGO_WINOGRAD_FP32_CC) return CONV2D_ERR_BAD_PARAM;
     const long long Hp = (long long)H + 2LL * pad, Wp = (long long)W + 2LL * pad;
     if (Hp < Kh || Wp < Kw || Wp > 0x7fffffffLL) return CONV2D_ERR_BAD_PARAM;
     const long long Ho = (Hp - Kh) / stride + 1, Wo = (Wp - Kw) / stride + 1;
@@ -358,6 +365,11 @@ conv2d_status fwd_impl(conv2d_desc_t dp, const void* x, const void* w, void* y, 
             if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
             if (e == cudaSuccess) s = launch_conv_tc(d, x, wq, y, 4, st);
             break;
+        case CONV2D_ALGO_WINOGRAD_FP32_CC:
+            if (!record(ev0, st)) return CONV2D_ERR_CUDA;   // brackets both kernels (filter transform + main)
+            s = launch_winograd(d, static_cast<const float*>(x), static_cast<const float*>(w),
+                                static_cast<float*>(wq), static_cast<float*>(y), st);
+            break;
         case CONV2D_ALGO_PADDED_TC:
             e = launch_pack_filter_tc(w, wq, d, false, st);
             if (e == cudaSuccess) e = launch_nchw_to_padded_nhwc16(x, win, d, st);
@@ -424,16 +436,18 @@ CONV2D_API conv2d_status conv2d_launches_per_call(conv2d_desc_t d, int* launches
 
 CONV2D_API conv2d_status conv2d_device_status(void* stream, uint32_t* code_out) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    uint32_t a = 0, b = 0;
-    if (status_read_clear_tc(st, &a) != cudaSuccess || status_read_clear_fp32(st, &b) != cudaSuccess)
+    uint32_t a = 0, b = 0, c = 0;
+    if (status_read_clear_tc(st, &a) != cudaSuccess || status_read_clear_fp32(st, &b) != cudaSuccess ||
+        status_read_clear_wg(st, &c) != cudaSuccess)
         return CONV2D_ERR_CUDA;
-    if (code_out) *code_out = a | b;
-    return (a | b) ? CONV2D_ERR_DEVICE_TIMEOUT : CONV2D_OK;
+    if (code_out) *code_out = a | b | c;
+    return (a | b | c) ? CONV2D_ERR_DEVICE_TIMEOUT : CONV2D_OK;
 }
 
 CONV2D_API conv2d_status conv2d_set_wait_limit(uint64_t ns, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (wait_limit_set_tc(st, ns) != cudaSuccess || wait_limit_set_fp32(st, ns) != cudaSuccess)
+    if (wait_limit_set_tc(st, ns) != cudaSuccess || wait_limit_set_fp32(st, ns) != cudaSuccess ||
+        wait_limit_set_wg(st, ns) != cudaSuccess)
         return CONV2D_ERR_CUDA;
     return CONV2D_OK;
 }

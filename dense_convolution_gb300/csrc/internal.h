@@ -88,6 +88,13 @@ cudaError_t launch_pack_filter_f32(const float* w, float* wq, const conv2d_desc&
 conv2d_status launch_conv_fp32(const conv2d_desc& d, const float* src, const float* wq, float* y,
                                bool im2win, cudaStream_t st);
 
+// winograd.cu
+size_t winograd_filter_bytes(const conv2d_desc& d);
+conv2d_status launch_winograd(const conv2d_desc& d, const float* x, const float* w, float* u, float* y,
+                              cudaStream_t st);
+cudaError_t status_read_clear_wg(cudaStream_t st, uint32_t* out);
+cudaError_t wait_limit_set_wg(cudaStream_t st, uint64_t ns);
+
 // conv_tc.cu
 conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* wq, void* y, int amode,
                              cudaStream_t st);

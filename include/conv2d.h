@@ -91,6 +91,18 @@ typedef enum { CONV2D_F32 = 0, CONV2D_F16 = 1, CONV2D_BF16 = 2 } conv2d_dtype;
  *                   shared memory; every tap of a filter-row group reads that
  *                   tile at a row offset.  Workspace: the repacked filter
  *                   only; two launches (repack, contraction).
+ *  WINOGRAD_FP32_CC fp32 on CUDA cores, 3x3 filters at stride 1 (any pad),
+ *                   NCHW input: Winograd minimal filtering F(2x2, 3x3)
+ *                   ("OpenCNN: a Winograd minimal filtering algorithm
+ *                   implementation in CUDA", Sec. 2-3; "im2col Expansion,
+ *                   FFT Convolution, and Winograd Transforms", Winograd
+ *                   section): a filter-transform kernel, then one kernel per
+ *                   call that transforms 4x4 input tiles, sums the 16
+ *                   transformed products over input channels and transforms
+ *                   each 2x2 output tile back.  2.25x fewer multiplications
+ *                   than the direct sum; the same fp32 parity contract.
+ *                   Workspace: the transformed filter (16 values per filter,
+ *                   input channels rounded up to 8, output channels to 64).
  *  AUTO             resolved per shape when the descriptor is created
  *                   (conv2d_get_algo reports the choice). */
 typedef enum {
@@ -100,7 +112,8 @@ typedef enum {
     CONV2D_ALGO_IMPLICIT_TC = 3,
     CONV2D_ALGO_IMPLICIT_FP32_CC = 4,
     CONV2D_ALGO_PADDED_TC = 5,
-    CONV2D_ALGO_IMPLICIT_NCHW_TC = 6
+    CONV2D_ALGO_IMPLICIT_NCHW_TC = 6,
+    CONV2D_ALGO_WINOGRAD_FP32_CC = 7
 } conv2d_algo;
 
 /* Memory layout of X.  Y is always NCHW.  W is always [Cout][Cin][Kh][Kw]. */

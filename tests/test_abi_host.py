@@ -288,3 +288,21 @@ def test_tuning_knobs_ranges(capi):
         assert e.value.status == capi.ERR_BAD_PARAM
     finally:
         capi.conv2d_desc_destroy(d)
+
+
+def test_winograd_descriptor(capi):
+    """F(2x2, 3x3): 3x3 stride-1 fp32 only; workspace = transformed filter
+    (16 values per (output channel rounded to 64, input channel rounded to 8))."""
+    d = capi.conv2d_desc_create(2, 13, 9, 11, 70, 3, 3, 1, 1, "f32", "winograd_fp32_cc")
+    try:
+        assert capi.conv2d_workspace_size(d) == 128 * 16 * 16 * 4
+        assert capi.conv2d_launches_per_call(d) == 2
+        assert capi.conv2d_get_algo(d) == "winograd_fp32_cc"
+    finally:
+        capi.conv2d_desc_destroy(d)
+    for shape, dt, status in (((1, 8, 9, 9, 8, 5, 5, 1, 2), "f32", capi.ERR_UNSUPPORTED),
+                              ((1, 8, 9, 9, 8, 3, 3, 2, 1), "f32", capi.ERR_UNSUPPORTED),
+                              ((1, 8, 9, 9, 8, 3, 3, 1, 1), "f16", capi.ERR_BAD_PARAM)):
+        with pytest.raises(capi.Conv2dError) as e:
+            capi.conv2d_desc_create(*shape, dt, "winograd_fp32_cc")
+        assert e.value.status == status
