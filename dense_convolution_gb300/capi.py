@@ -24,7 +24,8 @@ LAYOUTS = {"nchw": 0, "nhwc": 1}
 TUNING = {"stages": 0, "sync_copies": 1, "raster": 2, "no_resident": 3}
 
 EXPORTED = ("conv2d_desc_create", "conv2d_desc_set_input_layout", "conv2d_desc_set_output_dtype",
-            "conv2d_desc_set_bias", "conv2d_desc_set_tuning", "conv2d_desc_destroy", "conv2d_out_dims",
+            "conv2d_desc_set_bias", "conv2d_desc_set_tuning", "conv2d_packed_filter_bytes", "conv2d_pack_filter",
+            "conv2d_desc_set_filter_prepacked", "conv2d_desc_destroy", "conv2d_out_dims",
             "conv2d_workspace_size", "conv2d_get_algo", "conv2d_fwd", "conv2d_fwd_profiled", "conv2d_fwd_host",
             "conv2d_launches_per_call", "conv2d_fwd_static_workspace", "conv2d_static_workspace_bytes",
             "conv2d_set_wait_limit", "conv2d_device_status", "conv2d_status_string")
@@ -53,6 +54,9 @@ def load(path: str = LIB_PATH):
     L.conv2d_desc_set_output_dtype.argtypes = [vp, c_int]
     L.conv2d_desc_set_bias.argtypes = [vp, vp]
     L.conv2d_desc_set_tuning.argtypes = [vp, c_int, c_int]
+    L.conv2d_packed_filter_bytes.argtypes = [vp, ctypes.POINTER(c_size)]
+    L.conv2d_pack_filter.argtypes = [vp, vp, vp, vp]
+    L.conv2d_desc_set_filter_prepacked.argtypes = [vp, c_int]
     L.conv2d_desc_destroy.argtypes = [vp]
     L.conv2d_out_dims.argtypes = [vp, ctypes.POINTER(c_int), ctypes.POINTER(c_int)]
     L.conv2d_workspace_size.argtypes = [vp, ctypes.POINTER(c_size)]
@@ -110,6 +114,20 @@ def conv2d_desc_set_tuning(desc: int, knob, value: int):
     """Pipeline knob for ablations: "stages", "sync_copies", "raster", "no_resident"."""
     k = TUNING[knob] if isinstance(knob, str) else int(knob)
     _check(load().conv2d_desc_set_tuning(desc, k, int(value)), "conv2d_desc_set_tuning")
+
+
+def conv2d_packed_filter_bytes(desc: int) -> int:
+    b = ctypes.c_size_t()
+    _check(load().conv2d_packed_filter_bytes(desc, ctypes.byref(b)), "conv2d_packed_filter_bytes")
+    return b.value
+
+
+def conv2d_pack_filter(desc: int, w: int, w_packed: int, stream: int = 0):
+    _check(load().conv2d_pack_filter(desc, w, w_packed, stream or None), "conv2d_pack_filter")
+
+
+def conv2d_desc_set_filter_prepacked(desc: int, prepacked: bool = True):
+    _check(load().conv2d_desc_set_filter_prepacked(desc, 1 if prepacked else 0), "conv2d_desc_set_filter_prepacked")
 
 
 def conv2d_desc_destroy(desc: int):

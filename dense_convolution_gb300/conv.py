@@ -35,6 +35,22 @@ class Conv2d:
         self.workspace_bytes = capi.conv2d_workspace_size(self.desc)
         self.algo = capi.conv2d_get_algo(self.desc)
 
+    def pack_filter(self, w: torch.Tensor, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+        """The filter in the kernels' order (a byte tensor), for set_prepacked calls."""
+        N, Ci, H, W, Co, Kh, Kw = self.shape[:7]
+        if tuple(w.shape) != (Co, Ci, Kh, Kw) or not w.is_contiguous() or w.dtype != _TORCH_DTYPE[self.dtype]:
+            raise ValueError(f"w must be a contiguous {self.dtype} tensor of shape {(Co, Ci, Kh, Kw)}")
+        wp = torch.empty(capi.conv2d_packed_filter_bytes(self.desc), dtype=torch.uint8, device=w.device)
+        st = (stream or torch.cuda.current_stream(w.device)).cuda_stream
+        capi.conv2d_pack_filter(self.desc, w.data_ptr(), wp.data_ptr(), st)
+        return wp
+
+    def set_prepacked(self, on: bool = True):
+        """From now on __call__ takes the output of pack_filter as w (no repack per call)."""
+        capi.conv2d_desc_set_filter_prepacked(self.desc, on)
+        self.prepacked = on
+        self.workspace_bytes = capi.conv2d_workspace_size(self.desc)
+
     def __del__(self):
         d = getattr(self, "desc", None)
         if d:
@@ -63,7 +79,10 @@ class Conv2d:
         want_x = (N, Ci, H, W) if self.layout == "nchw" else (N, H, W, Ci)
         if tuple(x.shape) != want_x or not x.is_contiguous() or x.dtype != _TORCH_DTYPE[self.dtype]:
             raise ValueError(f"x must be a contiguous {self.dtype} tensor of shape {want_x}")
-        if tuple(w.shape) != (Co, Ci, Kh, Kw) or not w.is_contiguous() or w.dtype != x.dtype:
+        if getattr(self, "prepacked", False):
+            if w.dtype != torch.uint8 or w.numel() != capi.conv2d_packed_filter_bytes(self.desc):
+                raise ValueError("w must be the byte tensor pack_filter returned for this descriptor")
+        elif tuple(w.shape) != (Co, Ci, Kh, Kw) or not w.is_contiguous() or w.dtype != x.dtype:
             raise ValueError(f"w must be a contiguous {self.dtype} tensor of shape {(Co, Ci, Kh, Kw)}")
         if bias is not None and (tuple(bias.shape) != (Co,) or not bias.is_contiguous() or bias.dtype != x.dtype):
             raise ValueError(f"bias must be a contiguous {self.dtype} tensor of shape {(Co,)}")

@@ -96,7 +96,7 @@ conv2d_status finalize(conv2d_desc& d) {
         // F(2x2, 3x3): 3x3 filters, stride 1, NCHW input; workspace = the transformed filter.
         if (d.Kh != 3 || d.Kw != 3 || d.s != 1) return CONV2D_ERR_UNSUPPORTED;
         d.ws_weights = winograd_filter_bytes(d);
-        d.ws_total = d.ws_weights;
+        d.ws_total = d.prepacked ? 0 : d.ws_weights;
         return CONV2D_OK;
     }
     if (!tc) {
@@ -187,6 +187,11 @@ conv2d_status finalize(conv2d_desc& d) {
             d.ws_input = (size_t)((long long)d.N * d.H * d.W * d.Ci8) * 2;
         }
     }
+    if (d.prepacked) {   // the filter lives in the caller's packed buffer
+        d.ws_input_off = 0;
+        d.ws_total = d.ws_input;
+        return CONV2D_OK;
+    }
     d.ws_input_off = d.ws_input ? align_up(d.ws_weights, 1024) : 0;
     d.ws_total = d.ws_input ? d.ws_input_off + d.ws_input : d.ws_weights;
     return CONV2D_OK;
@@ -275,6 +280,49 @@ CONV2D_API conv2d_status conv2d_desc_set_tuning(conv2d_desc_t d, conv2d_tuning k
     return CONV2D_ERR_BAD_PARAM;
 }
 
+CONV2D_API conv2d_status conv2d_packed_filter_bytes(conv2d_desc_t d, size_t* bytes) {
+    if (!d || !bytes) return CONV2D_ERR_NULL_PTR;
+    *bytes = d->gemm1x1 ? (size_t)d->Co * d->Ci * 2 : d->ws_weights;
+    return CONV2D_OK;
+}
+
+CONV2D_API conv2d_status conv2d_desc_set_filter_prepacked(conv2d_desc_t d, int prepacked) {
+    if (!d) return CONV2D_ERR_NULL_PTR;
+    if (prepacked != 0 && prepacked != 1) return CONV2D_ERR_BAD_PARAM;
+    conv2d_desc t = *d;
+    t.prepacked = prepacked != 0;
+    conv2d_status st = finalize(t);
+    if (st != CONV2D_OK) return st;
+    *d = t;
+    return CONV2D_OK;
+}
+
+CONV2D_API conv2d_status conv2d_pack_filter(conv2d_desc_t dp, const void* w, void* w_packed, void* stream) {
+    if (!dp || !w || !w_packed) return CONV2D_ERR_NULL_PTR;
+    if (!aligned16(w) || !aligned16(w_packed)) return CONV2D_ERR_MISALIGNED;
+    const conv2d_desc& d = *dp;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    switch (d.algo) {
+        case CONV2D_ALGO_IM2WIN_FP32_CC:
+        case CONV2D_ALGO_IMPLICIT_FP32_CC:
+            e = launch_pack_filter_f32(static_cast<const float*>(w), static_cast<float*>(w_packed), d, st);
+            break;
+        case CONV2D_ALGO_WINOGRAD_FP32_CC:
+            e = launch_winograd_filter(d, static_cast<const float*>(w), static_cast<float*>(w_packed), st);
+            break;
+        case CONV2D_ALGO_IM2WIN_TC:
+            e = launch_pack_filter_tc(w, w_packed, d, true, st);
+            break;
+        default:
+            if (d.gemm1x1)   // the 1x1 GEMM reads the filter as given
+                e = cudaMemcpyAsync(w_packed, w, (size_t)d.Co * d.Ci * 2, cudaMemcpyDeviceToDevice, st);
+            else
+                e = launch_pack_filter_tc(w, w_packed, d, false, st);
+    }
+    return e == cudaSuccess ? CONV2D_OK : CONV2D_ERR_CUDA;
+}
+
 CONV2D_API conv2d_status conv2d_desc_destroy(conv2d_desc_t d) {
     delete d;
     return CONV2D_OK;
@@ -316,31 +364,43 @@ conv2d_status fwd_impl(conv2d_desc_t dp, const void* x, const void* w, void* y, 
     if (workspace_bytes < d.ws_total) return CONV2D_ERR_WORKSPACE_TOO_SMALL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    void* wq = ws;
+    // Pre-packed filter: w is already in the kernel's order (conv2d_pack_filter)
+    // and the workspace holds only the input-side tensor; the first kernel of
+    // the call is then a transform or the contraction itself.
+    const bool pre = d.prepacked;
+    void* wq = pre ? const_cast<void*>(w) : ws;
     void* win = ws ? ws + d.ws_input_off : nullptr;
     cudaError_t e = cudaSuccess;
     conv2d_status s = CONV2D_OK;
     switch (d.algo) {
         case CONV2D_ALGO_IM2WIN_FP32_CC:
-            e = launch_pack_filter_f32(static_cast<const float*>(w), static_cast<float*>(wq), d, st);
-            if (e == cudaSuccess) e = launch_im2win_strips_f32(static_cast<const float*>(x), static_cast<float*>(win), d, st);
+            if (!pre) e = launch_pack_filter_f32(static_cast<const float*>(w), static_cast<float*>(wq), d, st);
+            if (e == cudaSuccess)
+                e = launch_im2win_strips_f32(static_cast<const float*>(x), static_cast<float*>(win), d, st, !pre);
             if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
             if (e == cudaSuccess)
                 s = launch_conv_fp32(d, static_cast<const float*>(win), static_cast<const float*>(wq),
                                      static_cast<float*>(y), true, st);
             break;
         case CONV2D_ALGO_IMPLICIT_FP32_CC:
-            e = launch_pack_filter_f32(static_cast<const float*>(w), static_cast<float*>(wq), d, st);
+            if (!pre) e = launch_pack_filter_f32(static_cast<const float*>(w), static_cast<float*>(wq), d, st);
             if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
             if (e == cudaSuccess)
                 s = launch_conv_fp32(d, static_cast<const float*>(x), static_cast<const float*>(wq),
                                      static_cast<float*>(y), false, st);
             break;
+        case CONV2D_ALGO_WINOGRAD_FP32_CC:
+            if (!record(ev0, st)) return CONV2D_ERR_CUDA;   // brackets both kernels (filter transform + main)
+            if (!pre) e = launch_winograd_filter(d, static_cast<const float*>(w), static_cast<float*>(wq), st);
+            if (e == cudaSuccess)
+                s = launch_winograd_main(d, static_cast<const float*>(x), static_cast<const float*>(wq),
+                                         static_cast<float*>(y), st);
+            break;
         case CONV2D_ALGO_IM2WIN_TC:
-            e = launch_pack_filter_tc(w, wq, d, true, st);
+            if (!pre) e = launch_pack_filter_tc(w, wq, d, true, st);
             if (e == cudaSuccess)
                 e = launch_window_cl16(x, win, d.N, d.Ci, d.H, d.W, d.Ci8, d.Ck, d.Ho, d.Wq * d.s, d.Kh, d.s, d.p,
-                                       st);
+                                       st, !pre);
             if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
             if (e == cudaSuccess) s = launch_conv_tc(d, win, wq, y, 1, st);
             break;
@@ -350,10 +410,10 @@ conv2d_status fwd_impl(conv2d_desc_t dp, const void* x, const void* w, void* y, 
                 s = launch_conv_tc(d, x, w, y, 3, st);
                 break;
             }
-            e = launch_pack_filter_tc(w, wq, d, false, st);
+            if (!pre) e = launch_pack_filter_tc(w, wq, d, false, st);
             const void* src = x;
             if (e == cudaSuccess && d.layout == CONV2D_LAYOUT_NCHW) {
-                e = launch_nchw_to_nhwc16(x, win, d.N, d.Ci, d.H, d.W, d.Ci8, st);
+                e = launch_nchw_to_nhwc16(x, win, d.N, d.Ci, d.H, d.W, d.Ci8, st, !pre);
                 src = win;
             }
             if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
@@ -361,18 +421,13 @@ conv2d_status fwd_impl(conv2d_desc_t dp, const void* x, const void* w, void* y, 
             break;
         }
         case CONV2D_ALGO_IMPLICIT_NCHW_TC:   // the contraction kernel reads NCHW X itself
-            e = launch_pack_filter_tc(w, wq, d, false, st);
+            if (!pre) e = launch_pack_filter_tc(w, wq, d, false, st);
             if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
             if (e == cudaSuccess) s = launch_conv_tc(d, x, wq, y, 4, st);
             break;
-        case CONV2D_ALGO_WINOGRAD_FP32_CC:
-            if (!record(ev0, st)) return CONV2D_ERR_CUDA;   // brackets both kernels (filter transform + main)
-            s = launch_winograd(d, static_cast<const float*>(x), static_cast<const float*>(w),
-                                static_cast<float*>(wq), static_cast<float*>(y), st);
-            break;
         case CONV2D_ALGO_PADDED_TC:
-            e = launch_pack_filter_tc(w, wq, d, false, st);
-            if (e == cudaSuccess) e = launch_nchw_to_padded_nhwc16(x, win, d, st);
+            if (!pre) e = launch_pack_filter_tc(w, wq, d, false, st);
+            if (e == cudaSuccess) e = launch_nchw_to_padded_nhwc16(x, win, d, st, !pre);
             if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
             if (e == cudaSuccess) s = launch_conv_tc(d, win, wq, y, 2, st);
             break;
@@ -409,7 +464,8 @@ CONV2D_API conv2d_status conv2d_fwd_host(conv2d_desc_t dp, const void* x_host, c
     if (workspace_bytes < d.ws_total) return CONV2D_ERR_WORKSPACE_TOO_SMALL;
     const size_t elem = d.dtype == CONV2D_F32 ? 4 : 2;
     const size_t x_bytes = (size_t)d.N * d.Ci * d.H * d.W * elem;
-    const size_t w_bytes = (size_t)d.Co * d.Ci * d.Kh * d.Kw * elem;
+    const size_t w_bytes = d.prepacked ? (d.gemm1x1 ? (size_t)d.Co * d.Ci * elem : d.ws_weights)
+                                       : (size_t)d.Co * d.Ci * d.Kh * d.Kw * elem;
     const size_t y_bytes = (size_t)d.N * d.Co * d.Ho * d.Wo * (d.out_dtype == CONV2D_F32 ? 4 : 2);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return CONV2D_ERR_CUDA;
@@ -426,7 +482,7 @@ CONV2D_API conv2d_status conv2d_launches_per_call(conv2d_desc_t d, int* launches
         *launches = 1;
         return CONV2D_OK;
     }
-    int n = 2;   // filter repack + contraction
+    int n = d->prepacked ? 1 : 2;   // filter repack (unless pre-packed) + contraction
     if (d->algo == CONV2D_ALGO_IM2WIN_FP32_CC || d->algo == CONV2D_ALGO_IM2WIN_TC || d->algo == CONV2D_ALGO_PADDED_TC ||
         (d->algo == CONV2D_ALGO_IMPLICIT_TC && d->layout == CONV2D_LAYOUT_NCHW && !d->nchw_halo))
         ++n;

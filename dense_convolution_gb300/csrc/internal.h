@@ -20,6 +20,7 @@ struct conv2d_desc {
     int tune_sync_copies;     // 1: each stage's copies land before the next stage's are issued
     int tune_raster;          // tile visit order (0 channel tile fastest, 1 pixel group fastest, 2 zig-zag)
     int tune_no_resident;     // 1: never keep the whole filter slice resident in shared memory
+    bool prepacked;           // conv2d_fwd's w is the filter conv2d_pack_filter wrote (no repack per call)
     // Derived geometry.
     int Ho, Wo, Wp;       // output size; padded input width W + 2p
     conv2d_algo algo;     // resolved (never AUTO)
@@ -75,12 +76,31 @@ inline cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block,
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// transforms.cu
-cudaError_t launch_im2win_strips_f32(const float* x, float* xw, const conv2d_desc& d, cudaStream_t st);
+// A launch that is either a programmatic dependent of the previous kernel of
+// the stream (pdl) or an ordinary stream-ordered launch, for kernels that are
+// the first of a call when the filter repack is skipped (they read X at once
+// and must not start before the stream's previous work has finished).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_chain(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                cudaStream_t st, Args... args) {
+    if (pdl) return launch_after(kernel, grid, block, smem, st, args...);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// transforms.cu (pdl = false: the first kernel of a call, see launch_chain)
+cudaError_t launch_im2win_strips_f32(const float* x, float* xw, const conv2d_desc& d, cudaStream_t st,
+                                     bool pdl = true);
 cudaError_t launch_window_cl16(const void* x, void* out, int N, int Ci, int H, int W, int Ci8, int Ck, int R,
-                               int Wq, int Kh, int s, int p, cudaStream_t st);
-cudaError_t launch_nchw_to_nhwc16(const void* x, void* out, int N, int C, int H, int W, int C8, cudaStream_t st);
-cudaError_t launch_nchw_to_padded_nhwc16(const void* x, void* out, const conv2d_desc& d, cudaStream_t st);
+                               int Wq, int Kh, int s, int p, cudaStream_t st, bool pdl = true);
+cudaError_t launch_nchw_to_nhwc16(const void* x, void* out, int N, int C, int H, int W, int C8, cudaStream_t st,
+                                  bool pdl = true);
+cudaError_t launch_nchw_to_padded_nhwc16(const void* x, void* out, const conv2d_desc& d, cudaStream_t st,
+                                         bool pdl = true);
 cudaError_t launch_pack_filter_tc(const void* w, void* wq, const conv2d_desc& d, bool im2win, cudaStream_t st);
 cudaError_t launch_pack_filter_f32(const float* w, float* wq, const conv2d_desc& d, cudaStream_t st);
 
@@ -90,8 +110,9 @@ conv2d_status launch_conv_fp32(const conv2d_desc& d, const float* src, const flo
 
 // winograd.cu
 size_t winograd_filter_bytes(const conv2d_desc& d);
-conv2d_status launch_winograd(const conv2d_desc& d, const float* x, const float* w, float* u, float* y,
-                              cudaStream_t st);
+cudaError_t launch_winograd_filter(const conv2d_desc& d, const float* w, float* u, cudaStream_t st);
+conv2d_status launch_winograd_main(const conv2d_desc& d, const float* x, const float* u, float* y,
+                                   cudaStream_t st);
 cudaError_t status_read_clear_wg(cudaStream_t st, uint32_t* out);
 cudaError_t wait_limit_set_wg(cudaStream_t st, uint64_t ns);
 

@@ -50,12 +50,12 @@ __global__ void __launch_bounds__(256) im2win_strips_f32_kernel(const float* __r
     pdl_wait();   // complete only after the filter repack launched before us
 }
 
-cudaError_t launch_im2win_strips_f32(const float* x, float* xw, const conv2d_desc& d, cudaStream_t st) {
+cudaError_t launch_im2win_strips_f32(const float* x, float* xw, const conv2d_desc& d, cudaStream_t st, bool pdl) {
     const long long total_vec = (long long)d.N * d.Ci * d.Ho * (d.Lp / 4);
     if (total_vec > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const long long blocks = (total_vec + 255) / 256, cap = (long long)device_sm_count() * 16;
     const int grid = (int)(blocks < cap ? blocks : cap);
-    return launch_after(im2win_strips_f32_kernel, dim3(grid < 1 ? 1 : grid), dim3(256), 0, st, x,
+    return launch_chain(pdl, im2win_strips_f32_kernel, dim3(grid < 1 ? 1 : grid), dim3(256), 0, st, x,
                         reinterpret_cast<float4*>(xw), d.Ci, d.H, d.W, d.Ho, d.Kh, d.s, d.p, d.Wp, d.Lp,
                         (int)total_vec);
 }
@@ -115,12 +115,13 @@ __global__ void __launch_bounds__(256) nchw_to_nhwc16_kernel(const uint16_t* __r
     pdl_wait();   // complete only after the filter repack launched before us
 }
 
-cudaError_t launch_nchw_to_nhwc16(const void* x, void* out, int N, int C, int H, int W, int C8, cudaStream_t st) {
+cudaError_t launch_nchw_to_nhwc16(const void* x, void* out, int N, int C, int H, int W, int C8, cudaStream_t st,
+                                  bool pdl) {
     const int P = H * W;
     const int vec_ok = (P % 8 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) ? 1 : 0;
     dim3 grid((P + kNhwcTile - 1) / kNhwcTile, (C8 + kNhwcTile - 1) / kNhwcTile, N);
     if (grid.z > 65535 || grid.y > 65535) return cudaErrorInvalidConfiguration;
-    return launch_after(nchw_to_nhwc16_kernel, grid, dim3(256), 0, st, static_cast<const uint16_t*>(x),
+    return launch_chain(pdl, nchw_to_nhwc16_kernel, grid, dim3(256), 0, st, static_cast<const uint16_t*>(x),
                         static_cast<uint4*>(out), C, C8, P, vec_ok);
 }
 
@@ -192,13 +193,13 @@ __global__ void __launch_bounds__(256) nchw_to_padded_nhwc16_kernel(const uint16
     pdl_wait();   // complete only after the filter repack launched before us
 }
 
-cudaError_t launch_nchw_to_padded_nhwc16(const void* x, void* out, const conv2d_desc& d, cudaStream_t st) {
+cudaError_t launch_nchw_to_padded_nhwc16(const void* x, void* out, const conv2d_desc& d, cudaStream_t st, bool pdl) {
     const int n_xt = (d.Wq + kRowTileX - 1) / kRowTileX;
     const long long gx = (long long)n_xt * d.Hp;
     const int vec_ok = (d.W % 8 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) ? 1 : 0;
     dim3 grid((unsigned)gx, (d.Ci8 + 63) / 64, d.N);
     if (gx > 0x7fffffffLL || grid.z > 65535 || grid.y > 65535) return cudaErrorInvalidConfiguration;
-    return launch_after(nchw_to_padded_nhwc16_kernel, grid, dim3(256), 0, st, static_cast<const uint16_t*>(x),
+    return launch_chain(pdl, nchw_to_padded_nhwc16_kernel, grid, dim3(256), 0, st, static_cast<const uint16_t*>(x),
                         static_cast<uint4*>(out), d.Ci, d.Ci8, d.H, d.W, d.Hp, d.Wq, d.p, n_xt, vec_ok);
 }
 
@@ -357,7 +358,7 @@ __global__ void __launch_bounds__(256) window_cl16_rows_kernel(const uint16_t* _
 }
 
 cudaError_t launch_window_cl16(const void* x, void* out, int N, int Ci, int H, int W, int Ci8, int Ck, int R,
-                               int Wq, int Kh, int s, int p, cudaStream_t st) {
+                               int Wq, int Kh, int s, int p, cudaStream_t st, bool pdl) {
     const uint16_t* xi = static_cast<const uint16_t*>(x);
     uint4* o = static_cast<uint4*>(out);
     const long long row_smem = (long long)((kWinRowsPerBlock - 1) * s + Kh) * Ci * kWinRowPitch * 2;
@@ -369,20 +370,20 @@ cudaError_t launch_window_cl16(const void* x, void* out, int N, int Ci, int H, i
                                              (int)row_smem);
         if (e != cudaSuccess) return e;
         const int vec_ok = (W % 8 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) ? 1 : 0;
-        return launch_after(window_cl16_rows_kernel, dim3((unsigned)blocks), dim3(256), (size_t)row_smem, st, xi, o,
+        return launch_chain(pdl, window_cl16_rows_kernel, dim3((unsigned)blocks), dim3(256), (size_t)row_smem, st, xi, o,
                             Ci, H, W, Ck, R, Wq, Kh, s, p, n_xr, n_rb, vec_ok);
     }
     if (Ci8 <= 16) {
         long long total_vec = (long long)N * R * Wq * (Ck / 8);
         long long blocks = (total_vec + 255) / 256, cap = (long long)device_sm_count() * 16;
         int grid = (int)(blocks < cap ? blocks : cap);
-        return launch_after(window_cl16_small_kernel, dim3(grid < 1 ? 1 : grid), dim3(256), 0, st, xi, o, Ci, H, W,
+        return launch_chain(pdl, window_cl16_small_kernel, dim3(grid < 1 ? 1 : grid), dim3(256), 0, st, xi, o, Ci, H, W,
                             Ck, R, Wq, Kh, s, p, total_vec);
     } else {
         int n_xt = (Wq + kWinTileX - 1) / kWinTileX, n_ct = (Ci8 + kWinTileC - 1) / kWinTileC;
         long long blocks = (long long)n_xt * n_ct * Kh * N * R;
         if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-        return launch_after(window_cl16_tiled_kernel, dim3((unsigned)blocks), dim3(256), 0, st, xi, o, Ci, H, W, Ci8,
+        return launch_chain(pdl, window_cl16_tiled_kernel, dim3((unsigned)blocks), dim3(256), 0, st, xi, o, Ci, H, W, Ci8,
                             R, Wq, Kh, s, p, n_xt, n_ct);
     }
 }

@@ -196,6 +196,28 @@ typedef enum {
 } conv2d_tuning;
 conv2d_status conv2d_desc_set_tuning(conv2d_desc_t d, conv2d_tuning knob, int value);
 
+/* Pre-packed filters.  Every call repacks the filter into the order its
+ * kernels read (the filter-height-before-width, channel-innermost order of
+ * "Enabling Memory-efficient Im2win Convolution ...", Sec. III-C/III-D; the
+ * transformed filter G g G^T for Winograd).  A caller whose filter does not
+ * change between calls (inference) can pack it once:
+ *   conv2d_packed_filter_bytes  size of the packed filter for the
+ *                               descriptor's algorithm (bytes)
+ *   conv2d_pack_filter          w (the [Cout][Cin][Kh][Kw] filter, device)
+ *                               -> w_packed (device, that many bytes, 16-byte
+ *                               aligned), on `stream`
+ *   conv2d_desc_set_filter_prepacked(d, 1)
+ *                               from then on conv2d_fwd* take w_packed as
+ *                               their w argument: no repack launch, and
+ *                               conv2d_workspace_size no longer includes the
+ *                               packed filter.  0 restores the default.
+ * The packed layout depends on the descriptor's shape and algorithm only;
+ * pack again after changing either (a new descriptor).  Errors: NULL_PTR,
+ * MISALIGNED, CUDA; BAD_PARAM for a flag other than 0/1. */
+conv2d_status conv2d_packed_filter_bytes(conv2d_desc_t d, size_t *bytes);
+conv2d_status conv2d_pack_filter(conv2d_desc_t d, const void *w, void *w_packed, void *stream);
+conv2d_status conv2d_desc_set_filter_prepacked(conv2d_desc_t d, int prepacked);
+
 /* Release a descriptor (NULL is accepted and ignored). */
 conv2d_status conv2d_desc_destroy(conv2d_desc_t d);
 

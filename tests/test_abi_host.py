@@ -306,3 +306,30 @@ def test_winograd_descriptor(capi):
         with pytest.raises(capi.Conv2dError) as e:
             capi.conv2d_desc_create(*shape, dt, "winograd_fp32_cc")
         assert e.value.status == status
+
+
+@pytest.mark.parametrize("shape,dtype,algo", [((32, 64, 56, 56, 64, 3, 3, 1, 1), "f16", "padded_tc"),
+                                              ((64, 512, 28, 28, 512, 3, 3, 1, 1), "f16", "implicit_tc"),
+                                              ((16, 128, 64, 64, 128, 1, 1, 1, 0), "f16", "implicit_tc"),
+                                              ((32, 64, 56, 56, 64, 3, 3, 1, 1), "f32", "im2win_fp32_cc"),
+                                              ((32, 64, 56, 56, 64, 3, 3, 1, 1), "f32", "winograd_fp32_cc"),
+                                              ((32, 64, 56, 56, 64, 3, 3, 1, 1), "f16", "implicit_nchw_tc")])
+def test_prepacked_filter_workspace_and_launches(capi, shape, dtype, algo):
+    """Pre-packing moves the packed filter out of the workspace and drops the
+    repack launch (the 1x1 GEMM has neither)."""
+    d = capi.conv2d_desc_create(*shape, dtype, algo)
+    try:
+        ws0, n0 = capi.conv2d_workspace_size(d), capi.conv2d_launches_per_call(d)
+        packed = capi.conv2d_packed_filter_bytes(d)
+        assert packed > 0
+        capi.conv2d_desc_set_filter_prepacked(d, True)
+        ws1, n1 = capi.conv2d_workspace_size(d), capi.conv2d_launches_per_call(d)
+        if n0 == 1:     # 1x1 GEMM: the filter is read as given, nothing to drop
+            assert (ws1, n1) == (ws0, n0) == (0, 1)
+        else:
+            assert n1 == n0 - 1 and ws1 <= ws0 - packed
+        capi.conv2d_desc_set_filter_prepacked(d, False)
+        assert capi.conv2d_workspace_size(d) == ws0
+        assert capi.load().conv2d_desc_set_filter_prepacked(d, 2) == capi.ERR_BAD_PARAM
+    finally:
+        capi.conv2d_desc_destroy(d)
