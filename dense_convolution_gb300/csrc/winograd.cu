@@ -26,7 +26,7 @@ namespace conv2d_gb300 {
 constexpr int kWgTiles = 32;      // output tiles per block: 4 rows x 8 columns of 2x2 (8 x 16 outputs)
 constexpr int kWgCo = 64;         // output channels per block
 constexpr int kWgCb = 8;          // input channels per pipeline stage
-constexpr int kWgThreads = 512;
+constexpr int kWgThreads = 256;
 
 // ---------------------------------------------------------------- filter transform
 // U[kb][ci][e][k] = (G g G^T)[e] of filter (co = 64 kb + k, ci), e = 4a + b,
@@ -85,29 +85,23 @@ constexpr int kWgVFloats = kWgCb * 16 * kWgTiles;          // V stage: [c][e][t]
 constexpr int kWgUFloats = kWgCb * 16 * kWgCo;             // U stage: [c][e][k]
 constexpr int kWgStageFloats = kWgVFloats + kWgUFloats;
 constexpr int kWgExchFloats = 16 * kWgCo * kWgTiles;       // sums before the output transform: [e][k][t]
-constexpr int kWgRawRows = 10, kWgRawCols = 18;            // input region of a block: (2*4 + 2) x (2*8 + 2)
-constexpr int kWgRawFloats = kWgCb * kWgRawRows * kWgRawCols;
-constexpr int kWgRawPerThread = (kWgRawFloats + kWgThreads - 1) / kWgThreads;
-constexpr int kWgMainFloats = (2 * kWgStageFloats > kWgExchFloats) ? 2 * kWgStageFloats : kWgExchFloats;
-constexpr int kWgSmemBytes = (kWgMainFloats + kWgRawFloats) * 4 + 128;
+constexpr int kWgSmemFloats = (2 * kWgStageFloats > kWgExchFloats) ? 2 * kWgStageFloats : kWgExchFloats;
+constexpr int kWgSmemBytes = kWgSmemFloats * 4 + 128;
 
 // One block: 32 output tiles (2x2 each, 8 rows x 16 columns of outputs) of one
-// image for 64 output channels, over all input channels in stages of 8;
-// 16 warps, warp e accumulating transform point e.  Per stage: the block's
-// 10 x 18 input region of the stage's 8 channels is loaded once (coalesced,
-// zero outside the image) into shared memory; thread pairs transform the 4x4
-// tile t of channel c (B^T d B, half the rows each) into V[c][e][t]; lane
-// (ti, ki) = (lane / 8, lane % 8) of warp e then accumulates tiles
-// 8ti..8ti+7 x channels 8ki..8ki+7: per channel one 8x8 outer product from two
-// float4 reads of V and two of U (broadcast within the warp).  The next
-// stage's filter slice arrives by bulk copy and its input region is loaded
-// into registers while this stage's products run.  At the end the sums go
-// through shared memory as [e][k][t] so that each thread holds all 16 points
-// of its (tile, channel) pairs for A^T m A.
+// image for 64 output channels, over all input channels in stages of 8.
+// Thread (c, t) = (tid / 32, tid % 32) transforms the 4x4 input tile t of
+// channel c of a stage (B^T d B) into V[c][e][t].  Warp w then accumulates
+// transform points e = 2w, 2w+1; lane (ti, ki) = (lane / 8, lane % 8) holds
+// tiles 8ti..8ti+7 x channels 8ki..8ki+7 of both: per (channel, e) one 8x8
+// outer product from two float4 reads of V and two of U (shared-memory reads
+// broadcast within the warp).  The next stage's filter slice arrives by bulk
+// copy and its input tiles are loaded into registers while this stage runs.
+// At the end the sums go through shared memory as [e][k][t] so that each
+// thread holds all 16 points of its (tile, channel) pairs for A^T m A.
 __global__ void __launch_bounds__(kWgThreads, 1) winograd_f2x3_kernel(const WgParams prm) {
     extern __shared__ uint8_t wg_smem_raw[];
     float* smem = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(wg_smem_raw) + 127) & ~uintptr_t(127));
-    float* raw = smem + kWgMainFloats;
     __shared__ __align__(8) uint64_t bars[2];
     __shared__ int abort_flag;
 
@@ -128,36 +122,29 @@ __global__ void __launch_bounds__(kWgThreads, 1) winograd_f2x3_kernel(const WgPa
     __syncthreads();
     pdl_wait();   // the transformed filter comes from the kernel launched just before
 
-    // The block's input region: rows iy0.., columns ix0.. (padding included).
-    const int iy0 = 8 * by - prm.p, ix0 = 16 * bx - prm.p;
-    auto load_region = [&](int chunk, float (&r)[kWgRawPerThread]) {
+    // This thread's input tile: channel c of the stage, tile t = (ty, tx).
+    const int c_in = tid >> 5, t_in = tid & 31;
+    const int gy = by * 4 + (t_in >> 3), gx = bx * 8 + (t_in & 7);
+    const int iy0 = 2 * gy - prm.p, ix0 = 2 * gx - prm.p;
+    auto load_tile = [&](int chunk, float (&d)[16]) {
+        const int ci = chunk * kWgCb + c_in;
+        const float* plane = prm.x + ((long long)n * prm.Ci + ci) * prm.H * prm.W;
 #pragma unroll
-        for (int j = 0; j < kWgRawPerThread; ++j) {
-            const int idx = tid + j * kWgThreads;
-            r[j] = 0.f;
-            if (idx >= kWgRawFloats) continue;
-            const int c = idx / (kWgRawRows * kWgRawCols), rem = idx - c * (kWgRawRows * kWgRawCols);
-            const int rr = rem / kWgRawCols, cc = rem - rr * kWgRawCols;
-            const int ci = chunk * kWgCb + c, iy = iy0 + rr, ix = ix0 + cc;
-            if (ci < prm.Ci && iy >= 0 && iy < prm.H && ix >= 0 && ix < prm.W)
-                r[j] = __ldg(prm.x + (((long long)n * prm.Ci + ci) * prm.H + iy) * prm.W + ix);
-        }
-    };
-    auto store_region = [&](const float (&r)[kWgRawPerThread]) {
+        for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int j = 0; j < kWgRawPerThread; ++j) {
-            const int idx = tid + j * kWgThreads;
-            if (idx < kWgRawFloats) raw[idx] = r[j];
-        }
+            for (int q = 0; q < 4; ++q) {
+                const int iy = iy0 + r, ix = ix0 + q;
+                d[4 * r + q] = (ci < prm.Ci && iy >= 0 && iy < prm.H && ix >= 0 && ix < prm.W)
+                                   ? __ldg(plane + (long long)iy * prm.W + ix)
+                                   : 0.f;
+            }
     };
-    // Thread pair (c, t): B^T d B of tile t of stage channel c; half h writes rows 2h, 2h+1.
-    const int c_in = (tid >> 6), t_in = tid & 31, h_in = (tid >> 5) & 1;
-    auto transform = [&](int stage) {
-        const float* d = raw + c_in * (kWgRawRows * kWgRawCols) + (2 * (t_in >> 3)) * kWgRawCols + 2 * (t_in & 7);
+    // B^T d B into V[c][e][t] of a stage.
+    auto store_tile = [&](int stage, const float (&d)[16]) {
         float t[16];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {      // columns: B^T along rows
-            const float d0 = d[q], d1 = d[kWgRawCols + q], d2 = d[2 * kWgRawCols + q], d3 = d[3 * kWgRawCols + q];
+            const float d0 = d[q], d1 = d[4 + q], d2 = d[8 + q], d3 = d[12 + q];
             t[q] = d0 - d2;
             t[4 + q] = d1 + d2;
             t[8 + q] = d2 - d1;
@@ -165,8 +152,7 @@ __global__ void __launch_bounds__(kWgThreads, 1) winograd_f2x3_kernel(const WgPa
         }
         float* v = smem + stage * kWgStageFloats + c_in * 16 * kWgTiles + t_in;
 #pragma unroll
-        for (int aa = 0; aa < 2; ++aa) {   // rows: B along columns
-            const int a = 2 * h_in + aa;
+        for (int a = 0; a < 4; ++a) {      // rows: B along columns
             const float h0 = t[4 * a], h1 = t[4 * a + 1], h2 = t[4 * a + 2], h3 = t[4 * a + 3];
             v[(4 * a + 0) * kWgTiles] = h0 - h2;
             v[(4 * a + 1) * kWgTiles] = h1 + h2;
@@ -182,50 +168,54 @@ __global__ void __launch_bounds__(kWgThreads, 1) winograd_f2x3_kernel(const WgPa
         bulk_load(smem_addr(smem + stage * kWgStageFloats + kWgVFloats), src, kWgUFloats * 4, bar);
     };
 
-    float acc[8][8];
+    float acc[2][8][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int e = 0; e < 2; ++e)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[e][i][j] = 0.f;
 
     {
-        float r[kWgRawPerThread];
+        float d[16];
         if (tid == 0) issue_u(0, 0);
-        load_region(0, r);
-        store_region(r);
-        __syncthreads();
-        transform(0);
+        load_tile(0, d);
+        store_tile(0, d);
     }
     __syncthreads();
-    const int ti = lane >> 3, ki = lane & 7, e = warp;
+    const int ti = lane >> 3, ki = lane & 7;
     bool ok = true;
     for (int k = 0; k < n_chunks; ++k) {
         const int s = k & 1;
-        float r[kWgRawPerThread];
+        float d[16];
         const bool more = k + 1 < n_chunks;
         if (more) {
             if (tid == 0) issue_u(k + 1, s ^ 1);   // stage s^1 is free: its last reader finished before the barrier
-            load_region(k + 1, r);
+            load_tile(k + 1, d);
         }
         if (mbar_wait(smem_addr(&bars[s]), (uint32_t)((k >> 1) & 1), &abort_flag)) {
-            const float* vs = smem + s * kWgStageFloats + e * kWgTiles + 8 * ti;
-            const float* us = smem + s * kWgStageFloats + kWgVFloats + e * kWgCo + 8 * ki;
+            const float* vs = smem + s * kWgStageFloats;
+            const float* us = vs + kWgVFloats;
 #pragma unroll 2
             for (int c = 0; c < kWgCb; ++c) {
-                const float4 va = *reinterpret_cast<const float4*>(vs + c * 16 * kWgTiles);
-                const float4 vb = *reinterpret_cast<const float4*>(vs + c * 16 * kWgTiles + 4);
-                const float4 ua = *reinterpret_cast<const float4*>(us + c * 16 * kWgCo);
-                const float4 ub = *reinterpret_cast<const float4*>(us + c * 16 * kWgCo + 4);
-                const float vv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-                const float uu[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
+                for (int ee = 0; ee < 2; ++ee) {
+                    const int e = 2 * warp + ee;
+                    const float4 va = *reinterpret_cast<const float4*>(vs + (c * 16 + e) * kWgTiles + 8 * ti);
+                    const float4 vb = *reinterpret_cast<const float4*>(vs + (c * 16 + e) * kWgTiles + 8 * ti + 4);
+                    const float4 ua = *reinterpret_cast<const float4*>(us + (c * 16 + e) * kWgCo + 8 * ki);
+                    const float4 ub = *reinterpret_cast<const float4*>(us + (c * 16 + e) * kWgCo + 8 * ki + 4);
+                    const float vv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+                    const float uu[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(vv[i], uu[j], acc[i][j]);
+                    for (int i = 0; i < 8; ++i)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) acc[ee][i][j] = fmaf(vv[i], uu[j], acc[ee][i][j]);
+                }
             }
         }
-        if (more) store_region(r);
-        __syncthreads();                           // region k+1 stored; every warp done with stage s
+        if (more) store_tile(s ^ 1, d);
+        __syncthreads();
         if (*reinterpret_cast<volatile int*>(&abort_flag)) {
             // Let the filter copies issued for this stage and the next land before exiting.
             if (tid == 0) {
@@ -235,19 +225,19 @@ __global__ void __launch_bounds__(kWgThreads, 1) winograd_f2x3_kernel(const WgPa
             ok = false;
             break;
         }
-        if (more) {
-            transform(s ^ 1);
-            __syncthreads();                       // V of stage k+1 complete
-        }
     }
     if (!ok) return;
 
     // Sums of the 16 transform points, [e][k][t], then A^T m A per (tile, channel).
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        float* dst = smem + (e * kWgCo + 8 * ki + j) * kWgTiles + 8 * ti;
-        reinterpret_cast<float4*>(dst)[0] = make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
-        reinterpret_cast<float4*>(dst)[1] = make_float4(acc[4][j], acc[5][j], acc[6][j], acc[7][j]);
+    for (int ee = 0; ee < 2; ++ee) {
+        const int e = 2 * warp + ee;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float* dst = smem + (e * kWgCo + 8 * ki + j) * kWgTiles + 8 * ti;
+            reinterpret_cast<float4*>(dst)[0] = make_float4(acc[ee][0][j], acc[ee][1][j], acc[ee][2][j], acc[ee][3][j]);
+            reinterpret_cast<float4*>(dst)[1] = make_float4(acc[ee][4][j], acc[ee][5][j], acc[ee][6][j], acc[ee][7][j]);
+        }
     }
     __syncthreads();
     const int t = tid & 31;
@@ -258,7 +248,7 @@ __global__ void __launch_bounds__(kWgThreads, 1) winograd_f2x3_kernel(const WgPa
         if (co >= prm.Co) break;
         float m[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) m[q] = smem[(q * kWgCo + kk) * kWgTiles + t];
+        for (int e = 0; e < 16; ++e) m[e] = smem[(e * kWgCo + kk) * kWgTiles + t];
         float r0[4], r1[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {      // A^T along rows
