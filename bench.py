@@ -352,6 +352,34 @@ def run_gpu(args, rank, world):
     n_pipe = 6 if args.quick else max(6, min(K, 100))
     e2e_pipelined(min(n_pipe, 6))                        # warm-up
     e2e = max_over_ranks(e2e_pipelined(n_pipe), world, dev)
+
+    # The bound of that mode: the same pinned-host copies (X and W in, Y out)
+    # on the same three streams, with no convolution in between.
+    def copies_only(nsteps):
+        streams = [torch.cuda.Stream(dev) for _ in range(3)]
+        y_hosts = [torch.empty(y.shape, dtype=tdt, pin_memory=True) for _ in range(3)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for s_ in streams:
+            s_.wait_event(t0)
+        for i in range(nsteps):
+            k = i % 3
+            xi, wi, yi, _ = sets[k + 3 * ((i // 3) % (n_sets // 3))]
+            with torch.cuda.stream(streams[k]):
+                xi.copy_(xh, non_blocking=True)
+                wi.copy_(wh, non_blocking=True)
+                y_hosts[k].copy_(yi, non_blocking=True)
+        for s_ in streams:
+            ev = torch.cuda.Event()
+            ev.record(s_)
+            stream.wait_event(ev)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / nsteps
+
+    copies_only(min(n_pipe, 6))
+    copy_ms = max_over_ranks(copies_only(n_pipe), world, dev)
     assert capi.conv2d_device_status(sp) == 0
 
     flops = wl.flops()
@@ -406,7 +434,11 @@ def run_gpu(args, rank, world):
                 "h2d_bytes_per_step": xh.numel() * xh.element_size() + wh.numel() * wh.element_size(),
                 "d2h_bytes_per_step": yh.numel() * yh.element_size(), "ms_per_step": e2e,
                 "mode": "conv2d_fwd_host calls round-robin on three streams (copies of one call overlap others' compute)",
-                "serial_ms_per_step": e2e_serial},
+                "serial_ms_per_step": e2e_serial,
+                "copy_bound_ms_per_step": copy_ms,
+                "copy_bound": "the same pinned host<->device copies on the same three streams, no convolution",
+                "link_gbs": (xh.numel() * xh.element_size() + wh.numel() * wh.element_size()
+                             + yh.numel() * yh.element_size()) / (copy_ms * 1e-3) / 1e9},
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not (args.no_cpu_baseline or args.quick):

@@ -67,9 +67,14 @@ bool tc_shape_ok(const conv2d_desc& d, bool im2win) {
 }
 
 // Recorded per-shape choice.  fp32: the im2win strips (the method of the
-// im2win paper) unless the row width keeps the direct staging off 16-byte
-// boundaries.  16-bit: the operand source that wastes less of the 64-wide K
-// chunk; ties go to the implicit path, which needs less workspace.
+// im2win paper).  16-bit: the padded path where its halo reuse pays (below);
+// otherwise the window tensor only for small channel counts (Ci8 <= 16),
+// where its dense (row, channel) packing fills the 64-wide K chunk that a
+// 3-channel tap would leave nearly empty, and the channels-last copy for the
+// rest: the window tensor is about Kh/s times X, and its transform costs more
+// than the copy saves in K fill (measured on GB300, the im2win paper's cv5,
+// 96 channels, 5x5: 198.8 us per call on the window path, 113.5 us on the
+// channels-last one).
 conv2d_algo resolve_auto(const conv2d_desc& d) {
     if (d.dtype == CONV2D_F32) return CONV2D_ALGO_IM2WIN_FP32_CC;
     if (d.layout == CONV2D_LAYOUT_NHWC) return CONV2D_ALGO_IMPLICIT_TC;
@@ -80,7 +85,8 @@ conv2d_algo resolve_auto(const conv2d_desc& d) {
     if (d.s == 1 && d.Kw >= 2 && padded_waste(d) <= 0.15 && (d.Ci + 7) / 8 * 8 >= 64)
         return CONV2D_ALGO_PADDED_TC;
     const bool imp_ok = tc_shape_ok(d, false), win_ok = tc_shape_ok(d, true);
-    if (imp_ok && (!win_ok || tc_k_efficiency(d, false) >= tc_k_efficiency(d, true)))
+    const bool small_ci = (d.Ci + 7) / 8 * 8 <= 16;
+    if (imp_ok && (!win_ok || !small_ci || tc_k_efficiency(d, false) >= tc_k_efficiency(d, true)))
         return CONV2D_ALGO_IMPLICIT_TC;
     return CONV2D_ALGO_IM2WIN_TC;
 }
@@ -112,6 +118,7 @@ conv2d_status finalize(conv2d_desc& d) {
         if (d.algo == CONV2D_ALGO_IM2WIN_FP32_CC) {
             const long long strips = (long long)d.N * d.Ci * d.Ho * d.Lp;
             if (strips / 4 > kMaxElems) return CONV2D_ERR_UNSUPPORTED;   // 32-bit vector index
+            if ((long long)d.Kh * d.W * 4 > kStripSmemMax) return CONV2D_ERR_UNSUPPORTED;   // staged rows
             d.ws_input = (size_t)strips * 4;
         } else {
             if (d.W % 4 != 0) return CONV2D_ERR_UNSUPPORTED;    // 16-byte row pitch for the row copies
@@ -176,6 +183,9 @@ conv2d_status finalize(conv2d_desc& d) {
             if (rows * d.Ci8 > kMaxElems * 4) return CONV2D_ERR_UNSUPPORTED;
             d.ws_input = (size_t)(rows * d.Ci8) * 2;
         } else if (im2win) {
+            // Window transform for Ci8 > 16: Kh rows x Ci8 channels of at least 16 staged columns
+            // plus one output column per block in shared memory.
+            if (d.Ci8 > 16 && (long long)d.Kh * d.Ci8 * (16 * 2 + 2) + 16 > 200 * 1024) return CONV2D_ERR_UNSUPPORTED;
             d.Hp = d.Ho;
             d.Wq = window_grid_pitch(d);
             const long long rows = (long long)d.N * d.Ho * d.Wq;

@@ -51,6 +51,7 @@ namespace conv2d_gb300 {
 
 constexpr int kTcBlockM = 128;   // output pixels per MMA tile
 constexpr int kTcBlockK = 64;    // K elements per pipeline stage (128 bytes of 16-bit)
+constexpr long long kStripSmemMax = 200 * 1024;   // fp32 im2win transform: staged input rows per block
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

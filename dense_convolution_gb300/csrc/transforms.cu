@@ -18,34 +18,58 @@
 namespace conv2d_gb300 {
 
 // ---------------------------------------------------------------- fp32 strips
-// One thread writes one 16-byte vector (4 consecutive strip elements) and the
-// grid strides over all vectors, so consecutive threads write consecutive
-// bytes across strip boundaries.  Reads walk Kh neighbouring input rows and
-// are served by L1/L2.  32-bit index arithmetic (the launcher checks the
-// vector count fits).
+// A block makes the strips of `rows` (up to kStripRows) consecutive output rows of one
+// (n, ci) plane.  It first stages the input rows those strips read —
+// (rows - 1)*s + Kh rows of W floats, zero rows for the padding above and
+// below — with 16-byte loads where the rows allow (W % 4 == 0), then writes
+// each strip as 16-byte vectors, consecutive threads on consecutive vectors:
+// strip element e = kx*Kh + u is staged row (r*s + u) at column kx - p (zero
+// outside [0, W)).
+constexpr int kStripRows = 32;
+constexpr long long kStripSmemTarget = 48 * 1024;   // several blocks per SM
+
 __global__ void __launch_bounds__(256) im2win_strips_f32_kernel(const float* __restrict__ x,
                                                                 float4* __restrict__ xw, int Ci, int H, int W,
                                                                 int Ho, int Kh, int s, int p, int Wp, int Lp,
-                                                                int total_vec) {
+                                                                int rows, int n_rb, int vec_ok) {
+    extern __shared__ __align__(16) float srows[];            // [n_y][W]
     pdl_launch_dependents();
+    const int rb = blockIdx.x % n_rb;
+    const long long nc = blockIdx.x / n_rb;                   // n*Ci + ci
+    const int r0 = rb * rows, nrows = min(rows, Ho - r0);
+    const int n_y = (nrows - 1) * s + Kh;
+    const int y_lo = r0 * s - p;
+    const float* plane = x + nc * (long long)H * W;
+    if (vec_ok) {
+        const int wv = W >> 2;
+        for (int i = threadIdx.x; i < n_y * wv; i += blockDim.x) {
+            const int yi = i / wv, v = i - yi * wv;
+            const int y = y_lo + yi;
+            float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (y >= 0 && y < H) val = __ldg(reinterpret_cast<const float4*>(plane + (long long)y * W) + v);
+            reinterpret_cast<float4*>(srows + yi * W)[v] = val;
+        }
+    } else {
+        for (int i = threadIdx.x; i < n_y * W; i += blockDim.x) {
+            const int yi = i / W, xx = i - yi * W;
+            const int y = y_lo + yi;
+            srows[i] = (y >= 0 && y < H) ? __ldg(plane + (long long)y * W + xx) : 0.f;
+        }
+    }
+    __syncthreads();
     const int Lv = Lp >> 2;
-    for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < total_vec; q += gridDim.x * blockDim.x) {
-        const int strip = q / Lv;                       // (n*Ci + ci)*Ho + ho
-        const int e = (q - strip * Lv) * 4;
-        const int nc = strip / Ho;
-        const int ho = strip - nc * Ho;
-        const float* plane = x + (long long)nc * H * W;
-        int kx = e / Kh, u = e - kx * Kh;
+    float4* out = xw + (nc * Ho + r0) * (long long)Lv;
+    for (int q = threadIdx.x; q < nrows * Lv; q += blockDim.x) {
+        const int r = q / Lv, e0 = (q - r * Lv) * 4;
+        int kx = e0 / Kh, u = e0 - kx * Kh;
         float v[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int y = ho * s + u - p, xx = kx - p;
-            float val = 0.f;
-            if (kx < Wp && y >= 0 && y < H && xx >= 0 && xx < W) val = __ldg(plane + y * W + xx);
-            v[j] = val;
+            const int xx = kx - p;
+            v[j] = (kx < Wp && xx >= 0 && xx < W) ? srows[(r * s + u) * W + xx] : 0.f;
             if (++u == Kh) { u = 0; ++kx; }
         }
-        xw[q] = make_float4(v[0], v[1], v[2], v[3]);
+        out[q] = make_float4(v[0], v[1], v[2], v[3]);
     }
     pdl_wait();   // complete only after the filter repack launched before us
 }
@@ -53,11 +77,19 @@ __global__ void __launch_bounds__(256) im2win_strips_f32_kernel(const float* __r
 cudaError_t launch_im2win_strips_f32(const float* x, float* xw, const conv2d_desc& d, cudaStream_t st, bool pdl) {
     const long long total_vec = (long long)d.N * d.Ci * d.Ho * (d.Lp / 4);
     if (total_vec > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    const long long blocks = (total_vec + 255) / 256, cap = (long long)device_sm_count() * 16;
-    const int grid = (int)(blocks < cap ? blocks : cap);
-    return launch_chain(pdl, im2win_strips_f32_kernel, dim3(grid < 1 ? 1 : grid), dim3(256), 0, st, x,
-                        reinterpret_cast<float4*>(xw), d.Ci, d.H, d.W, d.Ho, d.Kh, d.s, d.p, d.Wp, d.Lp,
-                        (int)total_vec);
+    int rows = kStripRows;
+    while (rows > 1 && (long long)((rows - 1) * d.s + d.Kh) * d.W * 4 > kStripSmemTarget) --rows;
+    const int n_rb = (d.Ho + rows - 1) / rows;
+    const long long blocks = (long long)d.N * d.Ci * n_rb;
+    const long long smem = (long long)((rows - 1) * d.s + d.Kh) * d.W * 4;
+    if (blocks > 0x7fffffffLL || smem > kStripSmemMax) return cudaErrorInvalidConfiguration;
+    cudaError_t e = cudaFuncSetAttribute(im2win_strips_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    const int vec_ok = (d.W % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) ? 1 : 0;
+    return launch_chain(pdl, im2win_strips_f32_kernel, dim3((unsigned)blocks), dim3(256), (size_t)smem, st, x,
+                        reinterpret_cast<float4*>(xw), d.Ci, d.H, d.W, d.Ho, d.Kh, d.s, d.p, d.Wp, d.Lp, rows,
+                        n_rb, vec_ok);
 }
 
 // ---------------------------------------------------------------- 16-bit NCHW -> NHWC (channels padded to 8)
@@ -204,48 +236,81 @@ cudaError_t launch_nchw_to_padded_nhwc16(const void* x, void* out, const conv2d_
 }
 
 // ---------------------------------------------------------------- 16-bit channels-innermost window
-// Tiled version: a block transposes a 64-channel x 32-column tile of one input
-// row (reads coalesced along x) and writes it channel-innermost, one 16-byte
-// vector (8 channels) per thread.
-constexpr int kWinTileC = 64;
-constexpr int kWinTileX = 32;
-
+// Tiled version (Ci8 > 16): a block makes the window-tensor run of one image
+// row r and XT consecutive padded columns kx0.., i.e. out[n][r][kx][u][c] for
+// all (u, c): one contiguous run of XT*Kh*Ci8 elements.  It stages the Kh
+// input rows r*s + u - p, all Ci8 channels (zero past Ci and outside the
+// image), columns [xa, xa + XTs) with xa = kx0 - p rounded down to 8, as
+// [u][c][col] with 16-byte loads where the rows allow (W % 8 == 0; 8-byte
+// loads when W % 4 == 0); then
+// transposes 8 channels x 8 columns at a time (ldmatrix .trans) into a second
+// buffer laid out like the output run (stmatrix: one 16-byte row per
+// (column, u, 8 channels); columns outside the tile go to a discard row); then
+// copies that buffer to the output with 16-byte stores, consecutive threads
+// on consecutive vectors.
 __global__ void __launch_bounds__(256) window_cl16_tiled_kernel(const uint16_t* __restrict__ x,
                                                                 uint4* __restrict__ out, int Ci, int H, int W,
                                                                 int Ci8, int R, int Wq, int Kh, int s, int p,
-                                                                int n_xt, int n_ct) {
-    __shared__ uint16_t tile[kWinTileC][kWinTileX + 2];
+                                                                int XT, int XTs, int n_xt, int vec_ok) {
+    extern __shared__ __align__(16) uint16_t wsm[];
+    uint16_t* in = wsm;                                   // [Kh][Ci8][XTs]
+    uint16_t* ob = wsm + (size_t)Kh * Ci8 * XTs;          // [XT][Kh][Ci8], then a 16-byte discard row
     pdl_launch_dependents();
-    long long b = blockIdx.x;
-    const int xt = (int)(b % n_xt); b /= n_xt;
-    const int ct = (int)(b % n_ct); b /= n_ct;
-    const int u = (int)(b % Kh);    b /= Kh;
-    const long long nr = b;                              // n*R + r
+    const int xt = blockIdx.x % n_xt;
+    const long long nr = blockIdx.x / n_xt;               // n*R + r
     const int r = (int)(nr % R);
     const long long n = nr / R;
-    const int y = r * s + u - p;
-    const int kx0 = xt * kWinTileX, c0 = ct * kWinTileC;
-    const bool row_ok = (y >= 0 && y < H);
+    const int kx0 = xt * XT;
+    const int xt_n = min(XT, Wq - kx0);
+    int xa = kx0 - p;
+    xa = xa >= 0 ? (xa & ~7) : -((-xa + 7) & ~7);        // floor to a multiple of 8
+    const int nv = XTs / 8;
+    for (int i = threadIdx.x; i < Kh * Ci8 * nv; i += 256) {
+        const int v = i % nv, uc = i / nv;
+        const int c = uc % Ci8, u = uc / Ci8;
+        const int y = r * s + u - p, x0 = xa + 8 * v;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (c < Ci && y >= 0 && y < H) {
+            const uint16_t* src = x + ((n * Ci + c) * H + y) * (long long)W;
+            if (vec_ok == 2 && x0 >= 0 && x0 + 8 <= W) {
+                val = __ldg(reinterpret_cast<const uint4*>(src + x0));
+            } else if (vec_ok == 1 && x0 >= 0 && x0 + 8 <= W) {       // rows 8-byte aligned (W % 4 == 0)
+                const uint2 lo = __ldg(reinterpret_cast<const uint2*>(src + x0));
+                const uint2 hi = __ldg(reinterpret_cast<const uint2*>(src + x0 + 4));
+                val = make_uint4(lo.x, lo.y, hi.x, hi.y);
+            } else {
+                uint32_t w4[4] = {0, 0, 0, 0};
 #pragma unroll
-    for (int i = 0; i < (kWinTileC * kWinTileX) / 256; ++i) {
-        int e = threadIdx.x + 256 * i;
-        int c = e / kWinTileX, k = e % kWinTileX;
-        int xx = kx0 + k - p, cc = c0 + c;
-        uint16_t v = 0;
-        if (row_ok && cc < Ci && xx >= 0 && xx < W) v = x[((n * Ci + cc) * H + y) * (long long)W + xx];
-        tile[c][k] = v;
+                for (int e = 0; e < 8; ++e)
+                    if (x0 + e >= 0 && x0 + e < W) w4[e >> 1] |= (uint32_t)__ldg(src + x0 + e) << (16 * (e & 1));
+                val = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+        }
+        *reinterpret_cast<uint4*>(in + (size_t)uc * XTs + 8 * v) = val;
     }
     __syncthreads();
-    const int k = threadIdx.x / 8, cg = threadIdx.x % 8;
-    const int kx = kx0 + k, cc = c0 + cg * 8;
-    if (kx < Wq && cc < Ci8) {
-        uint32_t w[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            w[j] = (uint32_t)tile[cg * 8 + 2 * j][k] | ((uint32_t)tile[cg * 8 + 2 * j + 1][k] << 16);
-        long long o = ((nr * Wq + kx) * Kh + u) * (long long)Ci8 + cc;
-        out[o >> 3] = make_uint4(w[0], w[1], w[2], w[3]);
+    // Transpose: x4 item = (u, 32 channels, 8 columns); lane 8i + j addresses
+    // row j (channel) of matrix i for the load and row j (column) for the store.
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c32 = (Ci8 + 31) / 32, items = Kh * c32 * nv;
+    const uint32_t discard = smem_addr(ob + (size_t)XT * Kh * Ci8);
+    for (int it = warp; it < items; it += 8) {
+        const int v = it % nv, rest = it / nv;
+        const int cq = rest % c32, u = rest / c32;
+        const int mi = lane >> 3, j = lane & 7;
+        int c = cq * 32 + mi * 8 + j;
+        if (c >= Ci8) c = Ci8 - 1;                        // a matrix past Ci8: load any row, store nowhere
+        uint32_t q[4];
+        ldsm_x4_trans(smem_addr(in + ((size_t)u * Ci8 + c) * XTs + 8 * v), q);
+        const int col = xa + 8 * v + j + p - kx0;         // tile column of this lane's row
+        const int cg = cq * 32 + mi * 8;
+        const bool ok = col >= 0 && col < xt_n && cg < Ci8;
+        stsm_x4(ok ? smem_addr(ob + ((size_t)col * Kh + u) * Ci8 + cg) : discard, q);
     }
+    __syncthreads();
+    const long long run = (long long)xt_n * Kh * Ci8 / 8;  // 16-byte vectors
+    uint4* dst = out + ((nr * Wq + kx0) * (long long)Kh * Ci8) / 8;
+    for (long long i = threadIdx.x; i < run; i += 256) dst[i] = reinterpret_cast<const uint4*>(ob)[i];
     pdl_wait();   // complete only after the filter repack launched before us
 }
 
@@ -295,6 +360,7 @@ __global__ void __launch_bounds__(256) window_cl16_small_kernel(const uint16_t* 
 // pairs from shared memory: pair c = u*Ci + ci of window row r is staged row
 // (r - r0)*s*Ci + c.  The row pitch kWinRowPitch (not a multiple of 8 halves)
 // spreads rows 8 apart over different banks.
+constexpr long long kWindowSmemTarget = 64 * 1024;   // tiled window: both buffers of a block
 constexpr int kWinRowX = 128;                 // output columns per block
 constexpr int kWinRowCols = kWinRowX + 8;     // staged input columns (the 8-alignment slack)
 constexpr int kWinRowPitch = kWinRowCols + 2;
@@ -380,11 +446,25 @@ cudaError_t launch_window_cl16(const void* x, void* out, int N, int Ci, int H, i
         return launch_chain(pdl, window_cl16_small_kernel, dim3(grid < 1 ? 1 : grid), dim3(256), 0, st, xi, o, Ci, H, W,
                             Ck, R, Wq, Kh, s, p, total_vec);
     } else {
-        int n_xt = (Wq + kWinTileX - 1) / kWinTileX, n_ct = (Ci8 + kWinTileC - 1) / kWinTileC;
-        long long blocks = (long long)n_xt * n_ct * Kh * N * R;
+        // Columns per block: as many as keep both buffers within the budget (at least 1).
+        const long long per_col = (long long)Kh * Ci8 * 2 * 2;   // staged input + output bytes per column
+        int XT = (int)((kWindowSmemTarget - (long long)Kh * Ci8 * 2 * 8 - 16) / per_col);
+        if (XT > 64) XT = 64;
+        if (XT > Wq) XT = Wq;
+        if (XT < 1) XT = 1;
+        const int XTs = (XT + 7 + 7) / 8 * 8;
+        const long long smem = (long long)Kh * Ci8 * XTs * 2 + (long long)XT * Kh * Ci8 * 2 + 16;
+        if (smem > 200 * 1024) return cudaErrorInvalidConfiguration;
+        const int n_xt = (Wq + XT - 1) / XT;
+        const long long blocks = (long long)n_xt * N * R;
         if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-        return launch_chain(pdl, window_cl16_tiled_kernel, dim3((unsigned)blocks), dim3(256), 0, st, xi, o, Ci, H, W, Ci8,
-                            R, Wq, Kh, s, p, n_xt, n_ct);
+        cudaError_t e = cudaFuncSetAttribute(window_cl16_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        const bool a16 = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+        const int vec_ok = (W % 8 == 0 && a16) ? 2 : ((W % 4 == 0 && a16) ? 1 : 0);
+        return launch_chain(pdl, window_cl16_tiled_kernel, dim3((unsigned)blocks), dim3(256), (size_t)smem, st, xi, o,
+                            Ci, H, W, Ci8, R, Wq, Kh, s, p, XT, XTs, n_xt, vec_ok);
     }
 }
 
