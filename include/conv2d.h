@@ -17,7 +17,9 @@
  *   - All functions return a conv2d_status; no C++ exception crosses the ABI.
  *   - Device pointers are plain CUDA device addresses owned by the caller.
  *     The library never allocates, frees or retains device memory, and keeps
- *     no pointer after a call returns.
+ *     no pointer after a call returns, except the bias pointer a caller sets
+ *     on a descriptor (conv2d_desc_set_bias), which that descriptor's calls
+ *     read.
  *   - `stream` is a cudaStream_t (or CUstream) cast to void*; NULL is the
  *     legacy default stream.  Kernels are launched asynchronously on it;
  *     conv2d_fwd returns once the launches are queued.
