@@ -200,10 +200,28 @@ conv2d_status finalize(conv2d_desc& d) {
     if (d.prepacked) {   // the filter lives in the caller's packed buffer
         d.ws_input_off = 0;
         d.ws_total = d.ws_input;
-        return CONV2D_OK;
+    } else {
+        d.ws_input_off = d.ws_input ? align_up(d.ws_weights, 1024) : 0;
+        d.ws_total = d.ws_input ? d.ws_input_off + d.ws_input : d.ws_weights;
     }
-    d.ws_input_off = d.ws_input ? align_up(d.ws_weights, 1024) : 0;
-    d.ws_total = d.ws_input ? d.ws_input_off + d.ws_input : d.ws_weights;
+    // Split tail (tensor-core modes that take the im2col, padded or window
+    // source): room for the partial sums of grid - 1 share boundaries on the
+    // current device (a 148-SM one when there is none), when the tile groups
+    // leave the last wave short and the total stays within the im2win tensor
+    // N*Ci*Ho*(W+2p)*Kh of the im2win paper's Eq. (2).
+    d.ws_split_off = d.ws_split = 0;
+    const bool splittable = (d.algo == CONV2D_ALGO_IMPLICIT_TC && !d.gemm1x1) || d.algo == CONV2D_ALGO_PADDED_TC ||
+                            d.algo == CONV2D_ALGO_IM2WIN_TC;
+    if (splittable && !d.tune_no_split) {
+        const size_t need = tc_split_need(d, device_sm_count());
+        const double cap = 2.0 * d.N * d.Ci * d.Ho * (double)(d.W + 2 * d.p) * d.Kh;
+        const size_t off = align_up(d.ws_total, 256);
+        if (need && (double)(off + need) <= cap) {
+            d.ws_split = need;
+            d.ws_split_off = off;
+            d.ws_total = off + need;
+        }
+    }
     return CONV2D_OK;
 }
 
@@ -286,6 +304,15 @@ CONV2D_API conv2d_status conv2d_desc_set_tuning(conv2d_desc_t d, conv2d_tuning k
             if (value < 0 || value > 1) return CONV2D_ERR_BAD_PARAM;
             d->tune_no_resident = value;
             return CONV2D_OK;
+        case CONV2D_TUNE_NO_SPLIT: {
+            if (value < 0 || value > 1) return CONV2D_ERR_BAD_PARAM;
+            conv2d_desc t = *d;
+            t.tune_no_split = value;
+            const conv2d_status st = finalize(t);   // the split's workspace comes or goes
+            if (st != CONV2D_OK) return st;
+            *d = t;
+            return CONV2D_OK;
+        }
     }
     return CONV2D_ERR_BAD_PARAM;
 }
@@ -412,7 +439,7 @@ conv2d_status fwd_impl(conv2d_desc_t dp, const void* x, const void* w, void* y, 
                 e = launch_window_cl16(x, win, d.N, d.Ci, d.H, d.W, d.Ci8, d.Ck, d.Ho, d.Wq * d.s, d.Kh, d.s, d.p,
                                        st, !pre);
             if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
-            if (e == cudaSuccess) s = launch_conv_tc(d, win, wq, y, 1, st);
+            if (e == cudaSuccess) s = launch_conv_tc(d, win, wq, y, 1, st, ws + d.ws_split_off, d.ws_split);
             break;
         case CONV2D_ALGO_IMPLICIT_TC: {
             if (d.gemm1x1) {   // no repack, no copy: one launch on the caller's tensors
@@ -427,7 +454,7 @@ conv2d_status fwd_impl(conv2d_desc_t dp, const void* x, const void* w, void* y, 
                 src = win;
             }
             if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
-            if (e == cudaSuccess) s = launch_conv_tc(d, src, wq, y, 0, st);
+            if (e == cudaSuccess) s = launch_conv_tc(d, src, wq, y, 0, st, ws + d.ws_split_off, d.ws_split);
             break;
         }
         case CONV2D_ALGO_IMPLICIT_NCHW_TC:   // the contraction kernel reads NCHW X itself
@@ -439,7 +466,7 @@ conv2d_status fwd_impl(conv2d_desc_t dp, const void* x, const void* w, void* y, 
             if (!pre) e = launch_pack_filter_tc(w, wq, d, false, st);
             if (e == cudaSuccess) e = launch_nchw_to_padded_nhwc16(x, win, d, st, !pre);
             if (e == cudaSuccess && !record(ev0, st)) return CONV2D_ERR_CUDA;
-            if (e == cudaSuccess) s = launch_conv_tc(d, win, wq, y, 2, st);
+            if (e == cudaSuccess) s = launch_conv_tc(d, win, wq, y, 2, st, ws + d.ws_split_off, d.ws_split);
             break;
         default:
             return CONV2D_ERR_BAD_PARAM;

@@ -52,6 +52,9 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+#include <chrono>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -100,7 +103,67 @@ struct TcParams {
                         // 2 zig-zag (channel tiles in alternating direction on successive pixel groups)
     int sync_copies;    // 1: the producer waits for each stage's copies before issuing the next stage
     int n_mg;           // pixel groups (ceil(n_m_tiles / group))
+    // Split tail (MODE 0/1): groups [0, g_dp) are taken whole, one per CTA per
+    // wave; the k-stages of the remaining groups (t_stages in all) are divided
+    // evenly over the CTAs.  A group's first contributor owns it: the others
+    // store fp32 partial accumulators in `part` and publish `epoch` in `flags`;
+    // the owner adds them before its epilogue.
+    // A contributor CTA c stores its partial in block (c - 1)*group + tile
+    // (each such c is a share boundary inside a group, so grid - 1 blocks
+    // per tile suffice) and its flag at the same index.
+    int split, g_dp;
+    long long t_stages;
+    float* part;
+    unsigned long long* flags;
+    unsigned long long epoch;
 };
+
+// One unit of a CTA's work: stages [k0, k1) of tile group g.
+struct TcItem {
+    int g, k0, k1;
+    int owner;          // 1: this CTA stores the group's output (it holds the group's first stage)
+    int n_contrib;      // CTAs that share the group
+    int c_first;        // the owner CTA (split groups)
+    int tg;             // tail group index (split groups), else -1
+};
+
+// First stage of CTA c's share of the tail.
+__device__ __forceinline__ long long tail_begin(const TcParams& prm, int c) {
+    return (long long)c * prm.t_stages / gridDim.x;
+}
+// The CTA whose share holds tail stage x.
+__device__ __forceinline__ int tail_cta(const TcParams& prm, long long x) {
+    int c = (int)(x * gridDim.x / prm.t_stages);
+    while (c + 1 < (int)gridDim.x && tail_begin(prm, c + 1) <= x) ++c;
+    while (c > 0 && tail_begin(prm, c) > x) --c;
+    return c;
+}
+
+// Item `idx` of this CTA (false when there is none): first its whole groups,
+// g = blockIdx.x + i*gridDim.x below g_dp, then the group pieces of its share
+// of the tail in stage order.  Every role of the CTA walks the same items.
+__device__ __forceinline__ bool tc_item(const TcParams& prm, int idx, TcItem& it) {
+    const int n_dp = prm.g_dp > (int)blockIdx.x ? (prm.g_dp - (int)blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    if (idx < n_dp) {
+        it.g = blockIdx.x + idx * gridDim.x;
+        it.k0 = 0; it.k1 = prm.n_sp; it.owner = 1; it.n_contrib = 1; it.c_first = blockIdx.x; it.tg = -1;
+        return true;
+    }
+    if (!prm.split) return false;
+    const long long b0 = tail_begin(prm, blockIdx.x), b1 = tail_begin(prm, blockIdx.x + 1);
+    const long long tg = b0 / prm.n_sp + (idx - n_dp);
+    const long long gs = tg * prm.n_sp, ge = gs + prm.n_sp;
+    if (b0 >= b1 || gs >= b1) return false;
+    it.tg = (int)tg;
+    it.g = prm.g_dp + (int)tg;
+    it.k0 = (int)((b0 > gs ? b0 : gs) - gs);
+    it.k1 = (int)((b1 < ge ? b1 : ge) - gs);
+    const int c_first = tail_cta(prm, gs), c_last = tail_cta(prm, ge - 1);
+    it.owner = (int)blockIdx.x == c_first;
+    it.n_contrib = c_last - c_first + 1;
+    it.c_first = c_first;
+    return true;
+}
 
 // Tile group g -> (channel tile nt, pixel group mg) in the chosen raster order.
 // Every role walks g = blockIdx.x, +gridDim.x, ... and maps it the same way.
@@ -448,7 +511,9 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
             uint32_t phase = 0;
             long long issued = 0;
             bool free_now = false;
-            for (int g = blockIdx.x; g < prm.n_groups && ok; g += gridDim.x) {
+            TcItem it;
+            for (int idx = 0; ok && tc_item(prm, idx, it); ++idx) {
+                const int g = it.g;
                 if constexpr (MODE == 4) {
                     // A is built by the halo builders; only filter chunks stream
                     // here, one per (channel chunk, tap), in the issuers' order.
@@ -505,8 +570,9 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                 const uint32_t tx = (uint32_t)(n_val * prm.a_bytes + (prm.b_res ? 0 : kpb * Cfg::kBBytes));
                 // Stage coordinates advance incrementally (no divisions in the loop):
                 // channel block cb, first tap t = kh*Kw + kw of the stage's kpb taps.
-                int cb = 0, t = 0, kw = 0, kh = 0;
-                for (int sp = 0; sp < prm.n_sp; ++sp) {
+                // Stage coordinates of stage k0: channel block cb, first tap t = kh*Kw + kw.
+                int cb = it.k0 % prm.n_cchunks, t = (it.k0 / prm.n_cchunks) * kpb, kw = t % prm.Kw, kh = t / prm.Kw;
+                for (int sp = it.k0; sp < it.k1; ++sp) {
                     if (!free_now && !mbar_wait(empty_bar(stage), phase ^ 1, abort_flag)) { ok = false; break; }
                     // Probe the next slot now; the answer is used one stage later, so
                     // the probe's latency hides behind this stage's copies.
@@ -574,7 +640,10 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
             bool ok = true, issued_any = false, ready_now = false;
             if (prm.b_res && !mbar_wait(bres_bar, 0, abort_flag)) ok = false;
             const uint32_t bres_base = smem_addr(smem + prm.b_res_off);
-            for (int g = blockIdx.x; g < prm.n_groups && ok; g += gridDim.x) {
+            TcItem it;
+            for (int idx = 0; ok && tc_item(prm, idx, it); ++idx) {
+                const int g = it.g;
+                (void)g;
                 if (!mbar_wait(acce_bar(is, acc), acc_phase ^ 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)((is * nacc + acc) * BN);
@@ -625,8 +694,8 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                     if (++acc == nacc) { acc = 0; acc_phase ^= 1; }
                     continue;
                 }
-                int cb = 0, t = 0;
-                for (int sp = 0; sp < prm.n_sp; ++sp) {
+                int cb = it.k0 % prm.n_cchunks, t = (it.k0 / prm.n_cchunks) * kpb;
+                for (int sp = it.k0; sp < it.k1; ++sp) {
                     if (!ready_now && !mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
                     // Probe the next slot before issuing this stage's MMAs (its answer
                     // is used one stage later).
@@ -646,7 +715,7 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
 #pragma unroll
                         for (int k = 0; k < kTcBlockK / 16; ++k)
                             umma_f16(d_tmem, b_desc + (uint64_t)(2 * k), x_desc + (uint64_t)(128 * k), idesc,
-                                     (sp > 0 || k > 0) ? 1u : 0u);
+                                     (sp > it.k0 || k > 0) ? 1u : 0u);
                     } else {
                         for (int i = 0; i < kpb; ++i) {
                             // Halo: tap kw0+i reads the A tile from row i (128 bytes per row).
@@ -655,7 +724,7 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                             for (int k = 0; k < kTcBlockK / 16; ++k) {
                                 umma_f16(d_tmem, a_desc + (uint64_t)(i * 8 + 2 * k),
                                          b_desc + (uint64_t)(i * (Cfg::kBBytes >> 4) + 2 * k), idesc,
-                                         (sp > 0 || i > 0 || k > 0) ? 1u : 0u);
+                                         (sp > it.k0 || i > 0 || k > 0) ? 1u : 0u);
                             }
                         }
                     }
@@ -691,7 +760,9 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
         uint16_t* wst = reinterpret_cast<uint16_t*>(smem + prm.epi_off + ew * kEpiWarpBytes);
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int g = blockIdx.x; g < prm.n_groups && eg < prm.group; g += gridDim.x) {
+        TcItem it;
+        for (int idx = 0; eg < prm.group && tc_item(prm, idx, it); ++idx) {
+            const int g = it.g;
             const bool got = mbar_wait(accf_bar(eg, acc), acc_phase, abort_flag);
             if (!named_bar_and(1 + eg, 128, got)) break;
             tc_fence_after();
@@ -894,14 +965,74 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                         if (cob + j < prm.Co) yout[poff + (long long)(cob + j) * prm.HoWo] = cvt(f[j]);
                 }
             };
+            // Split tail: contributor CTA c's partial accumulators are block
+            // (c - 1)*group + eg of prm.part, [pixel 0..127][channel 0..BN-1] fp32;
+            // this lane's row is pixel quarter*32 + lane.
+            const long long prow = (long long)(quarter * 32 + lane) * BN;
+            auto part_block = [&](int c) { return prm.part + ((long long)(c - 1) * prm.group + eg) * ((long long)kTcBlockM * BN); };
+            auto flag_of = [&](int c) { return prm.flags + (long long)(c - 1) * prm.group + eg; };
+            bool emit_y = true, add_parts = false;
+            if (it.tg >= 0 && !it.owner) {
+                // Contributor: store the partial sums, then publish this call's epoch.
+                float* dst = part_block(blockIdx.x) + prow;
+#pragma unroll 1
+                for (int cc = 0; cc < BN / 32; cc += 2) {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld_32x32b_x32(t_row + cc * 32, v0);
+                    tmem_ld_32x32b_x32(t_row + (cc + 1) * 32, v1);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        reinterpret_cast<uint4*>(dst + cc * 32)[q] = make_uint4(v0[4 * q], v0[4 * q + 1], v0[4 * q + 2], v0[4 * q + 3]);
+                        reinterpret_cast<uint4*>(dst + cc * 32 + 32)[q] =
+                            make_uint4(v1[4 * q], v1[4 * q + 1], v1[4 * q + 2], v1[4 * q + 3]);
+                    }
+                }
+                __threadfence();                              // this row before the flag
+                named_bar_sync(1 + eg, 128);                  // the group's 128 rows are written
+                if ((ew & 3) == 0 && lane == 0) {
+                    __threadfence();
+                    *reinterpret_cast<volatile unsigned long long*>(flag_of(blockIdx.x)) = prm.epoch;
+                }
+                emit_y = false;
+            } else if (it.tg >= 0 && it.n_contrib > 1) {
+                // Owner: wait (bounded) until every other contributor has published.
+                bool okf = true;
+                if ((ew & 3) == 0 && lane == 0)
+                    for (int c = it.c_first + 1; c < it.c_first + it.n_contrib && okf; ++c)
+                        okf = flag_wait(flag_of(c), prm.epoch, abort_flag);
+                if (!named_bar_and(1 + eg, 128, okf)) break;
+                __threadfence();
+                add_parts = true;
+            }
+            if (emit_y) {
 #pragma unroll 1
             for (int cc = 0; cc < BN / 32; cc += 2) {
                 uint32_t v0[32], v1[32];
                 tmem_ld_32x32b_x32(t_row + cc * 32, v0);
                 tmem_ld_32x32b_x32(t_row + (cc + 1) * 32, v1);
                 tmem_ld_wait();
+                if (add_parts) {
+                    for (int c = it.c_first + 1; c < it.c_first + it.n_contrib; ++c) {
+                        const float* src = part_block(c) + prow + cc * 32;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 a = __ldcg(reinterpret_cast<const float4*>(src) + q);
+                            const float4 b = __ldcg(reinterpret_cast<const float4*>(src + 32) + q);
+                            v0[4 * q] = __float_as_uint(__uint_as_float(v0[4 * q]) + a.x);
+                            v0[4 * q + 1] = __float_as_uint(__uint_as_float(v0[4 * q + 1]) + a.y);
+                            v0[4 * q + 2] = __float_as_uint(__uint_as_float(v0[4 * q + 2]) + a.z);
+                            v0[4 * q + 3] = __float_as_uint(__uint_as_float(v0[4 * q + 3]) + a.w);
+                            v1[4 * q] = __float_as_uint(__uint_as_float(v1[4 * q]) + b.x);
+                            v1[4 * q + 1] = __float_as_uint(__uint_as_float(v1[4 * q + 1]) + b.y);
+                            v1[4 * q + 2] = __float_as_uint(__uint_as_float(v1[4 * q + 2]) + b.z);
+                            v1[4 * q + 3] = __float_as_uint(__uint_as_float(v1[4 * q + 3]) + b.w);
+                        }
+                    }
+                }
                 emit(v0, cc);
                 emit(v1, cc + 1);
+            }
             }
             }
             tc_fence_before();
@@ -927,7 +1058,9 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
             const uint32_t discard =
                 smem_addr(smem + prm.stg_off + kTransposerWarps * prm.n_slots * kSegBytes + tw * 128);
             const uint32_t slot_bar0 = smem_addr(&sbars[tw * kMaxSlots]);
-            for (int g = blockIdx.x; g < prm.n_groups && ok; g += gridDim.x) {
+            TcItem it;
+            for (int idx = 0; ok && tc_item(prm, idx, it); ++idx) {
+                const int g = it.g;
                 int nt_, mg_;
                 tile_of(prm, g, nt_, mg_);
                 const int mt0 = mg_ * prm.group;
@@ -1044,8 +1177,42 @@ static cudaError_t launch_tc_mode(int BN, int amode, const CUtensorMap& a, const
     }
 }
 
+// Split-tail workspace: fp32 partial sums (128 pixels x BN channels) and one
+// 64-bit flag per tile of each of the grid - 1 share boundaries.
+size_t tc_split_bytes(int grid, int group, int BN) {
+    if (grid < 2) return 0;
+    const size_t blocks = (size_t)(grid - 1) * group;
+    return align_up(blocks * kTcBlockM * BN * 4, 256) + blocks * 8;
+}
+
+// Bytes of split-tail workspace a launch of this descriptor on `n_sm` SMs
+// uses (0 when its tile groups divide evenly enough): the same tile geometry
+// as launch_conv_tc.
+size_t tc_split_need(const conv2d_desc& d, int n_sm) {
+    const bool grid_rows = d.algo == CONV2D_ALGO_PADDED_TC || d.algo == CONV2D_ALGO_IM2WIN_TC;
+    const long long m = grid_rows ? (long long)(d.N - 1) * d.Hp * d.Wq + (long long)(d.Ho - 1) * d.Wq + d.Wo
+                                  : (long long)d.N * d.Ho * d.Wo;
+    const long long m_tiles = (m + kTcBlockM - 1) / kTcBlockM, n_tiles = (d.Co + d.BN - 1) / d.BN;
+    const int group = m_tiles * n_tiles >= 2LL * n_sm ? kIssuers : 1;
+    const long long n_groups = (m_tiles + group - 1) / group * n_tiles;
+    const long long grid = n_sm < n_groups ? n_sm : n_groups;
+    if (n_groups <= grid || n_groups % grid == 0) return 0;
+    const long long waves = (n_groups + grid - 1) / grid;
+    if ((double)n_groups / grid / waves >= 0.95) return 0;
+    return tc_split_bytes((int)grid, group, d.BN);
+}
+
+// A value no flag of an earlier call (this process or another) is likely to
+// hold: the call count, offset by the time the library first ran.
+static unsigned long long next_epoch() {
+    static std::atomic<unsigned long long> counter{0};
+    static const unsigned long long base =
+        (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() * 1000003ull;
+    return base + 2 * counter.fetch_add(1) + 1;
+}
+
 conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* wq, void* y, int amode,
-                             cudaStream_t st) {
+                             cudaStream_t st, void* split_ws, size_t split_bytes) {
     const bool im2win = amode == 1;
     auto enc_tiled = reinterpret_cast<PFN_encodeTiled_t>(driver_entry("cuTensorMapEncodeTiled"));
     auto enc_im2col = reinterpret_cast<PFN_encodeIm2col_t>(driver_entry("cuTensorMapEncodeIm2col"));
@@ -1310,6 +1477,27 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     if (smem < kSmemLimit / 2 + 4096) smem = kSmemLimit / 2 + 4096;
     int grid = n_sm;
     if (grid > prm.n_groups) grid = prm.n_groups;
+    // Split tail: when the groups do not divide evenly over the CTAs (the last
+    // wave leaves some SMs idle for a whole group) and that costs more than
+    // 5 %, the stages of the last partial wave are spread over all CTAs.
+    prm.split = 0;
+    prm.g_dp = prm.n_groups;
+    prm.t_stages = 0;
+    if ((amode == 0 || amode == 1 || amode == 2) && !d.tune_no_split && prm.n_groups > grid &&
+        prm.n_groups % grid != 0) {
+        const int waves = (prm.n_groups + grid - 1) / grid;
+        const double balance = (double)prm.n_groups / grid / waves;
+        const size_t need = tc_split_bytes(grid, group, d.BN);
+        if (balance < 0.95 && split_ws && need <= split_bytes) {
+            prm.split = 1;
+            prm.g_dp = prm.n_groups / grid * grid;
+            prm.t_stages = (long long)(prm.n_groups - prm.g_dp) * prm.n_sp;
+            prm.part = static_cast<float*>(split_ws);
+            prm.flags = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(split_ws) +
+                                                              align_up((size_t)(grid - 1) * group * kTcBlockM * d.BN * 4, 256));
+            prm.epoch = next_epoch();
+        }
+    }
 
     const bool bf = d.dtype == CONV2D_BF16;
     cudaError_t e = bf ? launch_tc_mode<true>(d.BN, amode, amap, bmap, ymap, prm, grid, smem, st)

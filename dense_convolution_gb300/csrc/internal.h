@@ -20,6 +20,7 @@ struct conv2d_desc {
     int tune_sync_copies;     // 1: each stage's copies land before the next stage's are issued
     int tune_raster;          // tile visit order (0 channel tile fastest, 1 pixel group fastest, 2 zig-zag)
     int tune_no_resident;     // 1: never keep the whole filter slice resident in shared memory
+    int tune_no_split;        // 1: never split the last partial wave of tiles over all SMs
     bool prepacked;           // conv2d_fwd's w is the filter conv2d_pack_filter wrote (no repack per call)
     // Derived geometry.
     int Ho, Wo, Wp;       // output size; padded input width W + 2p
@@ -45,6 +46,7 @@ struct conv2d_desc {
                           // of Wq output slots (window tensor rows hold Wq*s columns)
     // Workspace layout (bytes): packed filter at 0, input-side tensor after it.
     size_t ws_weights, ws_input_off, ws_input, ws_total;
+    size_t ws_split_off, ws_split;   // split-tail partial sums and flags (tensor-core modes 0-2), at the end
 };
 
 namespace conv2d_gb300 {
@@ -119,7 +121,9 @@ cudaError_t wait_limit_set_wg(cudaStream_t st, uint64_t ns);
 
 // conv_tc.cu
 conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* wq, void* y, int amode,
-                             cudaStream_t st);
+                             cudaStream_t st, void* split_ws = nullptr, size_t split_bytes = 0);
+size_t tc_split_bytes(int grid, int group, int BN);
+size_t tc_split_need(const conv2d_desc& d, int n_sm);
 int device_sm_count();
 bool halo_plan_fits(const conv2d_desc& d);
 void* driver_entry(const char* name);

@@ -159,6 +159,29 @@ __device__ __forceinline__ bool mbar_drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
+// Wait until a 64-bit flag in global memory (written by another CTA of this
+// grid) holds `value`.  Bounded like mbar_wait: gives up after the wait
+// limit, or once *abort is set, recording kStatusTimeout on a timeout.
+__device__ __forceinline__ bool flag_wait(const unsigned long long* flag, unsigned long long value,
+                                          volatile int* abort) {
+    const volatile unsigned long long* f = flag;
+    if (*f == value) return true;
+    const uint64_t t0 = global_timer_ns();
+    const uint64_t limit = g_wait_limit_ns;
+    for (uint32_t i = 1;; ++i) {
+        if (*f == value) return true;
+        if ((i & 63u) == 0) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > limit) {
+                atomicOr(&g_device_status, kStatusTimeout);
+                *abort = 1;
+                return false;
+            }
+        }
+        __nanosleep(64);
+    }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

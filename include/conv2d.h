@@ -189,12 +189,19 @@ conv2d_status conv2d_desc_set_bias(conv2d_desc_t d, const void *bias);
  *                             successive pixel groups).
  *   CONV2D_TUNE_NO_RESIDENT   1 = never keep the filter slice resident in
  *                             shared memory (tensor cores); 0 = automatic.
+ *   CONV2D_TUNE_NO_SPLIT      1 = take the last, partial wave of output tiles
+ *                             whole; 0 = automatic: when the tiles do not
+ *                             divide evenly over the SMs, the filter-tap range
+ *                             of the last wave is split evenly over all SMs and
+ *                             the partial sums are added before the epilogue
+ *                             (the sum's order changes, not its terms).
  * Errors: NULL_PTR, BAD_PARAM (unknown knob or value out of range). */
 typedef enum {
     CONV2D_TUNE_STAGES = 0,
     CONV2D_TUNE_SYNC_COPIES = 1,
     CONV2D_TUNE_RASTER = 2,
-    CONV2D_TUNE_NO_RESIDENT = 3
+    CONV2D_TUNE_NO_RESIDENT = 3,
+    CONV2D_TUNE_NO_SPLIT = 4
 } conv2d_tuning;
 conv2d_status conv2d_desc_set_tuning(conv2d_desc_t d, conv2d_tuning knob, int value);
 
