@@ -21,7 +21,7 @@ ALGOS = {"auto": 0, "im2win_fp32_cc": 1, "im2win_tc": 2, "implicit_tc": 3, "impl
          "implicit_nchw_tc": 6, "winograd_fp32_cc": 7}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 LAYOUTS = {"nchw": 0, "nhwc": 1}
-TUNING = {"stages": 0, "sync_copies": 1, "raster": 2, "no_resident": 3, "no_split": 4}
+TUNING = {"stages": 0, "sync_copies": 1, "raster": 2, "no_resident": 3, "split": 4}
 
 EXPORTED = ("conv2d_desc_create", "conv2d_desc_set_input_layout", "conv2d_desc_set_output_dtype",
             "conv2d_desc_set_bias", "conv2d_desc_set_tuning", "conv2d_packed_filter_bytes", "conv2d_pack_filter",
@@ -111,7 +111,7 @@ def conv2d_desc_set_bias(desc: int, bias: int):
 
 
 def conv2d_desc_set_tuning(desc: int, knob, value: int):
-    """Pipeline knob for ablations: "stages", "sync_copies", "raster", "no_resident", "no_split"."""
+    """Pipeline knob for ablations: "stages", "sync_copies", "raster", "no_resident", "split"."""
     k = TUNING[knob] if isinstance(knob, str) else int(knob)
     _check(load().conv2d_desc_set_tuning(desc, k, int(value)), "conv2d_desc_set_tuning")
 

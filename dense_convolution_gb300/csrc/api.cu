@@ -204,15 +204,15 @@ conv2d_status finalize(conv2d_desc& d) {
         d.ws_input_off = d.ws_input ? align_up(d.ws_weights, 1024) : 0;
         d.ws_total = d.ws_input ? d.ws_input_off + d.ws_input : d.ws_weights;
     }
-    // Split tail (tensor-core modes that take the im2col, padded or window
-    // source): room for the partial sums of grid - 1 share boundaries on the
+    // Split tail (opt-in; tensor-core modes that take the im2col, padded or
+    // window source): room for the partial sums of grid - 1 share boundaries on the
     // current device (a 148-SM one when there is none), when the tile groups
     // leave the last wave short and the total stays within the im2win tensor
     // N*Ci*Ho*(W+2p)*Kh of the im2win paper's Eq. (2).
     d.ws_split_off = d.ws_split = 0;
     const bool splittable = (d.algo == CONV2D_ALGO_IMPLICIT_TC && !d.gemm1x1) || d.algo == CONV2D_ALGO_PADDED_TC ||
                             d.algo == CONV2D_ALGO_IM2WIN_TC;
-    if (splittable && !d.tune_no_split) {
+    if (splittable && d.tune_split) {
         const size_t need = tc_split_need(d, device_sm_count());
         const double cap = 2.0 * d.N * d.Ci * d.Ho * (double)(d.W + 2 * d.p) * d.Kh;
         const size_t off = align_up(d.ws_total, 256);
@@ -304,10 +304,10 @@ CONV2D_API conv2d_status conv2d_desc_set_tuning(conv2d_desc_t d, conv2d_tuning k
             if (value < 0 || value > 1) return CONV2D_ERR_BAD_PARAM;
             d->tune_no_resident = value;
             return CONV2D_OK;
-        case CONV2D_TUNE_NO_SPLIT: {
+        case CONV2D_TUNE_SPLIT: {
             if (value < 0 || value > 1) return CONV2D_ERR_BAD_PARAM;
             conv2d_desc t = *d;
-            t.tune_no_split = value;
+            t.tune_split = value;
             const conv2d_status st = finalize(t);   // the split's workspace comes or goes
             if (st != CONV2D_OK) return st;
             *d = t;

@@ -966,15 +966,17 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                 }
             };
             // Split tail: contributor CTA c's partial accumulators are block
-            // (c - 1)*group + eg of prm.part, [pixel 0..127][channel 0..BN-1] fp32;
-            // this lane's row is pixel quarter*32 + lane.
-            const long long prow = (long long)(quarter * 32 + lane) * BN;
+            // (c - 1)*group + eg of prm.part, laid out [channel chunk of 32]
+            // [4-channel column q][pixel 0..127][4] fp32, so that a warp (32
+            // consecutive pixels) reads and writes 512 contiguous bytes per access.
+            const int pix = quarter * 32 + lane;
+            auto pidx = [&](int chunk, int q) { return ((long long)(chunk * 8 + q) * kTcBlockM + pix) * 4; };
             auto part_block = [&](int c) { return prm.part + ((long long)(c - 1) * prm.group + eg) * ((long long)kTcBlockM * BN); };
             auto flag_of = [&](int c) { return prm.flags + (long long)(c - 1) * prm.group + eg; };
             bool emit_y = true, add_parts = false;
             if (it.tg >= 0 && !it.owner) {
                 // Contributor: store the partial sums, then publish this call's epoch.
-                float* dst = part_block(blockIdx.x) + prow;
+                float* dst = part_block(blockIdx.x);
 #pragma unroll 1
                 for (int cc = 0; cc < BN / 32; cc += 2) {
                     uint32_t v0[32], v1[32];
@@ -983,8 +985,9 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                     tmem_ld_wait();
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        reinterpret_cast<uint4*>(dst + cc * 32)[q] = make_uint4(v0[4 * q], v0[4 * q + 1], v0[4 * q + 2], v0[4 * q + 3]);
-                        reinterpret_cast<uint4*>(dst + cc * 32 + 32)[q] =
+                        *reinterpret_cast<uint4*>(dst + pidx(cc, q)) =
+                            make_uint4(v0[4 * q], v0[4 * q + 1], v0[4 * q + 2], v0[4 * q + 3]);
+                        *reinterpret_cast<uint4*>(dst + pidx(cc + 1, q)) =
                             make_uint4(v1[4 * q], v1[4 * q + 1], v1[4 * q + 2], v1[4 * q + 3]);
                     }
                 }
@@ -1000,7 +1003,8 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                 bool okf = true;
                 if ((ew & 3) == 0 && lane == 0)
                     for (int c = it.c_first + 1; c < it.c_first + it.n_contrib && okf; ++c)
-                        okf = flag_wait(flag_of(c), prm.epoch, abort_flag);
+                        if (tail_begin(prm, c) < tail_begin(prm, c + 1))   // CTAs with an empty share add nothing
+                            okf = flag_wait(flag_of(c), prm.epoch, abort_flag);
                 if (!named_bar_and(1 + eg, 128, okf)) break;
                 __threadfence();
                 add_parts = true;
@@ -1013,20 +1017,23 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                 tmem_ld_32x32b_x32(t_row + (cc + 1) * 32, v1);
                 tmem_ld_wait();
                 if (add_parts) {
+                    // One 32-channel chunk at a time keeps 8 loads (32 registers) in flight.
                     for (int c = it.c_first + 1; c < it.c_first + it.n_contrib; ++c) {
-                        const float* src = part_block(c) + prow + cc * 32;
+                        if (tail_begin(prm, c) == tail_begin(prm, c + 1)) continue;
+                        const float* src = part_block(c);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const float4 a = __ldcg(reinterpret_cast<const float4*>(src) + q);
-                            const float4 b = __ldcg(reinterpret_cast<const float4*>(src + 32) + q);
-                            v0[4 * q] = __float_as_uint(__uint_as_float(v0[4 * q]) + a.x);
-                            v0[4 * q + 1] = __float_as_uint(__uint_as_float(v0[4 * q + 1]) + a.y);
-                            v0[4 * q + 2] = __float_as_uint(__uint_as_float(v0[4 * q + 2]) + a.z);
-                            v0[4 * q + 3] = __float_as_uint(__uint_as_float(v0[4 * q + 3]) + a.w);
-                            v1[4 * q] = __float_as_uint(__uint_as_float(v1[4 * q]) + b.x);
-                            v1[4 * q + 1] = __float_as_uint(__uint_as_float(v1[4 * q + 1]) + b.y);
-                            v1[4 * q + 2] = __float_as_uint(__uint_as_float(v1[4 * q + 2]) + b.z);
-                            v1[4 * q + 3] = __float_as_uint(__uint_as_float(v1[4 * q + 3]) + b.w);
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t(&v)[32] = h == 0 ? v0 : v1;
+                            float4 pa[8];
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) pa[q] = __ldcg(reinterpret_cast<const float4*>(src + pidx(cc + h, q)));
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                v[4 * q] = __float_as_uint(__uint_as_float(v[4 * q]) + pa[q].x);
+                                v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) + pa[q].y);
+                                v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) + pa[q].z);
+                                v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) + pa[q].w);
+                            }
                         }
                     }
                 }
@@ -1477,13 +1484,14 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     if (smem < kSmemLimit / 2 + 4096) smem = kSmemLimit / 2 + 4096;
     int grid = n_sm;
     if (grid > prm.n_groups) grid = prm.n_groups;
-    // Split tail: when the groups do not divide evenly over the CTAs (the last
-    // wave leaves some SMs idle for a whole group) and that costs more than
-    // 5 %, the stages of the last partial wave are spread over all CTAs.
+    // Split tail (opt-in): when the groups do not divide evenly over the CTAs
+    // (the last wave leaves some SMs idle for a whole group) and that costs
+    // more than 5 %, the stages of the last partial wave are spread over all
+    // CTAs.
     prm.split = 0;
     prm.g_dp = prm.n_groups;
     prm.t_stages = 0;
-    if ((amode == 0 || amode == 1 || amode == 2) && !d.tune_no_split && prm.n_groups > grid &&
+    if ((amode == 0 || amode == 1 || amode == 2) && d.tune_split && prm.n_groups > grid &&
         prm.n_groups % grid != 0) {
         const int waves = (prm.n_groups + grid - 1) / grid;
         const double balance = (double)prm.n_groups / grid / waves;

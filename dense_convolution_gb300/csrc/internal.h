@@ -20,7 +20,7 @@ struct conv2d_desc {
     int tune_sync_copies;     // 1: each stage's copies land before the next stage's are issued
     int tune_raster;          // tile visit order (0 channel tile fastest, 1 pixel group fastest, 2 zig-zag)
     int tune_no_resident;     // 1: never keep the whole filter slice resident in shared memory
-    int tune_no_split;        // 1: never split the last partial wave of tiles over all SMs
+    int tune_split;           // 1: split the last partial wave of tiles over all SMs (opt-in)
     bool prepacked;           // conv2d_fwd's w is the filter conv2d_pack_filter wrote (no repack per call)
     // Derived geometry.
     int Ho, Wo, Wp;       // output size; padded input width W + 2p

@@ -189,19 +189,26 @@ conv2d_status conv2d_desc_set_bias(conv2d_desc_t d, const void *bias);
  *                             successive pixel groups).
  *   CONV2D_TUNE_NO_RESIDENT   1 = never keep the filter slice resident in
  *                             shared memory (tensor cores); 0 = automatic.
- *   CONV2D_TUNE_NO_SPLIT      1 = take the last, partial wave of output tiles
- *                             whole; 0 = automatic: when the tiles do not
- *                             divide evenly over the SMs, the filter-tap range
- *                             of the last wave is split evenly over all SMs and
- *                             the partial sums are added before the epilogue
- *                             (the sum's order changes, not its terms).
+ *   CONV2D_TUNE_SPLIT         1 = when the output tiles do not divide evenly
+ *                             over the SMs, split the filter-tap stages of the
+ *                             last, partial wave evenly over all SMs; each
+ *                             tile's first SM adds the others' fp32 partial
+ *                             sums (published through the workspace) before
+ *                             its epilogue, so only the order of the sum
+ *                             changes.  Needs more workspace (fp32 partials
+ *                             for up to one tile per SM; conv2d_workspace_size
+ *                             includes it when the split will run and the
+ *                             total stays within the im2win tensor).  0 = the
+ *                             last wave takes whole tiles (default: the split
+ *                             measured no faster on GB300, see the design
+ *                             notes).
  * Errors: NULL_PTR, BAD_PARAM (unknown knob or value out of range). */
 typedef enum {
     CONV2D_TUNE_STAGES = 0,
     CONV2D_TUNE_SYNC_COPIES = 1,
     CONV2D_TUNE_RASTER = 2,
     CONV2D_TUNE_NO_RESIDENT = 3,
-    CONV2D_TUNE_NO_SPLIT = 4
+    CONV2D_TUNE_SPLIT = 4
 } conv2d_tuning;
 conv2d_status conv2d_desc_set_tuning(conv2d_desc_t d, conv2d_tuning knob, int value);
 

@@ -36,7 +36,7 @@ def to_device(arr, dtype):
     return torch.from_numpy(np.ascontiguousarray(arr)).cuda()
 
 
-def run_gpu(X, W, s, p, dtype, algo="auto", layout="nchw", poison=True, guard=True):
+def run_gpu(X, W, s, p, dtype, algo="auto", layout="nchw", poison=True, guard=True, tuning=None):
     """Run one convolution through the C ABI.  Returns (y float64 numpy,
     algo used, workspace bytes).  The output is pre-filled with NaN and the
     workspace is followed by a guard region that must stay untouched."""
@@ -48,7 +48,7 @@ def run_gpu(X, W, s, p, dtype, algo="auto", layout="nchw", poison=True, guard=Tr
         xd = xd.permute(0, 2, 3, 1).contiguous()
     N, Ci, H, Wd = X.shape
     Co, _, Kh, Kw = W.shape
-    op = Conv2d(N, Ci, H, Wd, Co, Kh, Kw, s, p, dtype, algo, layout)
+    op = Conv2d(N, Ci, H, Wd, Co, Kh, Kw, s, p, dtype, algo, layout, tuning=tuning)
     y = op.alloc_output()
     if poison:
         y.fill_(float("nan"))

@@ -277,7 +277,7 @@ def test_tuning_knobs_ranges(capi):
     try:
         for knob, good, bad in (("stages", (0, 1, 2, 8), (-1, 9)), ("sync_copies", (0, 1), (2, -1)),
                                 ("raster", (0, 1, 2), (3, -1)), ("no_resident", (0, 1), (2,)),
-                                ("no_split", (0, 1, 0), (2,))):
+                                ("split", (0, 1, 0), (2,))):
             for v in good:
                 capi.conv2d_desc_set_tuning(d, knob, v)
             for v in bad:
@@ -337,15 +337,16 @@ def test_prepacked_filter_workspace_and_launches(capi, shape, dtype, algo):
 
 
 def test_split_tail_workspace(capi):
-    """The split tail reserves its partial sums at the end of the workspace;
-    switching it off gives the space back."""
+    """The opt-in split tail reserves its partial sums at the end of the
+    workspace; switching it off gives the space back."""
     d = capi.conv2d_desc_create(64, 512, 28, 28, 512, 3, 3, 1, 1, "f16", "implicit_tc")
     try:
-        with_split = capi.conv2d_workspace_size(d)
-        capi.conv2d_desc_set_tuning(d, "no_split", 1)
         without = capi.conv2d_workspace_size(d)
-        assert without == 64 * 28 * 28 * 512 * 2 + 512 * 9 * 512 * 2 and with_split > without
-        capi.conv2d_desc_set_tuning(d, "no_split", 0)
-        assert capi.conv2d_workspace_size(d) == with_split
+        assert without == 64 * 28 * 28 * 512 * 2 + 512 * 9 * 512 * 2
+        capi.conv2d_desc_set_tuning(d, "split", 1)
+        with_split = capi.conv2d_workspace_size(d)
+        assert with_split > without
+        capi.conv2d_desc_set_tuning(d, "split", 0)
+        assert capi.conv2d_workspace_size(d) == without
     finally:
         capi.conv2d_desc_destroy(d)

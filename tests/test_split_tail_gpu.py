@@ -1,4 +1,4 @@
-"""The split tail: when the tile groups of a call do not divide evenly over the
+"""The split tail (opt-in, CONV2D_TUNE_SPLIT): when the tile groups of a call do not divide evenly over the
 SMs, the filter-tap stages of the last partial wave are spread over all CTAs;
 each group's first CTA adds the other CTAs' fp32 partial sums (published with
 a per-call epoch flag) before its epilogue.  Only the summation order changes:
@@ -33,8 +33,8 @@ def _split_bytes(shape, dtype, algo):
     d = capi.conv2d_desc_create(*shape, dtype, algo)
     try:
         a = capi.conv2d_workspace_size(d)
-        capi.conv2d_desc_set_tuning(d, "no_split", 1)
-        return a - capi.conv2d_workspace_size(d)
+        capi.conv2d_desc_set_tuning(d, "split", 1)
+        return capi.conv2d_workspace_size(d) - a
     finally:
         capi.conv2d_desc_destroy(d)
 
@@ -46,6 +46,7 @@ CASES = [
     ((16, 128, 64, 64, 128, 3, 1, 1), "f16", "padded_tc"),       # the K3 sweep layer, halo mode
     ((16, 128, 64, 64, 128, 7, 1, 3), "f16", "implicit_tc"),     # the K7 sweep layer
     ((16, 64, 56, 56, 64, 3, 1, 1), "f16", "padded_tc"),         # 64-wide channel tiles, resident filter
+    ((10, 128, 64, 64, 128, 3, 1, 1), "f16", "padded_tc"),       # under one stage per CTA: empty shares
 ]
 
 
@@ -59,7 +60,7 @@ def test_split_tail_whole_output(case):
     X, X64 = synth.round_to(synth.normal(seed, 0, (N, Ci, H, W)), dtype)
     Wt, W64 = synth.round_to(synth.normal(seed, 1, (Co, Ci, K, K), (2.0 / (Ci * K * K)) ** 0.5), dtype)
     Y, S = oracle_full(X64, W64, s, p)
-    y, used, _ = run_gpu(X, Wt, s, p, dtype, algo)
+    y, used, _ = run_gpu(X, Wt, s, p, dtype, algo, tuning={"split": 1})
     assert np.all(np.isfinite(y))
     err, bad0 = parity(y, Y, S)
     assert bad0 == 0 and err <= TOL[dtype], (case, err)
@@ -74,7 +75,7 @@ def test_split_tail_small_integers_bit_exact():
     Y, _ = oracle_full(d["X64"], d["W64"], s, p)
     assert np.max(np.abs(Y)) < 2048
     expect = torch.from_numpy(Y.astype(np.float32)).half().double().numpy()
-    y, _, _ = run_gpu(d["X"], d["W"], s, p, "f16", "implicit_tc")
+    y, _, _ = run_gpu(d["X"], d["W"], s, p, "f16", "implicit_tc", tuning={"split": 1})
     mism = np.argwhere(y != expect)
     assert mism.size == 0, mism[:5].tolist()
 
@@ -85,8 +86,8 @@ def test_split_matches_unsplit_and_repeats():
     wl = synth.WORKLOADS["vgg"]
     d = synth.make_inputs(wl, "f16", N=26)
     x, w = torch.from_numpy(d["X"]).cuda(), torch.from_numpy(d["W"]).cuda()
-    split = Conv2d(26, 512, 28, 28, 512, 3, 3, 1, 1, "f16", "implicit_tc")
-    plain = Conv2d(26, 512, 28, 28, 512, 3, 3, 1, 1, "f16", "implicit_tc", tuning={"no_split": 1})
+    split = Conv2d(26, 512, 28, 28, 512, 3, 3, 1, 1, "f16", "implicit_tc", tuning={"split": 1})
+    plain = Conv2d(26, 512, 28, 28, 512, 3, 3, 1, 1, "f16", "implicit_tc")
     ws = split.alloc_workspace()
     ys = []
     for _ in range(2):                  # same workspace: the first call's flags hold the older epoch
