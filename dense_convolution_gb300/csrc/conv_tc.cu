@@ -140,8 +140,10 @@ __device__ __forceinline__ int tail_cta(const TcParams& prm, long long x) {
 }
 
 // Item `idx` of this CTA (false when there is none): first its whole groups,
-// g = blockIdx.x + i*gridDim.x below g_dp, then the group pieces of its share
-// of the tail in stage order.  Every role of the CTA walks the same items.
+// g = blockIdx.x + i*gridDim.x below g_dp, then (SPLIT kernels) the group
+// pieces of its share of the tail in stage order.  Every role of the CTA
+// walks the same items.
+template <bool SPLIT>
 __device__ __forceinline__ bool tc_item(const TcParams& prm, int idx, TcItem& it) {
     const int n_dp = prm.g_dp > (int)blockIdx.x ? (prm.g_dp - (int)blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     if (idx < n_dp) {
@@ -149,6 +151,9 @@ __device__ __forceinline__ bool tc_item(const TcParams& prm, int idx, TcItem& it
         it.k0 = 0; it.k1 = prm.n_sp; it.owner = 1; it.n_contrib = 1; it.c_first = blockIdx.x; it.tg = -1;
         return true;
     }
+    if constexpr (!SPLIT) {
+        return false;
+    } else {
     if (!prm.split) return false;
     const long long b0 = tail_begin(prm, blockIdx.x), b1 = tail_begin(prm, blockIdx.x + 1);
     const long long tg = b0 / prm.n_sp + (idx - n_dp);
@@ -163,6 +168,7 @@ __device__ __forceinline__ bool tc_item(const TcParams& prm, int idx, TcItem& it
     it.n_contrib = c_last - c_first + 1;
     it.c_first = c_first;
     return true;
+    }
 }
 
 // Tile group g -> (channel tile nt, pixel group mg) in the chosen raster order.
@@ -425,7 +431,7 @@ __device__ __forceinline__ void build_halo_stage(const TcParams& prm, int tw, in
 // a 128x64x16 MMA executes in 32: two issuers keep narrow tiles fed.  When the
 // whole filter slice fits (one channel tile), it is loaded once per CTA and
 // stays resident, and stages carry A only.
-template <int BN, bool BF16, int MODE>
+template <int BN, bool BF16, int MODE, bool SPLIT>
 __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __grid_constant__ CUtensorMap amap,
                                                                 const __grid_constant__ CUtensorMap bmap,
                                                                 const __grid_constant__ CUtensorMap ymap,
@@ -512,7 +518,7 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
             long long issued = 0;
             bool free_now = false;
             TcItem it;
-            for (int idx = 0; ok && tc_item(prm, idx, it); ++idx) {
+            for (int idx = 0; ok && tc_item<SPLIT>(prm, idx, it); ++idx) {
                 const int g = it.g;
                 if constexpr (MODE == 4) {
                     // A is built by the halo builders; only filter chunks stream
@@ -641,7 +647,7 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
             if (prm.b_res && !mbar_wait(bres_bar, 0, abort_flag)) ok = false;
             const uint32_t bres_base = smem_addr(smem + prm.b_res_off);
             TcItem it;
-            for (int idx = 0; ok && tc_item(prm, idx, it); ++idx) {
+            for (int idx = 0; ok && tc_item<SPLIT>(prm, idx, it); ++idx) {
                 const int g = it.g;
                 (void)g;
                 if (!mbar_wait(acce_bar(is, acc), acc_phase ^ 1, abort_flag)) { ok = false; break; }
@@ -761,7 +767,7 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
         int acc = 0;
         uint32_t acc_phase = 0;
         TcItem it;
-        for (int idx = 0; eg < prm.group && tc_item(prm, idx, it); ++idx) {
+        for (int idx = 0; eg < prm.group && tc_item<SPLIT>(prm, idx, it); ++idx) {
             const int g = it.g;
             const bool got = mbar_wait(accf_bar(eg, acc), acc_phase, abort_flag);
             if (!named_bar_and(1 + eg, 128, got)) break;
@@ -974,7 +980,7 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
             auto part_block = [&](int c) { return prm.part + ((long long)(c - 1) * prm.group + eg) * ((long long)kTcBlockM * BN); };
             auto flag_of = [&](int c) { return prm.flags + (long long)(c - 1) * prm.group + eg; };
             bool emit_y = true, add_parts = false;
-            if (it.tg >= 0 && !it.owner) {
+            if (SPLIT && it.tg >= 0 && !it.owner) {
                 // Contributor: store the partial sums, then publish this call's epoch.
                 float* dst = part_block(blockIdx.x);
 #pragma unroll 1
@@ -998,7 +1004,7 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                     *reinterpret_cast<volatile unsigned long long*>(flag_of(blockIdx.x)) = prm.epoch;
                 }
                 emit_y = false;
-            } else if (it.tg >= 0 && it.n_contrib > 1) {
+            } else if (SPLIT && it.tg >= 0 && it.n_contrib > 1) {
                 // Owner: wait (bounded) until every other contributor has published.
                 bool okf = true;
                 if ((ew & 3) == 0 && lane == 0)
@@ -1016,7 +1022,7 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                 tmem_ld_32x32b_x32(t_row + cc * 32, v0);
                 tmem_ld_32x32b_x32(t_row + (cc + 1) * 32, v1);
                 tmem_ld_wait();
-                if (add_parts) {
+                if (SPLIT && add_parts) {
                     // One 32-channel chunk at a time keeps 8 loads (32 registers) in flight.
                     for (int c = it.c_first + 1; c < it.c_first + it.n_contrib; ++c) {
                         if (tail_begin(prm, c) == tail_begin(prm, c + 1)) continue;
@@ -1066,7 +1072,7 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                 smem_addr(smem + prm.stg_off + kTransposerWarps * prm.n_slots * kSegBytes + tw * 128);
             const uint32_t slot_bar0 = smem_addr(&sbars[tw * kMaxSlots]);
             TcItem it;
-            for (int idx = 0; ok && tc_item(prm, idx, it); ++idx) {
+            for (int idx = 0; ok && tc_item<SPLIT>(prm, idx, it); ++idx) {
                 const int g = it.g;
                 int nt_, mg_;
                 tile_of(prm, g, nt_, mg_);
@@ -1153,7 +1159,12 @@ typedef CUresult (*PFN_encodeIm2col_t)(CUtensorMap*, CUtensorMapDataType, cuuint
 template <int BN, bool BF16, int MODE>
 static cudaError_t launch_tc_inst(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y,
                                   const TcParams& prm, int grid, int smem, cudaStream_t st) {
-    auto kern = conv_tc_kernel<BN, BF16, MODE>;
+    // The split-tail protocol is compiled only into the kernels that run it
+    // (modes 0 and 1), so the others carry none of its code or registers.
+    auto kern = conv_tc_kernel<BN, BF16, MODE, false>;
+    if constexpr (MODE == 0 || MODE == 1) {
+        if (prm.split) kern = conv_tc_kernel<BN, BF16, MODE, true>;
+    }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return launch_after(kern, dim3(grid), dim3(tc_threads<MODE>()), smem, st, a, b, y, prm);
