@@ -43,15 +43,14 @@ L2_BYTES = 129 << 20
 # DRAM bytes (read + write) per launch of the contraction kernel, from ncu
 # captures (launch lists where there is one, else the full capture; writes
 # that stay in L2 during a replay read as 0); null for workloads without such
-# a capture.  The VGG figure is from the current kernel (full-size launch);
-# the others predate this build's epilogue options and are kept as context.
+# a capture.  All from the current kernels, one full-size launch each
+# (profiles/launches_*.md).
 NCU_TRAFFIC_BYTES = {
-    ("resnet_stage1", "f16", "padded_tc"): 14.37e6,
+    ("resnet_stage1", "f16", "padded_tc"): 14.39e6,
     ("vgg", "f16", "implicit_tc"): 66.15e6,
-    ("sweep_k1", "f16", "implicit_tc"): 16.84e6,
-    ("sweep_k3", "f16", "padded_tc"): 18.73e6,
-    ("stem", "f16", "im2win_tc"): 40.34e6,
-    ("resnet_stage1", "f32", "im2win_fp32_cc"): 84.13e6,
+    ("sweep_k1", "f16", "implicit_tc"): 16.85e6,
+    ("sweep_k3", "f16", "padded_tc"): 18.75e6,
+    ("stem", "f16", "im2win_tc"): 42.14e6,
 }
 ROTATION_BYTES = 3 * L2_BYTES         # rotating sets: together at least three L2s
 
