@@ -60,6 +60,22 @@
 
 namespace conv2d_gb300 {
 
+// Division of a non-negative 31-bit integer by a divisor fixed per launch,
+// as a multiply-high, an add and a shift (Granlund and Montgomery, "Division
+// by invariant integers using multiplication", 1994): with s = ceil(log2 d)
+// and m = floor(2^32 (2^s - d) / d) + 1, x / d = (umulhi(x, m) + x) >> s.
+struct FastDiv {
+    uint32_t m, s;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+    uint32_t s = 0;
+    while ((1ull << s) < d) ++s;
+    return FastDiv{(uint32_t)(((1ull << 32) * ((1ull << s) - d)) / d + 1), s};
+}
+__device__ __forceinline__ int fdiv(const FastDiv& f, int x) {
+    return (int)((__umulhi((uint32_t)x, f.m) + (uint32_t)x) >> f.s);
+}
+
 struct TcParams {
     int M, HoWo, Ho, Wo, Co;
     int n_n_tiles;      // output-channel tiles (BN wide)
@@ -69,6 +85,7 @@ struct TcParams {
     int n_cchunks, CP, Kw, s, p;
     int amode;          // A source: 0 implicit, 1 im2win, 2 padded (1 and 2 run kernel MODE 1), 3 1x1 GEMM
     int N, Wq, HpWq;    // grid modes: batch, row pitch and image pitch of the virtual pixel grid
+    FastDiv fd_wq, fd_hpwq, fd_howo, fd_nnt;   // division by Wq, HpWq, Ho*Wo and n_n_tiles
     int vec_store;      // MODE 0: Ho*Wo % 8 == 0 (16-byte stores); MODE 1: Wo % 4 == 0 (8-byte stores); MODE 3 unused
     int kpb;            // taps per pipeline stage (halo mode), else 1
     int stages;         // depth of the shared-memory ring (<= kMaxStages)
@@ -178,7 +195,7 @@ __device__ __forceinline__ void tile_of(const TcParams& prm, int g, int& nt, int
         nt = g / prm.n_mg;
         mg = g - nt * prm.n_mg;
     } else {
-        mg = g / prm.n_n_tiles;
+        mg = fdiv(prm.fd_nnt, g);
         nt = g - mg * prm.n_n_tiles;
         if (prm.raster == 2 && (mg & 1)) nt = prm.n_n_tiles - 1 - nt;
     }
@@ -864,25 +881,25 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
             if constexpr (MODE == 1 || MODE == 4) {
                 vpc = lane & 7; vrow0 = lane >> 3;
                 const int qg = mw + 4 * vpc;
-                const int ng = qg / prm.HpWq, rg = qg - ng * prm.HpWq;
-                const int yg = rg / prm.Wq, xg = rg - yg * prm.Wq;
+                const int ng = fdiv(prm.fd_hpwq, qg), rg = qg - ng * prm.HpWq;
+                const int yg = fdiv(prm.fd_wq, rg), xg = rg - yg * prm.Wq;
                 v_ok = ng < prm.N && yg < prm.Ho && xg < prm.Wo;
                 voff = (long long)ng * prm.Co * prm.HoWo + yg * prm.Wo + xg;
                 const int qp = mw + lane;
-                const int np = qp / prm.HpWq, rp = qp - np * prm.HpWq;
-                const int yp = rp / prm.Wq, xp = rp - yp * prm.Wq;
+                const int np = fdiv(prm.fd_hpwq, qp), rp = qp - np * prm.HpWq;
+                const int yp = fdiv(prm.fd_wq, rp), xp = rp - yp * prm.Wq;
                 p_ok = np < prm.N && yp < prm.Ho && xp < prm.Wo;
                 poff = (long long)np * prm.Co * prm.HoWo + yp * prm.Wo + xp;
             } else {
                 vpc = lane & 3; vrow0 = lane >> 2;
                 const int mg = mw + 8 * vpc;
                 v_ok = mg < prm.M;
-                const int img = v_ok ? mg / prm.HoWo : 0;
+                const int img = v_ok ? fdiv(prm.fd_howo, mg) : 0;
                 const int r = v_ok ? mg - img * prm.HoWo : 0;
                 voff = ((long long)img * prm.Co) * prm.HoWo + r;
                 const int m = mw + lane;
                 p_ok = m < prm.M;
-                const int imgp = p_ok ? m / prm.HoWo : 0;
+                const int imgp = p_ok ? fdiv(prm.fd_howo, m) : 0;
                 const int rp = p_ok ? m - imgp * prm.HoWo : 0;
                 poff = ((long long)imgp * prm.Co) * prm.HoWo + rp;
             }
@@ -890,62 +907,63 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                 if (BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(f));
                 return __half_as_ushort(__float2half_rn(f));
             };
-            // Register j of a chunk is channel cob + j of this lane's pixel; the
-            // bias of channel cob + lane is loaded by lane `lane` and broadcast.
-            auto emit = [&](const uint32_t (&v)[32], int cc) {
-                const int cob = n0 + cc * 32;
-                float f[32];
-                float bl = 0.f;
-                if (prm.bias && cob + lane < prm.Co) bl = load_bias<BF16>(prm.bias, cob + lane);
+            // Register j of a chunk is channel cob + j of this lane's pixel.
+            // fp32 output: 16 channels x 32 pixels (2 KB) per pass.
+            auto emit32 = [&](const uint32_t (&v)[32], int cob) {
+                float* const y32 = static_cast<float*>(prm.y);
+                float* const wf = reinterpret_cast<float*>(wst);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    f[j] = __uint_as_float(v[j]);
-                    if (prm.bias) f[j] += __shfl_sync(0xffffffffu, bl, j);
-                }
-                if (prm.out32) {
-                    // fp32 output: 16 channels x 32 pixels (2 KB) per pass.
-                    float* const y32 = static_cast<float*>(prm.y);
-                    float* const wf = reinterpret_cast<float*>(wst);
+                for (int hlf = 0; hlf < 2; ++hlf) {
+                    const int c16 = cob + hlf * 16;
+                    if (prm.vec_store) {
 #pragma unroll
-                    for (int hlf = 0; hlf < 2; ++hlf) {
-                        const int c16 = cob + hlf * 16;
-                        if (prm.vec_store) {
+                        for (int j = 0; j < 16; ++j) wf[j * 32 + lane] = __uint_as_float(v[hlf * 16 + j]);
+                        __syncwarp();
+                        if constexpr (MODE == 1 || MODE == 4) {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) wf[j * 32 + lane] = f[hlf * 16 + j];
-                            __syncwarp();
-                            if constexpr (MODE == 1 || MODE == 4) {
+                            for (int i = 0; i < 4; ++i) {
+                                const int row = vrow0 + 4 * i;
+                                if (v_ok && c16 + row < prm.Co)
+                                    *reinterpret_cast<float4*>(y32 + voff + (long long)(c16 + row) * prm.HoWo) =
+                                        *reinterpret_cast<const float4*>(wf + row * 32 + 4 * vpc);
+                            }
+                        } else {
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    const int row = vrow0 + 4 * i;
-                                    if (v_ok && c16 + row < prm.Co)
-                                        *reinterpret_cast<float4*>(y32 + voff + (long long)(c16 + row) * prm.HoWo) =
-                                            *reinterpret_cast<const float4*>(wf + row * 32 + 4 * vpc);
-                                }
-                            } else {
-#pragma unroll
-                                for (int i = 0; i < 2; ++i) {
-                                    const int row = vrow0 + 8 * i;
-                                    if (v_ok && c16 + row < prm.Co) {
-                                        float4* dst = reinterpret_cast<float4*>(y32 + voff + (long long)(c16 + row) * prm.HoWo);
-                                        const float4* src = reinterpret_cast<const float4*>(wf + row * 32 + 8 * vpc);
-                                        dst[0] = src[0];
-                                        dst[1] = src[1];
-                                    }
+                            for (int i = 0; i < 2; ++i) {
+                                const int row = vrow0 + 8 * i;
+                                if (v_ok && c16 + row < prm.Co) {
+                                    float4* dst = reinterpret_cast<float4*>(y32 + voff + (long long)(c16 + row) * prm.HoWo);
+                                    const float4* src = reinterpret_cast<const float4*>(wf + row * 32 + 8 * vpc);
+                                    dst[0] = src[0];
+                                    dst[1] = src[1];
                                 }
                             }
-                            __syncwarp();
-                        } else if (p_ok) {
-#pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                if (c16 + j < prm.Co) y32[poff + (long long)(c16 + j) * prm.HoWo] = f[hlf * 16 + j];
                         }
+                        __syncwarp();
+                    } else if (p_ok) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (c16 + j < prm.Co) y32[poff + (long long)(c16 + j) * prm.HoWo] = __uint_as_float(v[hlf * 16 + j]);
                     }
+                }
+            };
+            auto emit = [&](uint32_t (&v)[32], int cc) {
+                const int cob = n0 + cc * 32;
+                if (prm.bias) {
+                    // The bias of channel cob + lane is loaded by lane `lane` and broadcast.
+                    const float bl = cob + lane < prm.Co ? load_bias<BF16>(prm.bias, cob + lane) : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = __float_as_uint(__uint_as_float(v[j]) + __shfl_sync(0xffffffffu, bl, j));
+                }
+                if (prm.out32) {
+                    emit32(v, cob);
                     return;
                 }
                 uint16_t* const yout = static_cast<uint16_t*>(prm.y);
                 if (prm.vec_store) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) wst[j * 32 + lane] = cvt(f[j]);
+                    for (int j = 0; j < 32; ++j) wst[j * 32 + lane] = cvt(__uint_as_float(v[j]));
                     __syncwarp();
                     if constexpr (MODE == 1 || MODE == 4) {
 #pragma unroll
@@ -968,7 +986,7 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                 } else if (p_ok) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (cob + j < prm.Co) yout[poff + (long long)(cob + j) * prm.HoWo] = cvt(f[j]);
+                        if (cob + j < prm.Co) yout[poff + (long long)(cob + j) * prm.HoWo] = cvt(__uint_as_float(v[j]));
                 }
             };
             // Split tail: contributor CTA c's partial accumulators are block
@@ -1444,6 +1462,10 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     prm.HpWq = d.Hp * d.Wq;
     prm.HoWo = d.Ho * d.Wo; prm.Ho = d.Ho; prm.Wo = d.Wo; prm.Co = d.Co;
     prm.n_n_tiles = n_n_tiles;
+    prm.fd_wq = make_fastdiv(prm.Wq > 0 ? prm.Wq : 1);
+    prm.fd_hpwq = make_fastdiv(prm.HpWq > 0 ? prm.HpWq : 1);
+    prm.fd_howo = make_fastdiv(prm.HoWo > 0 ? prm.HoWo : 1);
+    prm.fd_nnt = make_fastdiv(n_n_tiles > 0 ? n_n_tiles : 1);
     prm.n_m_tiles = n_m_tiles;
     prm.group = group;
     prm.n_groups = (n_m_tiles + group - 1) / group * n_n_tiles;

@@ -27,10 +27,11 @@ static __device__ uint32_t g_device_status = 0;
 static __constant__ uint64_t g_wait_limit_ns = kWaitLimitNs;
 
 // Set this translation unit's pipeline-wait limit for kernels launched on
-// `st` after this call (0 restores the default).
+// `st` after this call (0, or anything above the default, gives the default:
+// the limit can only be lowered, so every wait stays bounded).
 static inline cudaError_t wait_limit_set(cudaStream_t st, uint64_t ns) {
     static uint64_t v;   // the copy reads the source when the stream reaches it
-    v = ns ? ns : kWaitLimitNs;
+    v = (ns == 0 || ns > kWaitLimitNs) ? kWaitLimitNs : ns;
     cudaError_t e = cudaMemcpyToSymbolAsync(g_wait_limit_ns, &v, sizeof(v), 0, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     return e;
@@ -115,31 +116,40 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // *abort so that the other warps of the CTA stop too.  Returns false when the
 // wait did not complete.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-    if (mbar_test_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
     const uint64_t limit = g_wait_limit_ns;
-    if (limit < kWaitLimitNs) {
-        // A lowered limit: poll without suspending and test the clock every
-        // time, so that even a wait of a few microseconds can expire.
-        for (;;) {
-            if (mbar_test_wait(bar, parity)) return true;
-            if (*abort) return false;
-            if (global_timer_ns() - t0 > limit) {
-                atomicOr(&g_device_status, kStatusTimeout);
-                *abort = 1;
-                return false;
+    if (limit >= kWaitLimitNs) {
+        // Default limit: try_wait may suspend the thread for a hardware time
+        // slice, which covers nearly every pipeline wait; the clock is read
+        // only once 256 slices have passed, and then every 256 more.
+        bool started = false;
+        uint64_t t0 = 0;
+        for (uint32_t i = 1;; ++i) {
+            if (mbar_try_wait(bar, parity)) return true;
+            if ((i & 255u) == 0) {
+                if (*abort) return false;
+                const uint64_t t = global_timer_ns();
+                if (!started) {
+                    started = true;
+                    t0 = t;
+                } else if (t - t0 > limit) {
+                    atomicOr(&g_device_status, kStatusTimeout);
+                    *abort = 1;
+                    return false;
+                }
             }
         }
     }
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0) {
-            if (*abort) return false;
-            if (global_timer_ns() - t0 > limit) {
-                atomicOr(&g_device_status, kStatusTimeout);
-                *abort = 1;
-                return false;
-            }
+    // A lowered limit: poll without suspending and test the clock every time,
+    // so that even a wait of a few nanoseconds can expire.
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > limit) {
+            atomicOr(&g_device_status, kStatusTimeout);
+            *abort = 1;
+            return false;
         }
     }
 }

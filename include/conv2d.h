@@ -337,7 +337,8 @@ conv2d_status conv2d_static_workspace_bytes(size_t *bytes);
 conv2d_status conv2d_device_status(void *stream, uint32_t *code_out);
 
 /* Limit, in nanoseconds, of each pipeline wait of the library's kernels on
- * the current device (default 2 s; ns = 0 restores the default), for
+ * the current device (default 2 s, which is also the maximum: ns = 0 or a
+ * value above it gives the default), for
  * kernels launched on `stream` after this call returns (the call
  * synchronises `stream`).  A wait that runs past the limit gives up: the
  * kernel lets the copies and MMAs it already issued finish, exits, and sets
