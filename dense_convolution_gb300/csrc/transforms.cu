@@ -147,9 +147,15 @@ __global__ void __launch_bounds__(256) nchw_to_nhwc16_kernel(const uint16_t* __r
     pdl_wait();   // complete only after the filter repack launched before us
 }
 
+static cudaError_t launch_padded_reg(const void* x, void* out, int N, int C, int C8, int H, int W, int Hp, int Wq,
+                                     int p, cudaStream_t st, bool pdl);
+
 cudaError_t launch_nchw_to_nhwc16(const void* x, void* out, int N, int C, int H, int W, int C8, cudaStream_t st,
                                   bool pdl) {
     const int P = H * W;
+    // The image plane as one row of P columns, no padding.
+    const cudaError_t r = launch_padded_reg(x, out, N, C, C8, 1, P, 1, P, 0, st, pdl);
+    if (r != cudaErrorNotSupported) return r;
     const int vec_ok = (P % 8 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) ? 1 : 0;
     dim3 grid((P + kNhwcTile - 1) / kNhwcTile, (C8 + kNhwcTile - 1) / kNhwcTile, N);
     if (grid.z > 65535 || grid.y > 65535) return cudaErrorInvalidConfiguration;
@@ -225,7 +231,109 @@ __global__ void __launch_bounds__(256) nchw_to_padded_nhwc16_kernel(const uint16
     pdl_wait();   // complete only after the filter repack launched before us
 }
 
+// Register-transposing variant for W % V == 0 (V = 8 or 4 image columns per
+// load; X aligned to 2V bytes).  A block makes one segment of one padded row
+// (n, yy) for one 64-channel chunk: lane l of warp w takes channel group
+// cg = l & 7 (8 channels) and column group 4w + (l >> 3) of the segment.  It
+// loads V columns of each of its 8 channel rows (a warp's loads of one
+// channel are 4 contiguous pieces), transposes the 8 x V block in registers
+// (byte permutes merge the two channels of a pair, pixel by pixel), and
+// stores V pixels x 8 channels as 16-byte vectors: the 8 lanes of a column
+// group write each pixel's 128 contiguous bytes.  No shared memory.  Border
+// and junk columns, padding rows and channels past C are written as zeros
+// (a padding row's columns split over its segments; the border columns of an
+// image row by its first segment).  With H = 1, Hp = 1, p = 0 and W = H*W of
+// the image it is the plain NCHW -> NHWC copy.
+template <int V>
+__global__ void __launch_bounds__(128) nchw_to_padded_nhwc16_reg_kernel(const uint16_t* __restrict__ x,
+                                                                        uint4* __restrict__ out, int C, int C8,
+                                                                        int H, int W, int Hp, int Wq, int p,
+                                                                        int n_seg) {
+    pdl_launch_dependents();
+    const int nw = blockDim.x >> 5;
+    const int seg = blockIdx.x % n_seg, yy = blockIdx.x / n_seg;
+    const long long n = blockIdx.y;
+    const int y = yy - p;
+    const int cgn = C8 / 8;                                   // 16-byte channel vectors per pixel
+    const int g0 = blockIdx.z * 8, ng = min(8, cgn - g0);     // this chunk's vectors
+    const int seg_cols = 4 * nw * V;                          // image columns per segment
+    uint4* const orow = out + (n * Hp + yy) * (long long)Wq * cgn + g0;
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    if (y < 0 || y >= H) {
+        const int xa = seg * seg_cols, xb = seg == n_seg - 1 ? Wq : min(Wq, xa + seg_cols);
+        for (int i = threadIdx.x; i < (xb - xa) * ng; i += blockDim.x)
+            orow[(long long)(xa + i / ng) * cgn + i % ng] = z;
+        pdl_wait();
+        return;
+    }
+    if (seg == 0) {
+        // Columns [0, p) and [W + p, Wq): zc < p is column zc, the others W + zc.
+        for (int i = threadIdx.x; i < (Wq - W) * ng; i += blockDim.x) {
+            const int zc = i / ng;
+            orow[(long long)(zc < p ? zc : W + zc) * cgn + i % ng] = z;
+        }
+    }
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int cg = lane & 7;
+    const int pg = seg * 4 * nw + 4 * w + (lane >> 3);
+    if (cg < ng && pg < W / V) {
+        const int c = 8 * (g0 + cg), x0 = pg * V;
+        const long long plane = (long long)H * W;
+        const uint16_t* const src0 = x + (n * C + c) * plane + (long long)y * W + x0;
+        uint32_t r[8][V / 2];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (c + k < C) {
+                if constexpr (V == 8) {
+                    const uint4 t = __ldg(reinterpret_cast<const uint4*>(src0 + k * plane));
+                    r[k][0] = t.x; r[k][1] = t.y; r[k][2] = t.z; r[k][3] = t.w;
+                } else {
+                    const uint2 t = __ldg(reinterpret_cast<const uint2*>(src0 + k * plane));
+                    r[k][0] = t.x; r[k][1] = t.y;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < V / 2; ++j) r[k][j] = 0;
+            }
+        }
+        // Word j of channel row k holds pixels 2j (low half) and 2j + 1.
+        uint4* dst = orow + (long long)(x0 + p) * cgn + cg;
+#pragma unroll
+        for (int j = 0; j < V / 2; ++j) {
+            uint32_t lo[4], hi[4];
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                lo[kk] = __byte_perm(r[2 * kk][j], r[2 * kk + 1][j], 0x5410);   // pixel 2j: channels 2kk, 2kk+1
+                hi[kk] = __byte_perm(r[2 * kk][j], r[2 * kk + 1][j], 0x7632);   // pixel 2j + 1
+            }
+            dst[(long long)(2 * j) * cgn] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            dst[(long long)(2 * j + 1) * cgn] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        }
+    }
+    pdl_wait();   // complete only after the filter repack launched before us
+}
+
+// Launch of the register-transposing copy, or cudaErrorNotSupported when the
+// shape or the alignment does not allow it.
+static cudaError_t launch_padded_reg(const void* x, void* out, int N, int C, int C8, int H, int W, int Hp, int Wq,
+                                     int p, cudaStream_t st, bool pdl) {
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x);
+    const int v = (W % 8 == 0 && (xa & 15) == 0) ? 8 : ((W % 4 == 0 && (xa & 7) == 0) ? 4 : 0);
+    if (!v || N > 65535 || C8 % 8 != 0 || (C8 + 63) / 64 > 65535) return cudaErrorNotSupported;
+    const int n_pg = W / v;
+    const int nw = n_pg <= 4 ? 1 : (n_pg <= 8 ? 2 : 4);       // warps per block: 4 column groups each
+    const int n_seg = (n_pg + 4 * nw - 1) / (4 * nw);
+    const long long gx = (long long)Hp * n_seg;
+    if (gx > 0x7fffffffLL) return cudaErrorNotSupported;
+    const dim3 grid((unsigned)gx, (unsigned)N, (unsigned)((C8 + 63) / 64));
+    auto kern = v == 8 ? nchw_to_padded_nhwc16_reg_kernel<8> : nchw_to_padded_nhwc16_reg_kernel<4>;
+    return launch_chain(pdl, kern, grid, dim3(32 * nw), 0, st, static_cast<const uint16_t*>(x),
+                        static_cast<uint4*>(out), C, C8, H, W, Hp, Wq, p, n_seg);
+}
+
 cudaError_t launch_nchw_to_padded_nhwc16(const void* x, void* out, const conv2d_desc& d, cudaStream_t st, bool pdl) {
+    const cudaError_t r = launch_padded_reg(x, out, d.N, d.Ci, d.Ci8, d.H, d.W, d.Hp, d.Wq, d.p, st, pdl);
+    if (r != cudaErrorNotSupported) return r;
     const int n_xt = (d.Wq + kRowTileX - 1) / kRowTileX;
     const long long gx = (long long)n_xt * d.Hp;
     const int vec_ok = (d.W % 8 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) ? 1 : 0;
