@@ -304,6 +304,10 @@ CONV2D_API conv2d_status conv2d_desc_set_tuning(conv2d_desc_t d, conv2d_tuning k
             if (value < 0 || value > 1) return CONV2D_ERR_BAD_PARAM;
             d->tune_no_resident = value;
             return CONV2D_OK;
+        case CONV2D_TUNE_EPI_GROUPS:
+            if (value != 0 && value != 2 && value != 3) return CONV2D_ERR_BAD_PARAM;
+            d->tune_epi_groups = value;
+            return CONV2D_OK;
         case CONV2D_TUNE_SPLIT: {
             if (value < 0 || value > 1) return CONV2D_ERR_BAD_PARAM;
             conv2d_desc t = *d;

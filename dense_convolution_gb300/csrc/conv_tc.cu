@@ -93,6 +93,9 @@ struct TcParams {
     int a_bytes;        // one A region: a 128-row chunk, or a halo of 128 + kpb - 1 rows
     int n_sp;           // pipeline stages per tile group
     int n_acc;          // TMEM accumulators per issuer (BN columns each)
+    int n_egroups;      // epilogue groups of four warps: 2 (group e drains issuer e), or 3 with n_acc == 3
+                        // (group e drains both tiles of the items idx with idx % 3 == e)
+    int epi_bytes;      // epilogue staging: 4 * n_egroups warps
     int taps;           // filter taps of the repacked filter
     int b_res;          // 1: the whole filter slice of the (single) channel tile stays in shared memory
     int b_res_off;      // byte offsets in the aligned dynamic shared memory
@@ -216,14 +219,18 @@ constexpr int kEpiWarpBytes = 32 * 32 * 2;                       // epilogue sta
 constexpr int kEpiBytes = 2 * 4 * kEpiWarpBytes;                 // two epilogue groups of four warps
 constexpr int kEpi1x1WarpBytes = 32 * 64 * 2;                      // MODE 3: one 32 ch x 64 px store box per warp
 constexpr int kEpi1x1Bytes = 2 * 4 * kEpi1x1WarpBytes;
-template <int MODE>
-__host__ __device__ constexpr int epi_bytes() { return MODE == 3 ? kEpi1x1Bytes : kEpiBytes; }
 constexpr int kBarBytes = 512;
 constexpr int kTcThreads = 32 * (1 + kIssuers + 8);              // producer, issuers, 8 epilogue warps
 constexpr int kTransposerWarps = 4;                              // MODE 4: halo builders
 constexpr int kMaxAStages = 4;
 template <int MODE>
 __host__ __device__ constexpr int tc_threads() { return kTcThreads + (MODE == 4 ? 32 * kTransposerWarps : 0); }
+// Launch bound: modes 0 and 1 (without the split protocol) may run a third
+// epilogue group of four warps.
+template <int MODE, bool SPLIT>
+__host__ __device__ constexpr int tc_max_threads() {
+    return ((MODE == 0 || MODE == 1) && !SPLIT) ? kTcThreads + 32 * 4 : tc_threads<MODE>();
+}
 
 template <int BN>
 struct TcConfig {
@@ -449,7 +456,7 @@ __device__ __forceinline__ void build_halo_stage(const TcParams& prm, int tw, in
 // whole filter slice fits (one channel tile), it is loaded once per CTA and
 // stays resident, and stages carry A only.
 template <int BN, bool BF16, int MODE, bool SPLIT>
-__global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __grid_constant__ CUtensorMap amap,
+__global__ void __launch_bounds__(tc_max_threads<MODE, SPLIT>(), 1) conv_tc_kernel(const __grid_constant__ CUtensorMap amap,
                                                                 const __grid_constant__ CUtensorMap bmap,
                                                                 const __grid_constant__ CUtensorMap ymap,
                                                                 const TcParams prm) {
@@ -459,7 +466,7 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
     // 128-byte swizzled operand tiles need 1024-byte alignment.  (Offsetting
     // the shared array itself keeps pointers in the shared address space.)
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + prm.epi_off + epi_bytes<MODE>());
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + prm.epi_off + prm.epi_bytes);
     // bars: [0, S) full, [S, 2S) empty, then per issuer i: accf[i][0..n_acc),
     // acce[i][0..n_acc), then the resident-filter barrier and kIssuers drain barriers.
     const int nacc = prm.n_acc;
@@ -477,7 +484,10 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
     auto acce_bar = [&](int is, int a) { return smem_addr(&bars[2 * S + is * 2 * nacc + nacc + a]); };
     const uint32_t bres_bar = smem_addr(&bars[2 * S + 2 * kIssuers * nacc]);
     auto drain_bar = [&](int is) { return smem_addr(&bars[2 * S + 2 * kIssuers * nacc + 1 + is]); };
-    const uint32_t tmem_cols = kIssuers * nacc * BN;
+    // Accumulators: (issuer, buffer) at column (is * nacc + a) * BN; the
+    // allocation is a power of two of at least 32 columns.
+    uint32_t tmem_cols = 32;
+    while (tmem_cols < (uint32_t)(prm.group * nacc * BN)) tmem_cols <<= 1;
 
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < S; ++i) { mbar_init(full_bar(i), 1); mbar_init(empty_bar(i), prm.group); }
@@ -765,7 +775,7 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                 mbar_drain_wait(drain_bar(is), 0);
             }
         }
-    } else if (warp < kTcThreads / 32) {
+    } else if (warp < 1 + kIssuers + 4 * prm.n_egroups) {
         // ------------------------------------------------------------ epilogue
         // Two groups of four warps; group e drains the accumulators of issuer
         // e.  Warp q of a group owns TMEM lanes 32q..32q+31, i.e. pixels
@@ -777,24 +787,35 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
         // Wo % 4 == 0).  Two chunks are loaded from TMEM per wait.  The
         // per-tile barrier only ANDs the wait results so that a group's four
         // warps leave together.
-        const int ew = warp - 1 - kIssuers;             // 0..7
-        const int eg = ew >> 2;                         // epilogue group = issuer
+        const int ew = warp - 1 - kIssuers;             // 0 .. 4 * n_egroups - 1
+        const int eg = ew >> 2;                         // epilogue group
         const int quarter = warp & 3;                   // TMEM lane quarter this warp may access
         uint16_t* wst = reinterpret_cast<uint16_t*>(smem + prm.epi_off + ew * kEpiWarpBytes);
-        int acc = 0;
-        uint32_t acc_phase = 0;
+        // Every accumulator buffer (issuer is, buffer acc) is drained by one
+        // group only, so its uses are waited for in order: with two groups,
+        // group e takes issuer e's tiles of every item; with three (n_acc = 3),
+        // group e takes both tiles of the items idx = e, e + 3, ..., whose
+        // buffer is acc = idx % 3 = e.  Use j = idx / n_acc of a buffer
+        // completes its barriers' phase j.
+        const bool by_item = prm.n_egroups == 3;
+        const int istep = by_item ? 3 : 1;
+        const int is_lo = by_item ? 0 : eg, is_hi = by_item ? prm.group : eg + 1;
         TcItem it;
-        for (int idx = 0; eg < prm.group && tc_item<SPLIT>(prm, idx, it); ++idx) {
+        bool go = by_item || eg < prm.group;
+        for (int idx = by_item ? eg : 0; go && tc_item<SPLIT>(prm, idx, it); idx += istep) {
+          const int acc = idx % nacc;
+          const uint32_t acc_phase = (uint32_t)(idx / nacc) & 1u;
+          for (int is = is_lo; is < is_hi; ++is) {
             const int g = it.g;
-            const bool got = mbar_wait(accf_bar(eg, acc), acc_phase, abort_flag);
-            if (!named_bar_and(1 + eg, 128, got)) break;
+            const bool got = mbar_wait(accf_bar(is, acc), acc_phase, abort_flag);
+            if (!named_bar_and(1 + eg, 128, got)) { go = false; break; }
             tc_fence_after();
             int nt_, mg_;
             tile_of(prm, g, nt_, mg_);
             const int n0 = nt_ * BN;
-            const int m0 = (mg_ * prm.group + eg) * kTcBlockM;
+            const int m0 = (mg_ * prm.group + is) * kTcBlockM;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                   (uint32_t)((eg * nacc + acc) * BN);
+                                   (uint32_t)((is * nacc + acc) * BN);
             if constexpr (MODE == 3) {
                 // Lane = output channel co0 + lane; columns = the tile's pixels p0..
                 // of one image.  Each 64-pixel half goes through the warp's 4 KB
@@ -995,8 +1016,8 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
             // consecutive pixels) reads and writes 512 contiguous bytes per access.
             const int pix = quarter * 32 + lane;
             auto pidx = [&](int chunk, int q) { return ((long long)(chunk * 8 + q) * kTcBlockM + pix) * 4; };
-            auto part_block = [&](int c) { return prm.part + ((long long)(c - 1) * prm.group + eg) * ((long long)kTcBlockM * BN); };
-            auto flag_of = [&](int c) { return prm.flags + (long long)(c - 1) * prm.group + eg; };
+            auto part_block = [&](int c) { return prm.part + ((long long)(c - 1) * prm.group + is) * ((long long)kTcBlockM * BN); };
+            auto flag_of = [&](int c) { return prm.flags + (long long)(c - 1) * prm.group + is; };
             bool emit_y = true, add_parts = false;
             if (SPLIT && it.tg >= 0 && !it.owner) {
                 // Contributor: store the partial sums, then publish this call's epoch.
@@ -1029,7 +1050,7 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
                     for (int c = it.c_first + 1; c < it.c_first + it.n_contrib && okf; ++c)
                         if (tail_begin(prm, c) < tail_begin(prm, c + 1))   // CTAs with an empty share add nothing
                             okf = flag_wait(flag_of(c), prm.epoch, abort_flag);
-                if (!named_bar_and(1 + eg, 128, okf)) break;
+                if (!named_bar_and(1 + eg, 128, okf)) { go = false; break; }
                 __threadfence();
                 add_parts = true;
             }
@@ -1068,8 +1089,8 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acce_bar(eg, acc));
-            if (++acc == nacc) { acc = 0; acc_phase ^= 1; }
+            if (lane == 0) mbar_arrive(acce_bar(is, acc));
+          }
         }
         // MODE 3: the TMA stores of this warp complete before the CTA exits.
         if constexpr (MODE == 3) {
@@ -1081,7 +1102,7 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) conv_tc_kernel(const __
         // this warp's share of the group's halo regions, make the generic-proxy
         // stores visible to the tensor core (async proxy), arrive.
         if constexpr (MODE == 4) {
-            const int tw = warp - kTcThreads / 32;
+            const int tw = warp - kTcThreads / 32;     // (two epilogue groups in this mode)
             int a_stage = 0;
             uint32_t a_phase = 0, slot_phases = 0;
             bool ok = true;
@@ -1185,7 +1206,8 @@ static cudaError_t launch_tc_inst(const CUtensorMap& a, const CUtensorMap& b, co
     }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_after(kern, dim3(grid), dim3(tc_threads<MODE>()), smem, st, a, b, y, prm);
+    const int threads = 32 * (1 + kIssuers + 4 * prm.n_egroups) + (MODE == 4 ? 32 * kTransposerWarps : 0);
+    return launch_after(kern, dim3(grid), dim3(threads), smem, st, a, b, y, prm);
 }
 
 template <bool BF16, int MODE>
@@ -1278,8 +1300,16 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
         gemm1x1 ? d.N * n_pt : ((grid_rows ? m_end : d.N * d.Ho * d.Wo) + kTcBlockM - 1) / kTcBlockM;
     // Pairs of tiles share B and keep two MMA issuers busy; with fewer than
     // two tiles per SM, single tiles keep every SM busy instead.
-    const int group = (long long)n_m_tiles * n_n_tiles >= 2LL * n_sm ? kIssuers : 1;
-    const int epi_region = gemm1x1 ? kEpi1x1Bytes : kEpiBytes;
+    int group = (long long)n_m_tiles * n_n_tiles >= 2LL * n_sm ? kIssuers : 1;
+    // Epilogue groups: three (a third buffer of BN columns per issuer in
+    // TMEM: 2 x 3 x 64 columns with tile pairs, 1 x 3 x 128 with single tiles)
+    // where storing the output, not the MMAs, bounds the kernel.
+    int n_eg = 2;
+    if (!halo4 && !gemm1x1 && !d.tune_split && d.tune_epi_groups == 3) {
+        if (d.BN == 64 && group == kIssuers) n_eg = 3;
+        else if (d.BN <= 128) { n_eg = 3; group = 1; }
+    }
+    const int epi_region = gemm1x1 ? kEpi1x1Bytes : n_eg * 4 * kEpiWarpBytes;
     const int budget = kSmemLimit - 1024 - epi_region - kBarBytes;
     // Ring plan for a budget: halo width kpb (largest divisor of Kw leaving at
     // least 2 stages: a halo stage holds kpb taps' MMAs, so two of them keep
@@ -1345,7 +1375,7 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
         stages = d.tune_stages;
         if (!halo4) stage_bytes = group * a_rows * 128 + (b_res ? 0 : kpb * b_chunk);
     }
-    const int n_acc = 2 * kIssuers * d.BN <= 512 ? 2 : 1;
+    const int n_acc = n_eg == 3 ? 3 : (2 * kIssuers * d.BN <= 512 ? 2 : 1);
 
     CUresult r;
     if (halo4) {
@@ -1478,6 +1508,8 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     prm.a_bytes = a_rows * 128;
     prm.n_sp = halo ? d.Kh * (d.Kw / kpb) * n_cchunks : d.taps * n_cchunks;
     prm.n_acc = n_acc;
+    prm.n_egroups = n_eg;
+    prm.epi_bytes = epi_region;
     prm.taps = d.taps;
     prm.b_res = b_res ? 1 : 0;
     prm.b_res_off = stages * stage_bytes;

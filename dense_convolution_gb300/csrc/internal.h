@@ -21,6 +21,7 @@ struct conv2d_desc {
     int tune_raster;          // tile visit order (0 channel tile fastest, 1 pixel group fastest, 2 zig-zag)
     int tune_no_resident;     // 1: never keep the whole filter slice resident in shared memory
     int tune_split;           // 1: split the last partial wave of tiles over all SMs (opt-in)
+    int tune_epi_groups;      // epilogue groups of four warps: 2, 3, or 0 = automatic
     bool prepacked;           // conv2d_fwd's w is the filter conv2d_pack_filter wrote (no repack per call)
     // Derived geometry.
     int Ho, Wo, Wp;       // output size; padded input width W + 2p

@@ -202,13 +202,21 @@ conv2d_status conv2d_desc_set_bias(conv2d_desc_t d, const void *bias);
  *                             last wave takes whole tiles (default: the split
  *                             measured no faster on GB300, see the design
  *                             notes).
+ *   CONV2D_TUNE_EPI_GROUPS    warps that store the output (tensor cores,
+ *                             implicit, padded and im2win sources): 2 = two
+ *                             groups of four warps, 3 = three groups with a
+ *                             third accumulator buffer per MMA issuer (output
+ *                             tiles up to 128 channels wide; 128-wide tiles
+ *                             then run one per MMA issuer), 0 = automatic
+ *                             (default).  Ignored when the split runs.
  * Errors: NULL_PTR, BAD_PARAM (unknown knob or value out of range). */
 typedef enum {
     CONV2D_TUNE_STAGES = 0,
     CONV2D_TUNE_SYNC_COPIES = 1,
     CONV2D_TUNE_RASTER = 2,
     CONV2D_TUNE_NO_RESIDENT = 3,
-    CONV2D_TUNE_SPLIT = 4
+    CONV2D_TUNE_SPLIT = 4,
+    CONV2D_TUNE_EPI_GROUPS = 5
 } conv2d_tuning;
 conv2d_status conv2d_desc_set_tuning(conv2d_desc_t d, conv2d_tuning knob, int value);
 

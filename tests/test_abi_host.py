@@ -277,7 +277,7 @@ def test_tuning_knobs_ranges(capi):
     try:
         for knob, good, bad in (("stages", (0, 1, 2, 8), (-1, 9)), ("sync_copies", (0, 1), (2, -1)),
                                 ("raster", (0, 1, 2), (3, -1)), ("no_resident", (0, 1), (2,)),
-                                ("split", (0, 1, 0), (2,))):
+                                ("split", (0, 1, 0), (2,)), ("epi_groups", (0, 2, 3, 0), (1, 4, -1))):
             for v in good:
                 capi.conv2d_desc_set_tuning(d, knob, v)
             for v in bad:

@@ -32,12 +32,16 @@ CASES = [
     ((2, 64, 28, 28, 128, 3, 1, 1), "f16", "implicit_nchw_tc"),  # in-kernel NCHW halo
     ((2, 16, 30, 30, 40, 3, 1, 1), "f32", "im2win_fp32_cc"),     # CUDA cores
     ((2, 16, 30, 32, 40, 5, 1, 2), "f32", "implicit_fp32_cc"),
+    ((8, 3, 64, 64, 64, 3, 1, 0), "f16", "im2win_tc"),           # three-channel window, pairs, 64-wide tiles
+    ((4, 32, 40, 40, 96, 5, 1, 2), "bf16", "implicit_tc"),       # 128-wide tiles (single tiles with 3 groups)
+    ((8, 64, 56, 56, 64, 3, 1, 1), "f16", "padded_tc"),          # many pairs per CTA
 ]
 
 # (The opt-in split tail changes the summation order of the split tiles; it
 # has its own tests.)
 SETTINGS = [{"stages": 1}, {"stages": 2}, {"sync_copies": 1}, {"raster": 1}, {"raster": 2}, {"no_resident": 1},
-            {"stages": 1, "raster": 2, "sync_copies": 1}]
+            {"stages": 1, "raster": 2, "sync_copies": 1}, {"epi_groups": 2}, {"epi_groups": 3},
+            {"epi_groups": 3, "stages": 1}]
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: c[2] + "-" + "x".join(map(str, c[0])))
