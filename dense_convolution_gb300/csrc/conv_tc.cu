@@ -37,15 +37,18 @@
 // pixels: the epilogue rounds them into a swizzled shared-memory box that one
 // TMA store writes to Y.
 //
-// Warp roles (352 threads; one persistent CTA per SM):
+// Warp roles (352 threads, or 480 with a third epilogue group or the MODE 4
+// halo builders; one persistent CTA per SM):
 //   warp 0      TMA producer (one lane), STAGES-deep shared-memory ring
 //   warps 1-2   MMA issue (one lane each; warp 1 also allocates TMEM): tile i
 //               of a pair of tiles into its own TMEM accumulators
-//   warps 3-10  two epilogue groups of four warps, group e draining issuer e:
-//               tcgen05.ld of their 32-lane TMEM quarter, round to the output
-//               type, transpose through shared memory, store NCHW
-// Two TMEM accumulators per issuer (when TMEM holds them) let the epilogue of
-// one tile overlap the MMAs of the next.
+//   warps 3-10  two epilogue groups of four warps, group e draining issuer e
+//               (warps 3-14, three groups, optional: group e drains both tiles
+//               of every third item): tcgen05.ld of their 32-lane TMEM
+//               quarter, round to the output type, transpose through shared
+//               memory, store NCHW
+// Two TMEM accumulators per issuer (three with three groups; when TMEM holds
+// them) let the epilogue of one tile overlap the MMAs of the next.
 // Every wait is bounded (ptx.cuh); on a timeout the CTA drains what it issued,
 // frees its TMEM and exits with the device status word set.
 #include <cuda.h>
@@ -777,8 +780,8 @@ __global__ void __launch_bounds__(tc_max_threads<MODE, SPLIT>(), 1) conv_tc_kern
         }
     } else if (warp < 1 + kIssuers + 4 * prm.n_egroups) {
         // ------------------------------------------------------------ epilogue
-        // Two groups of four warps; group e drains the accumulators of issuer
-        // e.  Warp q of a group owns TMEM lanes 32q..32q+31, i.e. pixels
+        // Groups of four warps (which tiles a group drains: below).  Warp q
+        // of a group owns TMEM lanes 32q..32q+31, i.e. pixels
         // 32q..32q+31 of the tile, and works on its own: each 32-column chunk
         // (32 channels x its 32 pixels) is rounded, transposed through the
         // warp's 2 KB of shared memory as [channel][pixel] and written as
