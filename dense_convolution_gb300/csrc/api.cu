@@ -22,6 +22,31 @@ bool is_tc(conv2d_algo a) {
 
 // Padded algorithm geometry: row pitch W+2p, rounded up to 4 when Wo % 4 == 0
 // so that 4-pixel output groups never straddle a row (8-byte stores).
+// Output-channel tile width of the tensor-core kernel: 64 for Co <= 64, 128
+// for Co <= 128; wider layers take the one of 256, 176 and 128 that needs
+// the fewest waves of tile groups on this GPU, each wave weighted by the
+// group's MMA time (tiles per group x width).  A group is a pair of
+// 128-pixel tiles when there are at least two tiles per SM; ties keep the
+// wider tile.  176 = 512 / 3 rounded up to 16: three tiles of a 512-channel
+// layer instead of two (not with the split tail, whose partial blocks are
+// laid out in 64-wide pairs of chunks).
+int choose_bn(const conv2d_desc& d, int n_sm) {
+    if (d.Co <= 64) return 64;
+    if (d.Co <= 128) return 128;
+    const long long m_tiles = ((long long)d.N * d.Ho * d.Wo + kTcBlockM - 1) / kTcBlockM;
+    int best = 256;
+    long long best_t = -1;
+    for (int bn : {256, 176, 128}) {
+        if (bn == 176 && d.tune_split) continue;
+        const long long n_tiles = (d.Co + bn - 1) / bn;
+        const int group = m_tiles * n_tiles >= 2LL * n_sm ? 2 : 1;
+        const long long groups = (m_tiles + group - 1) / group * n_tiles;
+        const long long t = (groups + n_sm - 1) / n_sm * group * bn;
+        if (best_t < 0 || t < best_t) { best_t = t; best = bn; }
+    }
+    return best;
+}
+
 int padded_pitch(const conv2d_desc& d) { return d.Wo % 4 == 0 ? (d.Wp + 3) / 4 * 4 : d.Wp; }
 
 // Fraction of the padded grid's virtual pixels that are junk (not outputs).
@@ -141,7 +166,7 @@ conv2d_status finalize(conv2d_desc& d) {
         d.taps = im2win ? 1 : d.Kh * d.Kw;
         const long long chunk = im2win ? (long long)d.Kw * d.Ck : d.Ci8;
         d.CP = (int)((chunk + kTcBlockK - 1) / kTcBlockK * kTcBlockK);
-        d.BN = d.Co <= 64 ? 64 : (d.Co <= 128 ? 128 : 256);
+        d.BN = choose_bn(d, device_sm_count());
         // A 1x1 layer is a GEMM on the NCHW tensors themselves: the TMA maps
         // read X as [N][Ci][H*W] and the filter as [Co][Ci] (16-byte strides).
         d.gemm1x1 = d.algo == CONV2D_ALGO_IMPLICIT_TC && d.layout == CONV2D_LAYOUT_NCHW && d.Kh == 1 &&
@@ -154,6 +179,7 @@ conv2d_status finalize(conv2d_desc& d) {
         // == 0 for the 8-byte stores); the narrowest pitch wins.
         d.nchw_halo = false;
         if (d.algo == CONV2D_ALGO_IMPLICIT_NCHW_TC) {
+            d.BN = d.Co <= 64 ? 64 : (d.Co <= 128 ? 128 : 256);   // the in-kernel builders use these widths
             int best_v = 0, best_wq = 0;
             for (int v = 8; v >= 1; v /= 2) {
                 if (d.W % v) continue;
@@ -212,7 +238,7 @@ conv2d_status finalize(conv2d_desc& d) {
     d.ws_split_off = d.ws_split = 0;
     const bool splittable = (d.algo == CONV2D_ALGO_IMPLICIT_TC && !d.gemm1x1) || d.algo == CONV2D_ALGO_PADDED_TC ||
                             d.algo == CONV2D_ALGO_IM2WIN_TC;
-    if (splittable && d.tune_split) {
+    if (splittable && d.tune_split && d.BN % 64 == 0) {
         const size_t need = tc_split_need(d, device_sm_count());
         const double cap = 2.0 * d.N * d.Ci * d.Ho * (double)(d.W + 2 * d.p) * d.Kh;
         const size_t off = align_up(d.ws_total, 256);

@@ -235,6 +235,10 @@ __host__ __device__ constexpr int tc_max_threads() {
     return ((MODE == 0 || MODE == 1) && !SPLIT) ? kTcThreads + 32 * 4 : tc_threads<MODE>();
 }
 
+// TMEM columns between accumulators: BN rounded up to a power of two (a
+// 176-wide accumulator starts on a 256-column boundary).
+__host__ __device__ constexpr int acc_stride(int bn) { return bn <= 64 ? 64 : (bn <= 128 ? 128 : 256); }
+
 template <int BN>
 struct TcConfig {
     static constexpr int kBBytes = BN * kTcBlockK * 2;          // one BN x 64 B chunk
@@ -490,7 +494,7 @@ __global__ void __launch_bounds__(tc_max_threads<MODE, SPLIT>(), 1) conv_tc_kern
     // Accumulators: (issuer, buffer) at column (is * nacc + a) * BN; the
     // allocation is a power of two of at least 32 columns.
     uint32_t tmem_cols = 32;
-    while (tmem_cols < (uint32_t)(prm.group * nacc * BN)) tmem_cols <<= 1;
+    while (tmem_cols < (uint32_t)(prm.group * nacc * acc_stride(BN))) tmem_cols <<= 1;
 
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < S; ++i) { mbar_init(full_bar(i), 1); mbar_init(empty_bar(i), prm.group); }
@@ -682,7 +686,7 @@ __global__ void __launch_bounds__(tc_max_threads<MODE, SPLIT>(), 1) conv_tc_kern
                 (void)g;
                 if (!mbar_wait(acce_bar(is, acc), acc_phase ^ 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)((is * nacc + acc) * BN);
+                const uint32_t d_tmem = tmem_base + (uint32_t)((is * nacc + acc) * acc_stride(BN));
                 if constexpr (MODE == 4) {
                     // One A stage = this tile's halo for (channel chunk cb, filter rows
                     // kg*khg ..): tap (kh, kw) reads it from row (kh - kg*khg)*Wq + kw
@@ -818,7 +822,7 @@ __global__ void __launch_bounds__(tc_max_threads<MODE, SPLIT>(), 1) conv_tc_kern
             const int n0 = nt_ * BN;
             const int m0 = (mg_ * prm.group + is) * kTcBlockM;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                   (uint32_t)((is * nacc + acc) * BN);
+                                   (uint32_t)((is * nacc + acc) * acc_stride(BN));
             if constexpr (MODE == 3) {
                 // Lane = output channel co0 + lane; columns = the tile's pixels p0..
                 // of one image.  Each 64-pixel half goes through the warp's 4 KB
@@ -897,6 +901,9 @@ __global__ void __launch_bounds__(tc_max_threads<MODE, SPLIT>(), 1) conv_tc_kern
                 }
             } else {
             const int mw = m0 + quarter * 32;
+            // Channels this tile stores: a 176-wide tile's last 32-column chunk
+            // reaches 16 columns past it.
+            const int co_end = min(prm.Co, n0 + BN);
             // Store geometry: this lane's piece of the warp's 32 pixels (vector
             // paths) or its own pixel (scalar path), as element offsets into Y.
             bool v_ok, p_ok;
@@ -947,7 +954,7 @@ __global__ void __launch_bounds__(tc_max_threads<MODE, SPLIT>(), 1) conv_tc_kern
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 const int row = vrow0 + 4 * i;
-                                if (v_ok && c16 + row < prm.Co)
+                                if (v_ok && c16 + row < co_end)
                                     *reinterpret_cast<float4*>(y32 + voff + (long long)(c16 + row) * prm.HoWo) =
                                         *reinterpret_cast<const float4*>(wf + row * 32 + 4 * vpc);
                             }
@@ -955,7 +962,7 @@ __global__ void __launch_bounds__(tc_max_threads<MODE, SPLIT>(), 1) conv_tc_kern
 #pragma unroll
                             for (int i = 0; i < 2; ++i) {
                                 const int row = vrow0 + 8 * i;
-                                if (v_ok && c16 + row < prm.Co) {
+                                if (v_ok && c16 + row < co_end) {
                                     float4* dst = reinterpret_cast<float4*>(y32 + voff + (long long)(c16 + row) * prm.HoWo);
                                     const float4* src = reinterpret_cast<const float4*>(wf + row * 32 + 8 * vpc);
                                     dst[0] = src[0];
@@ -967,7 +974,7 @@ __global__ void __launch_bounds__(tc_max_threads<MODE, SPLIT>(), 1) conv_tc_kern
                     } else if (p_ok) {
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            if (c16 + j < prm.Co) y32[poff + (long long)(c16 + j) * prm.HoWo] = __uint_as_float(v[hlf * 16 + j]);
+                            if (c16 + j < co_end) y32[poff + (long long)(c16 + j) * prm.HoWo] = __uint_as_float(v[hlf * 16 + j]);
                     }
                 }
             };
@@ -993,7 +1000,7 @@ __global__ void __launch_bounds__(tc_max_threads<MODE, SPLIT>(), 1) conv_tc_kern
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const int row = vrow0 + 4 * i;
-                            if (v_ok && cob + row < prm.Co)
+                            if (v_ok && cob + row < co_end)
                                 *reinterpret_cast<uint2*>(yout + voff + (long long)(cob + row) * prm.HoWo) =
                                     *reinterpret_cast<const uint2*>(wst + row * 32 + 4 * vpc);
                         }
@@ -1001,7 +1008,7 @@ __global__ void __launch_bounds__(tc_max_threads<MODE, SPLIT>(), 1) conv_tc_kern
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int row = vrow0 + 8 * i;
-                            if (v_ok && cob + row < prm.Co)
+                            if (v_ok && cob + row < co_end)
                                 *reinterpret_cast<uint4*>(yout + voff + (long long)(cob + row) * prm.HoWo) =
                                     *reinterpret_cast<const uint4*>(wst + row * 32 + 8 * vpc);
                         }
@@ -1010,7 +1017,7 @@ __global__ void __launch_bounds__(tc_max_threads<MODE, SPLIT>(), 1) conv_tc_kern
                 } else if (p_ok) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (cob + j < prm.Co) yout[poff + (long long)(cob + j) * prm.HoWo] = cvt(__uint_as_float(v[j]));
+                        if (cob + j < co_end) yout[poff + (long long)(cob + j) * prm.HoWo] = cvt(__uint_as_float(v[j]));
                 }
             };
             // Split tail: contributor CTA c's partial accumulators are block
@@ -1204,7 +1211,7 @@ static cudaError_t launch_tc_inst(const CUtensorMap& a, const CUtensorMap& b, co
     // The split-tail protocol is compiled only into the kernels that run it
     // (modes 0 and 1), so the others carry none of its code or registers.
     auto kern = conv_tc_kernel<BN, BF16, MODE, false>;
-    if constexpr (MODE == 0 || MODE == 1) {
+    if constexpr ((MODE == 0 || MODE == 1) && BN % 64 == 0) {
         if (prm.split) kern = conv_tc_kernel<BN, BF16, MODE, true>;
     }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -1222,6 +1229,9 @@ static cudaError_t launch_tc_bn(int BN, const CUtensorMap& a, const CUtensorMap&
         switch (BN) {
             case 64:  return launch_tc_inst<64, BF16, MODE>(a, b, y, prm, grid, smem, st);
             case 128: return launch_tc_inst<128, BF16, MODE>(a, b, y, prm, grid, smem, st);
+            case 176:
+                if constexpr (MODE == 0 || MODE == 1) return launch_tc_inst<176, BF16, MODE>(a, b, y, prm, grid, smem, st);
+                return cudaErrorInvalidValue;
             default:  return launch_tc_inst<256, BF16, MODE>(a, b, y, prm, grid, smem, st);
         }
     }
@@ -1378,7 +1388,7 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
         stages = d.tune_stages;
         if (!halo4) stage_bytes = group * a_rows * 128 + (b_res ? 0 : kpb * b_chunk);
     }
-    const int n_acc = n_eg == 3 ? 3 : (2 * kIssuers * d.BN <= 512 ? 2 : 1);
+    const int n_acc = n_eg == 3 ? 3 : (2 * kIssuers * acc_stride(d.BN) <= 512 ? 2 : 1);
 
     CUresult r;
     if (halo4) {
@@ -1559,7 +1569,7 @@ conv2d_status launch_conv_tc(const conv2d_desc& d, const void* src, const void* 
     prm.split = 0;
     prm.g_dp = prm.n_groups;
     prm.t_stages = 0;
-    if ((amode == 0 || amode == 1 || amode == 2) && d.tune_split && prm.n_groups > grid &&
+    if ((amode == 0 || amode == 1 || amode == 2) && d.tune_split && d.BN % 64 == 0 && prm.n_groups > grid &&
         prm.n_groups % grid != 0) {
         const int waves = (prm.n_groups + grid - 1) / grid;
         const double balance = (double)prm.n_groups / grid / waves;
