@@ -21,7 +21,7 @@ ALGOS = {"auto": 0, "im2win_fp32_cc": 1, "im2win_tc": 2, "implicit_tc": 3, "impl
          "implicit_nchw_tc": 6, "winograd_fp32_cc": 7}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 LAYOUTS = {"nchw": 0, "nhwc": 1}
-TUNING = {"stages": 0, "sync_copies": 1, "raster": 2, "no_resident": 3, "split": 4, "epi_groups": 5}
+TUNING = {"stages": 0, "sync_copies": 1, "raster": 2, "no_resident": 3, "split": 4, "epi_groups": 5, "tile_n": 6}
 
 EXPORTED = ("conv2d_desc_create", "conv2d_desc_set_input_layout", "conv2d_desc_set_output_dtype",
             "conv2d_desc_set_bias", "conv2d_desc_set_tuning", "conv2d_packed_filter_bytes", "conv2d_pack_filter",

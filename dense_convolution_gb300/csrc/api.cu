@@ -166,12 +166,13 @@ conv2d_status finalize(conv2d_desc& d) {
         d.taps = im2win ? 1 : d.Kh * d.Kw;
         const long long chunk = im2win ? (long long)d.Kw * d.Ck : d.Ci8;
         d.CP = (int)((chunk + kTcBlockK - 1) / kTcBlockK * kTcBlockK);
-        d.BN = choose_bn(d, device_sm_count());
+        d.BN = d.tune_tile_n ? d.tune_tile_n : choose_bn(d, device_sm_count());
         // A 1x1 layer is a GEMM on the NCHW tensors themselves: the TMA maps
         // read X as [N][Ci][H*W] and the filter as [Co][Ci] (16-byte strides).
         d.gemm1x1 = d.algo == CONV2D_ALGO_IMPLICIT_TC && d.layout == CONV2D_LAYOUT_NCHW && d.Kh == 1 &&
                     d.Kw == 1 && d.s == 1 && d.p == 0 && d.Ci % 8 == 0 && ((long long)d.H * d.W) % 8 == 0;
         if (d.gemm1x1) d.BN = 128;   // 128 output channels x 128 pixels per MMA tile
+        if (d.BN == 176 && d.tune_split) return CONV2D_ERR_UNSUPPORTED;   // the split's partial layout
         // Implicit GEMM on NCHW input at stride 1: operand tiles are built from X
         // inside the contraction kernel (zero-padded halo over a virtual grid of
         // pitch Wq), so no copy of X is made.  Vector width: the widest that
@@ -179,7 +180,8 @@ conv2d_status finalize(conv2d_desc& d) {
         // == 0 for the 8-byte stores); the narrowest pitch wins.
         d.nchw_halo = false;
         if (d.algo == CONV2D_ALGO_IMPLICIT_NCHW_TC) {
-            d.BN = d.Co <= 64 ? 64 : (d.Co <= 128 ? 128 : 256);   // the in-kernel builders use these widths
+            if (d.tune_tile_n == 176) return CONV2D_ERR_UNSUPPORTED;   // the in-kernel builders: 64, 128, 256
+            d.BN = d.tune_tile_n ? d.tune_tile_n : (d.Co <= 64 ? 64 : (d.Co <= 128 ? 128 : 256));
             int best_v = 0, best_wq = 0;
             for (int v = 8; v >= 1; v /= 2) {
                 if (d.W % v) continue;
@@ -334,6 +336,15 @@ CONV2D_API conv2d_status conv2d_desc_set_tuning(conv2d_desc_t d, conv2d_tuning k
             if (value != 0 && value != 2 && value != 3) return CONV2D_ERR_BAD_PARAM;
             d->tune_epi_groups = value;
             return CONV2D_OK;
+        case CONV2D_TUNE_TILE_N: {
+            if (value != 0 && value != 64 && value != 128 && value != 176 && value != 256) return CONV2D_ERR_BAD_PARAM;
+            conv2d_desc t = *d;
+            t.tune_tile_n = value;
+            const conv2d_status st = finalize(t);
+            if (st != CONV2D_OK) return st;
+            *d = t;
+            return CONV2D_OK;
+        }
         case CONV2D_TUNE_SPLIT: {
             if (value < 0 || value > 1) return CONV2D_ERR_BAD_PARAM;
             conv2d_desc t = *d;

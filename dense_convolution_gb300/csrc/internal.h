@@ -22,6 +22,7 @@ struct conv2d_desc {
     int tune_no_resident;     // 1: never keep the whole filter slice resident in shared memory
     int tune_split;           // 1: split the last partial wave of tiles over all SMs (opt-in)
     int tune_epi_groups;      // epilogue groups of four warps: 2, 3, or 0 = automatic
+    int tune_tile_n;          // tensor-core channel tile width: 64, 128, 176, 256, or 0 = automatic
     bool prepacked;           // conv2d_fwd's w is the filter conv2d_pack_filter wrote (no repack per call)
     // Derived geometry.
     int Ho, Wo, Wp;       // output size; padded input width W + 2p

@@ -209,6 +209,13 @@ conv2d_status conv2d_desc_set_bias(conv2d_desc_t d, const void *bias);
  *                             tiles up to 128 channels wide; 128-wide tiles
  *                             then run one per MMA issuer), 0 = automatic
  *                             (default).  Ignored when the split runs.
+ *   CONV2D_TUNE_TILE_N        output channels per tensor-core tile: 64, 128,
+ *                             176 or 256 (176 on the implicit, padded and
+ *                             im2win sources only, not with the split), 0 =
+ *                             automatic (default: the width that needs the
+ *                             fewest waves of tile groups).  1x1 layers keep
+ *                             128.  Errors: UNSUPPORTED when the width does
+ *                             not apply to the descriptor's algorithm.
  * Errors: NULL_PTR, BAD_PARAM (unknown knob or value out of range). */
 typedef enum {
     CONV2D_TUNE_STAGES = 0,
@@ -216,7 +223,8 @@ typedef enum {
     CONV2D_TUNE_RASTER = 2,
     CONV2D_TUNE_NO_RESIDENT = 3,
     CONV2D_TUNE_SPLIT = 4,
-    CONV2D_TUNE_EPI_GROUPS = 5
+    CONV2D_TUNE_EPI_GROUPS = 5,
+    CONV2D_TUNE_TILE_N = 6
 } conv2d_tuning;
 conv2d_status conv2d_desc_set_tuning(conv2d_desc_t d, conv2d_tuning knob, int value);
 

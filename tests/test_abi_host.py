@@ -277,7 +277,8 @@ def test_tuning_knobs_ranges(capi):
     try:
         for knob, good, bad in (("stages", (0, 1, 2, 8), (-1, 9)), ("sync_copies", (0, 1), (2, -1)),
                                 ("raster", (0, 1, 2), (3, -1)), ("no_resident", (0, 1), (2,)),
-                                ("split", (0, 1, 0), (2,)), ("epi_groups", (0, 2, 3, 0), (1, 4, -1))):
+                                ("split", (0, 1, 0), (2,)), ("epi_groups", (0, 2, 3, 0), (1, 4, -1)),
+                                ("tile_n", (0, 64, 128, 176, 256, 0), (32, 192, -1))):
             for v in good:
                 capi.conv2d_desc_set_tuning(d, knob, v)
             for v in bad:
@@ -348,5 +349,35 @@ def test_split_tail_workspace(capi):
         assert with_split > without
         capi.conv2d_desc_set_tuning(d, "split", 0)
         assert capi.conv2d_workspace_size(d) == without
+    finally:
+        capi.conv2d_desc_destroy(d)
+
+
+def test_tile_width_knob_limits(capi):
+    """176-wide tiles exist on the implicit, padded and im2win sources only
+    and not with the split tail; the workspace does not depend on the width."""
+    d = capi.conv2d_desc_create(4, 64, 28, 28, 512, 3, 3, 1, 1, "f16", "implicit_tc")
+    try:
+        ws = capi.conv2d_workspace_size(d)
+        for v in (64, 128, 176, 256, 0):
+            capi.conv2d_desc_set_tuning(d, "tile_n", v)
+            assert capi.conv2d_workspace_size(d) == ws
+        capi.conv2d_desc_set_tuning(d, "tile_n", 176)
+        with pytest.raises(capi.Conv2dError) as e:
+            capi.conv2d_desc_set_tuning(d, "split", 1)
+        assert e.value.status == capi.ERR_UNSUPPORTED
+        capi.conv2d_desc_set_tuning(d, "tile_n", 0)
+        capi.conv2d_desc_set_tuning(d, "split", 1)
+        with pytest.raises(capi.Conv2dError) as e:
+            capi.conv2d_desc_set_tuning(d, "tile_n", 176)
+        assert e.value.status == capi.ERR_UNSUPPORTED
+    finally:
+        capi.conv2d_desc_destroy(d)
+    d = capi.conv2d_desc_create(2, 64, 28, 28, 512, 3, 3, 1, 1, "f16", "implicit_nchw_tc")
+    try:
+        with pytest.raises(capi.Conv2dError) as e:
+            capi.conv2d_desc_set_tuning(d, "tile_n", 176)
+        assert e.value.status == capi.ERR_UNSUPPORTED
+        capi.conv2d_desc_set_tuning(d, "tile_n", 128)
     finally:
         capi.conv2d_desc_destroy(d)

@@ -4,7 +4,7 @@ The tensor-core kernel takes tiles in pairs (two MMA issuers, two epilogue
 groups) only when a call has at least two tiles per SM; smaller calls run
 single tiles.  These cases are sized past 2 x 152 tiles so that the pair
 path, the streamed (non-resident) filter, one accumulator per issuer
-(256-wide channel tiles) and the 1x1 GEMM with pairs all run, and every
+(256- and 176-wide channel tiles) and the 1x1 GEMM with pairs all run, and every
 output element is compared with the fp64 oracle (outputs pre-filled with
 NaN, workspace guard bytes checked).  Tolerance as in the other parity tests:
 max |y - Y| / sum|x*w| <= 1e-2 for 16-bit inputs with fp32 accumulation.
@@ -44,19 +44,22 @@ PAIR_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("tile_n", [0, 256, 176])
 @pytest.mark.parametrize("shape", PAIR_SHAPES, ids=lambda s: "x".join(map(str, s[:8])))
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_pairs_whole_output(shape, dtype):
+def test_pairs_whole_output(shape, dtype, tile_n):
     N, Ci, H, W, Co, K, s, p, algos = shape
+    if tile_n and Co <= 128:
+        pytest.skip("one channel-tile width below 256 channels")
     Ho, Wo = (H + 2 * p - K) // s + 1, (W + 2 * p - K) // s + 1
-    bn = 64 if Co <= 64 else (128 if Co <= 128 else 256)
+    bn = tile_n or (64 if Co <= 64 else 128)
     assert _tiles(N, Ho, Wo, Co, bn) >= 2 * SMS
     seed = sum(shape[:8]) * 31 + len(dtype)
     X, X64 = synth.round_to(synth.normal(seed, 0, (N, Ci, H, W)), dtype)
     Wt, W64 = synth.round_to(synth.normal(seed, 1, (Co, Ci, K, K), (2.0 / (Ci * K * K)) ** 0.5), dtype)
     Y, S = oracle_full(X64, W64, s, p)
     for algo in algos:
-        y, used, _ = run_gpu(X, Wt, s, p, dtype, algo)
+        y, used, _ = run_gpu(X, Wt, s, p, dtype, algo, tuning={"tile_n": tile_n} if tile_n else None)
         assert used == algo
         assert np.all(np.isfinite(y)), (algo, "unwritten outputs")
         err, bad0 = parity(y, Y, S)
@@ -69,7 +72,7 @@ def test_workload_whole_output_with_pairs(name, n, dtype):
     """Benchmark layers at a batch large enough for pairs, automatic algorithm."""
     wl = synth.WORKLOADS[name]
     Ho, Wo = wl.out_hw()
-    bn = 64 if wl.Co <= 64 else (128 if wl.Co <= 128 else 256)
+    bn = 64 if wl.Co <= 64 else (128 if wl.Co <= 128 else 176)
     assert _tiles(n, Ho, Wo, wl.Co, bn) >= 2 * SMS
     d = synth.make_inputs(wl, dtype, N=n)
     Y, S = oracle_full(d["X64"], d["W64"], wl.stride, wl.pad)
@@ -86,8 +89,9 @@ def _exact_expected(Y, dtype):
     return t.double().numpy()
 
 
+@pytest.mark.parametrize("tile_n", [256, 176, 128])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_pairs_small_integers_bit_exact(dtype):
+def test_pairs_small_integers_bit_exact(dtype, tile_n):
     """Small integers make every order of summation exact: the pair path must
     match the oracle bit for bit after the one rounding to the output type."""
     from dense_convolution_gb300 import capi
@@ -99,7 +103,7 @@ def test_pairs_small_integers_bit_exact(dtype):
     assert np.max(np.abs(Y)) < 2048
     expect = _exact_expected(Y, dtype)
     for algo in ("implicit_tc", "padded_tc", "im2win_tc"):
-        y, _, _ = run_gpu(d["X"], d["W"], s, p, dtype, algo)
+        y, _, _ = run_gpu(d["X"], d["W"], s, p, dtype, algo, tuning={"tile_n": tile_n})
         mism = np.argwhere(y != expect)
         assert mism.size == 0, (algo, mism[:5].tolist())
     assert capi.conv2d_device_status(0) == 0

@@ -41,7 +41,7 @@ CASES = [
 # has its own tests.)
 SETTINGS = [{"stages": 1}, {"stages": 2}, {"sync_copies": 1}, {"raster": 1}, {"raster": 2}, {"no_resident": 1},
             {"stages": 1, "raster": 2, "sync_copies": 1}, {"epi_groups": 2}, {"epi_groups": 3},
-            {"epi_groups": 3, "stages": 1}]
+            {"epi_groups": 3, "stages": 1}, {"tile_n": 128}, {"tile_n": 256}, {"tile_n": 64}]
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: c[2] + "-" + "x".join(map(str, c[0])))
