@@ -26,7 +26,9 @@
 //             paper, channels-last): the whole window of output (ho, wo) is
 //             the Kw*Ck contiguous elements from column wo*s on, so the map's
 //             rows are s*Ck elements apart and overlap; one tap, K = Kw*Ck.
-// B tile (BN channels x 64 K) is a tiled TMA load of the repacked filter.
+// B tile (BN channels x 64 K) is a tiled TMA load of the repacked filter;
+// BN is 64, 128, 176 or 256 (the host picks the width with the fewest waves
+// of tile groups; a 176-wide accumulator sits on a 256-column TMEM boundary).
 //
 // 1x1 layers (stride 1, no padding; kernel MODE 3) need no transform at all:
 // per image Y[co][p] = sum_ci W[co][ci] X[ci][p] is a plain GEMM on the NCHW
