@@ -201,7 +201,9 @@ conv2d_status conv2d_desc_set_bias(conv2d_desc_t d, const void *bias);
  *                             total stays within the im2win tensor).  0 = the
  *                             last wave takes whole tiles (default: the split
  *                             measured no faster on GB300, see the design
- *                             notes).
+ *                             notes).  UNSUPPORTED while a 176-wide tile is
+ *                             requested (CONV2D_TUNE_TILE_N); the automatic
+ *                             width then keeps to 64, 128 or 256.
  *   CONV2D_TUNE_EPI_GROUPS    warps that store the output (tensor cores,
  *                             implicit, padded and im2win sources): 2 = two
  *                             groups of four warps, 3 = three groups with a
