@@ -199,9 +199,12 @@ conv2d_status conv2d_desc_set_bias(conv2d_desc_t d, const void *bias);
  *                             for up to one tile per SM; conv2d_workspace_size
  *                             includes it when the split will run and the
  *                             total stays within the im2win tensor).  0 = the
- *                             last wave takes whole tiles (default: the split
- *                             measured no faster on GB300, see the design
- *                             notes).  UNSUPPORTED while a 176-wide tile is
+ *                             last wave takes whole tiles (default: on GB300
+ *                             a last wave of whole tiles runs faster per SM
+ *                             than a full one, and the owners' additions
+ *                             give back most of the balance, so the split
+ *                             measured at best 1 % faster and often slower).
+ *                             UNSUPPORTED while a 176-wide tile is
  *                             requested (CONV2D_TUNE_TILE_N); the automatic
  *                             width then keeps to 64, 128 or 256.
  *   CONV2D_TUNE_EPI_GROUPS    warps that store the output (tensor cores,
