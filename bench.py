@@ -43,8 +43,7 @@ L2_BYTES = 129 << 20
 # DRAM bytes (read + write) per launch of the contraction kernel, from ncu
 # captures (launch lists where there is one, else the full capture; writes
 # that stay in L2 during a replay read as 0); null for workloads without such
-# a capture.  All from the current kernels, one full-size launch each
-# (profiles/launches_*.md).
+# a capture.  All from the current kernels, one full-size launch each.
 NCU_TRAFFIC_BYTES = {
     ("resnet_stage1", "f16", "padded_tc"): 14.39e6,
     ("vgg", "f16", "implicit_tc"): 64.85e6,
