@@ -103,11 +103,13 @@ bool tc_shape_ok(const conv2d_desc& d, bool im2win) {
 conv2d_algo resolve_auto(const conv2d_desc& d) {
     if (d.dtype == CONV2D_F32) return CONV2D_ALGO_IM2WIN_FP32_CC;
     if (d.layout == CONV2D_LAYOUT_NHWC) return CONV2D_ALGO_IMPLICIT_TC;
-    // Stride 1 with several taps per filter row: the padded path shares one
-    // halo operand tile among neighbouring taps, which wins unless the padded
-    // grid adds too many junk rows (measured on GB300: ResNet stage 1 and the
-    // K=3/5 sweep layers gain, 1x1 layers and VGG do not).
-    if (d.s == 1 && d.Kw >= 2 && padded_waste(d) <= 0.15 && (d.Ci + 7) / 8 * 8 >= 64)
+    // Stride 1 with two or three taps per filter row: the padded path shares
+    // one halo operand tile among neighbouring taps, which wins unless the
+    // padded grid adds too many junk rows (measured on GB300: ResNet stage 1
+    // and the K=3 sweep layer gain 2-4 %; 1x1 layers, VGG and 5-wide filters,
+    // whose halo stages grow to five taps' filter chunks, do not: the K=5
+    // sweep layer runs 7 % faster implicit).
+    if (d.s == 1 && d.Kw >= 2 && d.Kw <= 3 && padded_waste(d) <= 0.15 && (d.Ci + 7) / 8 * 8 >= 64)
         return CONV2D_ALGO_PADDED_TC;
     const bool imp_ok = tc_shape_ok(d, false), win_ok = tc_shape_ok(d, true);
     const bool small_ci = (d.Ci + 7) / 8 * 8 <= 16;

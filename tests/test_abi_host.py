@@ -74,6 +74,8 @@ def test_auto_choices_and_workspace(capi):
         "resnet_f16": ((32, 64, 56, 56, 64, 3, 3, 1, 1), "f16", "padded_tc"),
         "k1_f16": ((16, 128, 64, 64, 128, 1, 1, 1, 0), "f16", "implicit_tc"),
         "k3s2_f16": ((16, 128, 64, 64, 128, 3, 3, 2, 1), "f16", "implicit_tc"),
+        "k3_f16": ((16, 128, 64, 64, 128, 3, 3, 1, 1), "f16", "padded_tc"),
+        "k5_f16": ((16, 128, 64, 64, 128, 5, 5, 1, 2), "f16", "implicit_tc"),
         "stem_f16": ((32, 3, 224, 224, 64, 7, 7, 2, 3), "f16", "im2win_tc"),
         "vgg_bf16": ((64, 512, 28, 28, 512, 3, 3, 1, 1), "bf16", "implicit_tc"),
         "resnet_f32": ((32, 64, 56, 56, 64, 3, 3, 1, 1), "f32", "im2win_fp32_cc"),
